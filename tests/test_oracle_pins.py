@@ -1,0 +1,346 @@
+"""Pins for the CPU oracle: facts that do not come from the oracle itself.
+
+Each test checks the oracle against something the pages or the mathematics fix —
+hand-computed values, closed forms, brute-force OBS, limit cases that reduce to
+round-to-nearest, and the seeded demo printed on the AutoGPTQ page — chosen so
+that a dropped term, a wrong sign or index, or a transposed operand in the
+oracle fails at least one of them.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _damped(H, damp=0.01):
+    return O.add_damping(O.fix_dead(H), damp)
+
+
+# -------------------------------------------------------------------------- Hessian
+
+def test_hessian_by_hand():
+    # X^T X for X = [[1,2],[3,4],[0,1]] is [[10,14],[14,21]]; n = 3.
+    X = np.array([[1.0, 2.0], [3.0, 4.0], [0.0, 1.0]])
+    H = O.hessian(X)
+    np.testing.assert_array_equal(H * 3 / 2, np.array([[10.0, 14.0], [14.0, 21.0]]))
+
+
+def test_hessian_streaming_equals_one_shot():
+    X = _rng(1).standard_normal((300, 7))
+    S, n = O.hessian_accumulate([X[:128], X[128:256], X[256:]])
+    assert n == 300
+    np.testing.assert_allclose(O.hessian_from_sum(S, n), O.hessian(X), rtol=1e-13, atol=1e-14)
+
+
+def test_dead_fix_and_damping_by_hand():
+    H = np.array([[4.0, 1.0, 0.0], [1.0, 3.0, 0.0], [0.0, 0.0, 0.0]])
+    np.testing.assert_array_equal(O.dead_mask(H), [False, False, True])
+    Hf = O.fix_dead(H)
+    np.testing.assert_array_equal(Hf, [[4, 1, 0], [1, 3, 0], [0, 0, 1]])
+    Hd = O.add_damping(Hf, 0.03)          # mean diag after the fix = 8/3 -> +0.08
+    np.testing.assert_allclose(np.diag(Hd), [4.08, 3.08, 1.08], rtol=0, atol=1e-15)
+    assert Hd[0, 1] == 1.0 and Hd[1, 0] == 1.0
+
+
+def test_upper_cholesky_of_inverse_2x2_closed_form():
+    a, b, c = 5.0, 2.0, 3.0
+    det = a * c - b * b
+    u11 = np.sqrt(c / det)
+    u12 = -b / (det * u11)
+    u22 = np.sqrt(a / det - u12 ** 2)
+    U = O.upper_cholesky_of_inverse(np.array([[a, b], [b, c]]))
+    np.testing.assert_allclose(U, [[u11, u12], [0.0, u22]], rtol=1e-14, atol=1e-15)
+
+
+def test_u_rows_are_eliminated_inverse_rows():
+    # Trick 2: row j of U is row j of H_F^-1 (F = {j..d-1}) over sqrt(H_F^-1[j, j]),
+    # with H_F^-1 from successive Gaussian elimination of H^-1.
+    d = 6
+    A = _rng(2).standard_normal((40, d))
+    H = _damped(O.hessian(A))
+    U = O.upper_cholesky_of_inverse(H)
+    Hinv = np.linalg.inv(H)
+    for j in range(d):
+        row = Hinv[j, j:] / np.sqrt(Hinv[j, j])
+        np.testing.assert_allclose(U[j, j:], row, rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(U[j, :j], 0.0, atol=0)
+        Hinv = Hinv - np.outer(Hinv[:, j], Hinv[j, :]) / Hinv[j, j]
+    # and the factorisation itself: U^T U H = I, positive diagonal
+    U = O.upper_cholesky_of_inverse(H)
+    np.testing.assert_allclose(U.T @ U @ H, np.eye(d), atol=1e-12)
+    assert np.all(np.diag(U) > 0)
+
+
+# ----------------------------------------------------------------------- quantizers
+
+def test_qmax():
+    assert [O.qmax_sym(b) for b in (2, 3, 4)] == [1, 3, 7]
+    assert [O.maxq_asym(b) for b in (2, 3, 4)] == [3, 7, 15]
+
+
+def test_sym_quantizer_by_hand_half_to_even_and_clip():
+    # row max 0.875, qmax 7 -> scale 0.125 (exact in fp32); t = w / 0.125
+    w = np.array([[0.875, -0.3125, 0.1875, 0.4375, 0.0625, 1.0]])
+    s, z = O.sym_params(w[:, :5], 7)
+    assert s[0] == 0.125 and z[0] == 0
+    c = O.quant_codes(w, s[:, None], z[:, None], 4, True)
+    # 7, -2.5 -> -2, 1.5 -> 2, 3.5 -> 4, 0.5 -> 0, 8 -> clipped to 7
+    np.testing.assert_array_equal(c, [[7, -2, 2, 4, 0, 7]])
+    np.testing.assert_array_equal(O.dequant(c, s[:, None], 0, True), [[0.875, -0.25, 0.25, 0.5, 0.0, 0.875]])
+
+
+def test_sym_scale_floor_for_zero_row():
+    s, _ = O.sym_params(np.zeros((1, 4)), 7, scale_dtype=None)
+    assert s[0] == 1e-12 / 7
+
+
+def test_asym_quantizer_by_hand():
+    # 2 bits: maxq 3; min -0.5, max 1.0 -> scale 0.5, zero round(1.0) = 1
+    b = np.array([[-0.5, 1.0, 0.25, 0.0]])
+    s, z = O.asym_params(b, 3)
+    assert s[0] == 0.5 and z[0] == 1
+    c = O.quant_codes(b, s[:, None], z[:, None], 2, False)
+    np.testing.assert_array_equal(c, [[0, 3, 2, 1]])          # round(1.5) = 2 (half to even)
+    np.testing.assert_array_equal(O.dequant(c, s[:, None], z[:, None], False), [[-0.5, 1.0, 0.5, 0.0]])
+    # all-positive block: -min/scale < 0, zero clamped to 0
+    s2, z2 = O.asym_params(np.array([[0.5, 1.0]]), 3)
+    assert z2[0] == 0 and np.isclose(s2[0], 0.5 / 3, rtol=1e-7)
+    # constant block: scale 1.0
+    s3, z3 = O.asym_params(np.array([[0.25, 0.25]]), 15)
+    assert s3[0] == 1.0 and z3[0] == 0
+
+
+def test_stored_scale_is_float32_grid():
+    w = _rng(3).standard_normal((5, 9))
+    s, _ = O.sym_params(w, 7)
+    assert np.all(s.astype(np.float32).astype(np.float64) == s)
+
+
+# ----------------------------------------------------------------------------- pack
+
+def test_pack_4bit_by_hand():
+    u = np.array([[1, 2, 3, 4, 5, 6, 7, 8]])
+    np.testing.assert_array_equal(O.pack_rows(u, 4), np.array([[0x87654321]], dtype=np.uint32))
+
+
+def test_pack_2bit_by_hand():
+    u = np.zeros((1, 16), dtype=np.int64)
+    u[0, :3] = [1, 2, 3]                   # 1 + (2 << 2) + (3 << 4) = 57
+    np.testing.assert_array_equal(O.pack_rows(u, 2), [[57]])
+
+
+def test_pack_3bit_straddles_words():
+    u = np.full((1, 32), 7)
+    np.testing.assert_array_equal(O.pack_rows(u, 3), [[0xFFFFFFFF] * 3])
+    u[0, 10] = 5                           # bits 30, 31, 32 = 1, 0, 1
+    np.testing.assert_array_equal(O.pack_rows(u, 3), [[0x7FFFFFFF, 0xFFFFFFFF, 0xFFFFFFFF]])
+
+
+def test_pack_ragged_row_pads_zero_bits():
+    u = np.full((2, 5), 3)
+    w = O.pack_rows(u, 3)                  # 15 bits -> one word
+    np.testing.assert_array_equal(w, [[0b011011011011011] * 1] * 2)
+
+
+def test_g_idx_by_hand():
+    np.testing.assert_array_equal(O.g_idx_for(np.array([2, 0, 3, 1]), 2, 4), [0, 1, 0, 1])
+    np.testing.assert_array_equal(O.g_idx_for(None, 2, 5), [0, 0, 1, 1, 2])
+    np.testing.assert_array_equal(O.g_idx_for(None, 0, 3), [0, 0, 0])
+
+
+def test_act_order_perm_stable_descending():
+    np.testing.assert_array_equal(O.act_order_perm([3.0, 1.0, 3.0, 0.0, 2.0]), [0, 2, 4, 1, 3])
+
+
+# ------------------------------------------------------------------- the GPTQ loop
+
+@pytest.mark.parametrize("d,group,sym,bits", [(4, 0, True, 3), (6, 0, True, 2), (8, 0, True, 4),
+                                              (8, 4, True, 3), (8, 4, False, 4), (6, 3, False, 2)])
+def test_cholesky_loop_equals_bruteforce_obs(d, group, sym, bits):
+    """P-1/P-2: the Cholesky-form loop equals explicit OBS with Gaussian elimination,
+    and each step raises the loss by err_j^2 / 2 = e^2 / (2 Hinv_F[j, j])."""
+    rng = _rng(10 + d + group)
+    X = rng.standard_normal((3 * d, d)) @ rng.standard_normal((d, d))
+    W = rng.standard_normal((5, d)) * 0.3
+    H = _damped(O.hessian(X))
+    U = O.upper_cholesky_of_inverse(H)
+    r = O.gptq_loop(W, U, bits, group, sym)
+    for i in range(W.shape[0]):
+        q, incr = O.obs_bruteforce_row(W[i], H, bits, group, sym)
+        np.testing.assert_allclose(r["Q"][i], q, rtol=0, atol=1e-12)
+    # error increments: OBS's e^2 / (2 Hinv_F[j, j]) summed over the steps equals the
+    # loop's sum of err_j^2 / 2, row by row
+    for i in range(W.shape[0]):
+        _, incr = O.obs_bruteforce_row(W[i], H, bits, group, sym)
+        np.testing.assert_allclose(incr, 0.5 * r["err"][i] ** 2, rtol=1e-9, atol=1e-15)
+        np.testing.assert_allclose(incr.sum(), 0.5 * r["err_sq"][i], rtol=1e-10, atol=1e-15)
+
+
+@pytest.mark.parametrize("group,sym,act", [(0, True, False), (16, True, False), (16, False, False),
+                                           (16, True, True)])
+def test_total_error_closed_form(group, sym, act):
+    """P-3: per row (q - w0) H (q - w0)^T = sum_j err_j^2 with the damped, dead-fixed H."""
+    rng = _rng(20 + group)
+    d = 48
+    X = rng.standard_normal((200, d)) * np.exp(rng.standard_normal(d))
+    X[:, 5] = 0.0
+    W = rng.standard_normal((7, d)) * 0.05
+    H = O.hessian(X)
+    U, perm, dead = O.prepare(H, 0.01, act, np.diag(O.xtx(X)))
+    r = O.gptq_quantize(W, U, perm, dead, 3, group, sym)
+    W0 = W.copy()
+    W0[:, dead] = 0
+    Hp = H[perm][:, perm]
+    Hd = _damped(Hp)
+    loss = O.layer_loss(r["Wq"][:, perm], W0[:, perm], Hd)
+    np.testing.assert_allclose(loss, r["err_sq"], rtol=1e-10)
+
+
+@pytest.mark.parametrize("group,sym", [(0, True), (64, True), (64, False)])
+def test_diagonal_hessian_reduces_to_rtn_exactly(group, sym):
+    """P-4: X = Hadamard columns gives H = 2I, U diagonal, so GPTQ == RTN bit for bit."""
+    spec = synth.XSpec(n=512, d=256, kind="hadamard", dtype="f32")
+    X = synth.to_numpy_f64(synth.make_x(spec, 0))
+    H = O.hessian(X)
+    np.testing.assert_array_equal(H, 2 * np.eye(256))
+    W = synth.to_numpy_f64(synth.make_weight(128, 256, 0.1, 7))
+    U, perm, dead = O.prepare(H, 0.01, False)
+    assert np.count_nonzero(U - np.diag(np.diag(U))) == 0
+    g = O.gptq_quantize(W, U, perm, dead, 4, group, sym)
+    r = O.rtn_quantize(W, 4, group, sym)
+    np.testing.assert_array_equal(g["codes"], r["codes"])
+    np.testing.assert_array_equal(g["Wq"], r["Wq"])
+    np.testing.assert_array_equal(g["packed"], r["packed"])
+
+
+def test_heavy_damping_reduces_to_rtn():
+    """P-5 ([guide] "When it breaks"): heavy damping makes U nearly diagonal -> RTN codes."""
+    wl = synth.workload(0)
+    X = synth.to_numpy_f64(synth.make_x(wl.layers[0].x, 5))
+    W = synth.to_numpy_f64(synth.make_weight(128, 256, 0.1, 6))
+    H = O.hessian(X)
+    U, perm, dead = O.prepare(H, 1e8, False)
+    g = O.gptq_quantize(W, U, perm, dead, 4, 0, True)
+    r = O.rtn_quantize(W, 4, 0, True)
+    assert np.count_nonzero(g["codes"] != r["codes"]) == 0
+
+
+@pytest.mark.parametrize("sym", [True, False])
+def test_dead_columns_come_out_zero(sym):
+    """P-6: W[:, dead] = 0 before the loop, and the grid represents 0 exactly."""
+    spec = synth.XSpec(n=1024, d=256, kind="scaled", dtype="bf16", n_outliers=4,
+                       outlier_factor=20.0, dead_frac=0.05)
+    X = synth.to_numpy_f64(synth.make_x(spec, 11))
+    dead_expected = synth.dead_channels(spec, 11).numpy()
+    W = synth.to_numpy_f64(synth.make_weight(64, 256, 0.02, 12))
+    H = O.hessian(X)
+    U, perm, dead = O.prepare(H, 0.01, False)
+    np.testing.assert_array_equal(np.nonzero(dead)[0], dead_expected)
+    g = O.gptq_quantize(W, U, perm, dead, 4, 128, sym)
+    assert np.all(g["Wq"][:, dead] == 0.0)
+
+
+def test_gptq_output_error_below_rtn():
+    """P-7 ([loop]: output error on X well below plain rounding's), per-row scales."""
+    wl = synth.workload(0)
+    X = synth.to_numpy_f64(synth.make_x(wl.layers[0].x, synth.x_seed(0, wl.layers[0].x)))
+    W = synth.to_numpy_f64(synth.make_weight(128, 256, 0.1, synth.weight_seed(0, "w")))
+    for bits in (2, 3, 4):
+        g = O.gptq_layer(W, X, bits=bits)
+        r = O.rtn_quantize(W, bits, 0, True)
+        eg = O.rel_output_error(X, W, g["Wq"])
+        er = O.rel_output_error(X, W, r["Wq"])
+        assert eg < 0.9 * er, (bits, eg, er)
+
+
+def test_output_error_identity_through_xtx():
+    rng = _rng(4)
+    X = rng.standard_normal((50, 6))
+    W = rng.standard_normal((3, 6))
+    Q = W + 0.01 * rng.standard_normal((3, 6))
+    assert np.isclose(O.rel_output_error(X, W, Q), O.rel_output_error_from_xtx(O.xtx(X), W, Q), rtol=1e-12)
+
+
+def test_clipped_codes_stay_on_grid():
+    """[guide] "When it breaks": compensation can push weights past the row scale;
+    those are clipped to +-qmax, never beyond."""
+    rng = _rng(5)
+    X = rng.standard_normal((64, 32)) @ rng.standard_normal((32, 32))
+    W = rng.standard_normal((16, 32))
+    g = O.gptq_layer(W, X, bits=2)
+    assert g["codes"].min() >= -1 and g["codes"].max() <= 1
+
+
+def test_act_order_is_plain_loop_on_permuted_problem():
+    """P-10: act_order equals the plain loop on (W[:, perm], H[perm][:, perm]), unpermuted."""
+    rng = _rng(6)
+    d = 40
+    X = rng.standard_normal((160, d)) * np.exp(rng.standard_normal(d))
+    W = rng.standard_normal((9, d)) * 0.05
+    g = O.gptq_layer(W, X, bits=3, group=8, act_order=True)
+    perm = np.argsort(-np.diag(X.T @ X), kind="stable")
+    Hp = O.hessian(X[:, perm])
+    U2 = O.upper_cholesky_of_inverse(_damped(Hp))
+    r = O.gptq_loop(W[:, perm], U2, 3, 8, True)
+    np.testing.assert_array_equal(g["perm"], perm)
+    np.testing.assert_allclose(g["Wq"][:, perm], r["Q"], rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(g["g_idx"][perm], np.arange(d) // 8)
+
+
+# ------------------------------------------------------------ AutoGPTQ page fixture
+
+def test_auto_page_demo_printed_values():
+    """P-8: the AutoGPTQ page's seeded one-row demo prints GPTQ MSE 0.000135, naive
+    0.000086, ratio 1.56 — this pins the asymmetric quantizer (half-to-even, zero clamp,
+    group-start scale from updated weights)."""
+    torch = pytest.importorskip("torch")
+    gold = json.load(open(os.path.join(GOLDEN, "auto_demo.json")))
+    torch.manual_seed(gold["setup"]["seed"])
+    Wt = torch.randn(128, 256) * 0.1
+    Xt = torch.randn(512, 256)
+    W = Wt.double().numpy()
+    X = Xt.double().numpy()
+    Hinv = np.linalg.inv(O.auto_compute_hessian(X))
+    codes, params = O.auto_gptq_quantize_row(W[0], Hinv, 4, 128)
+    deq = O.auto_dequantize_row(codes, params, 128)
+    mse = float(np.mean((W[0] - deq) ** 2))
+    naive = O.rtn_quantize(W[:1], 4, 0, False, scale_dtype=None)
+    naive_mse = float(np.mean((W[0] - naive["Wq"][0]) ** 2))
+    p = gold["printed"]
+    assert round(mse, 6) == p["gptq_mse"]
+    assert round(naive_mse, 6) == p["naive_mse"]
+    assert round(mse / naive_mse, 2) == p["ratio"]
+
+
+# ------------------------------------------------------------ comparison machinery
+
+def test_teacher_forcing_accepts_ties_and_rejects_real_mismatches():
+    # codes decided exactly at a half-point: 0.0625 / 0.125 = 0.5 -> 0 (half-to-even)
+    W = np.array([[0.875, 0.0625, 0.3]])
+    U = np.eye(3)
+    r = O.gptq_loop(W, U, 4, 0, True)
+    assert r["codes"][0, 1] == 0
+    forced = r["codes"].copy()
+    forced[0, 1] = 1                       # the other side of the tie: accepted
+    r2 = O.gptq_loop(W, U, 4, 0, True, forced_codes=forced)
+    assert r2["codes"][0, 1] == 1 and len(r2["ties"]) == 1
+    forced = r["codes"].copy()
+    forced[0, 2] += 1                      # 0.3/0.125 = 2.4: not a tie -> rejected
+    with pytest.raises(O.TieMismatch):
+        O.gptq_loop(W, U, 4, 0, True, forced_codes=forced)
+
+
+def test_perm_equivalent():
+    keys = np.array([5.0, 3.0, 3.0000001, 1.0])
+    assert O.perm_equivalent([0, 2, 1, 3], [0, 1, 2, 3], keys, 1e-6)
+    assert not O.perm_equivalent([0, 3, 1, 2], [0, 1, 2, 3], keys, 1e-6)
