@@ -1,0 +1,514 @@
+#!/usr/bin/env python
+"""GPTQ per-layer quantization benchmark on GB300.
+
+One step = one whole layer pass of the workload: Hessian accumulate + finalize,
+prepare (dead fix, damping, act_order, U), and the GPTQ column loop + packing for
+every weight that shares the layer input. Inputs are seeded synthetic layers.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+Prints one JSON line. `value` is milliseconds per layer pass (lower is better),
+device-timed with CUDA events, L2 flushed between steps when the inputs fit in it.
+`e2e` is the same pass through the C ABI from pinned host buffers, host<->device
+copies included. `roofline` is for the kernel with the largest share of the step,
+from a second, profiled pass over the same steps. `cpu_baseline` times the CPU
+oracle on this host (test infrastructure, reported for context).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GPTQ layer quantize time (ms, incl. H+Cholesky) and % of roofline per kernel"
+L2_BYTES = 129 * 1024 * 1024
+FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x 2 flop x max SM clock
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-profile", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:  # noqa: BLE001
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:  # noqa: BLE001
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- workload
+
+class Layer:
+    def __init__(self, spec, X, Ws, names):
+        self.spec = spec
+        self.X = X
+        self.Ws = Ws
+        self.names = names
+
+
+def build_layers(cfg: int, device, host: bool = False):
+    import torch
+    import synth
+    wl = synth.workload(cfg)
+    layers = []
+    xcache = {}
+    for li, L in enumerate(wl.layers):
+        key = (L.x, li % 4 if cfg == 4 else li)
+        if key not in xcache:
+            seed = synth.x_seed(cfg, L.x) + (key[1] if cfg == 4 else 0)
+            xcache[key] = synth.make_x(L.x, seed, device=device)
+        X = xcache[key]
+        Ws = [synth.make_weight(w.out, w.inp, w.std, synth.weight_seed(cfg, w.name), device=device) for w in L.weights]
+        layers.append(Layer(L, X, Ws, [w.name for w in L.weights]))
+    return wl, layers
+
+
+class Runner:
+    """Holds preallocated outputs/workspaces so a step only enqueues library calls."""
+
+    def __init__(self, lib, layers, device):
+        import torch
+        self.lib = lib
+        self.layers = layers
+        self.dev = device
+        self.hess = {}
+        self.prep_ws = {}
+        self.q_ws = {}
+        self.outs = []
+        for L in layers:
+            d = L.X.shape[1]
+            if d not in self.hess:
+                self.hess[d] = lib.Hessian(d, device)
+                self.prep_ws[d] = torch.empty(lib.gptq_prepare_workspace_bytes(d, True), dtype=torch.uint8,
+                                              device=device)
+            q = L.spec.q
+            outs = []
+            for W in L.Ws:
+                r, c = W.shape
+                nb = lib.gptq_quantize_workspace_bytes(r, c, q.bits, q.group, q.sym)
+                if (r, c) not in self.q_ws or self.q_ws[(r, c)].numel() < nb:
+                    self.q_ws[(r, c)] = torch.empty(nb, dtype=torch.uint8, device=device)
+                G = -(-c // q.group) if q.group else 1
+                outs.append({
+                    "codes": torch.empty(r, c, dtype=torch.int8, device=device),
+                    "scales": torch.empty(r, G, dtype=torch.float32, device=device),
+                    "zeros": torch.empty(r, G, dtype=torch.uint8, device=device),
+                    "g_idx": torch.empty(c, dtype=torch.int32, device=device),
+                    "Wq": torch.empty(r, c, dtype=torch.float32, device=device),
+                    "packed": torch.empty(r, lib.gptq_packed_words_per_row(c, q.bits), dtype=torch.int32,
+                                          device=device),
+                    "row_loss": torch.empty(r, dtype=torch.float32, device=device),
+                })
+            self.outs.append(outs)
+
+    def step(self, events=None, Xs=None, Wss=None):
+        """One layer pass over every layer; `events` collects (stage, start, end) CUDA events."""
+        import torch
+        lib = self.lib
+        for li, L in enumerate(self.layers):
+            X = L.X if Xs is None else Xs[li]
+            Ws = L.Ws if Wss is None else Wss[li]
+            q = L.spec.q
+            h = self.hess[X.shape[1]]
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if events is not None else None
+            if e:
+                e[0].record()
+            h.reset()
+            h.accumulate(X)
+            H, diag, _ = h.finalize()
+            if e:
+                e[1].record()
+            U, perm, dead = lib.gptq_prepare(H, diag, q.damp, act_order=q.act_order, ws=self.prep_ws[X.shape[1]])
+            if e:
+                e[2].record()
+            for W, o in zip(Ws, self.outs[li]):
+                lib.gptq_quantize(W, U, perm, dead, q.bits, q.group, q.sym, ws=self.q_ws[tuple(W.shape)], out=o)
+            if e:
+                e[3].record()
+                events.append(e)
+        return self.outs
+
+
+def flush_l2(buf):
+    buf.zero_()
+
+
+def algorithmic(cfg_layers):
+    """Per-kernel-class algorithmic work for one step: flops or bytes, and the unit."""
+    work = {}
+
+    def add(k, v):
+        work[k] = work.get(k, 0.0) + v
+
+    NB, QB = 128, 128
+    for L in cfg_layers:
+        n, d = L.X.shape
+        add("hessian_tc_kernel", 2.0 * n * d * (d + 1) / 2)
+        # prepare: blocked Cholesky (panel TRSM + lower SYRK) and the block-row inverse
+        for k0 in range(0, d, NB):
+            nb = min(NB, d - k0)
+            m = d - k0 - nb
+            add("sgemm_kernel[prepare]", 2.0 * m * nb * nb + 2.0 * (m * (m + 1) / 2) * nb)
+            ncols = k0 + nb
+            add("sgemm_kernel[prepare]", 2.0 * nb * ncols * nb + 2.0 * m * ncols * nb)
+        for W in L.Ws:
+            r, c = W.shape
+            for j0 in range(0, c, QB):
+                bw = min(QB, c - j0)
+                add("gptq_block_kernel", 2.0 * r * bw * bw)
+                add("sgemm_kernel[trailing]", 2.0 * r * bw * (c - j0 - bw))
+            add("pack_kernel", r * c * 1.0 + r * -(-c * L.spec.q.bits // 32) * 4.0)   # bytes
+    return work
+
+
+ROOF = {  # kernel class -> (bound, unit)
+    "hessian_tc_kernel": ("tensor", "TFLOP/s"),
+    "sgemm_kernel[prepare]": ("alu", "TFLOP/s"),
+    "sgemm_kernel[trailing]": ("alu", "TFLOP/s"),
+    "gptq_block_kernel": ("alu", "TFLOP/s"),
+    "pack_kernel": ("hbm", "GB/s"),
+}
+
+
+# ------------------------------------------------------------------------- CPU oracle
+
+def oracle_pass(cfg: int, layers_host):
+    """One layer pass of the oracle (numpy fp64) over host copies of the inputs; returns
+    (ms for H + prepare, ms for the column loops + packing on the rows given)."""
+    import numpy as np
+    import oracle as O
+    t_hp = t_q = 0.0
+    for X, Ws, q in layers_host:
+        t0 = time.perf_counter()
+        S = O.xtx(X)
+        H = O.hessian_from_sum(S, X.shape[0])
+        U, perm, dead = O.prepare(H, q.damp, q.act_order, np.diag(S))
+        t1 = time.perf_counter()
+        for W in Ws:
+            O.gptq_quantize(W, U, perm, dead, q.bits, q.group, q.sym)
+        t2 = time.perf_counter()
+        t_hp += (t1 - t0) * 1e3
+        t_q += (t2 - t1) * 1e3
+    return t_hp, t_q
+
+
+def host_layers(cfg: int, layers, row_frac: float = 1.0):
+    import synth
+    out = []
+    for L in layers:
+        X = synth.to_numpy_f64(L.X)
+        Ws = [synth.to_numpy_f64(W[: max(1, int(round(W.shape[0] * row_frac)))]) for W in L.Ws]
+        out.append((X, Ws, L.spec.q))
+    return out
+
+
+def cpu_sample_desc(cfg, row_frac):
+    if row_frac >= 1.0:
+        return (f"the whole workload-{cfg} layer pass in the oracle (numpy fp64: H, inv+cholesky, column loop, "
+                "packing) on the host cores")
+    return (f"workload-{cfg} in the oracle (numpy fp64): H and inv+cholesky in full, the column loop and packing "
+            f"on the first {row_frac:.4g} of each weight's rows (rows are independent given U), loop time scaled "
+            f"by {1 / row_frac:.4g}")
+
+
+def time_oracle(cfg, layers, row_frac, reps=1):
+    hl = host_layers(cfg, layers, row_frac)
+    ts = []
+    for _ in range(reps):
+        t_hp, t_q = oracle_pass(cfg, hl)
+        ts.append(t_hp + t_q / row_frac)
+    return ts
+
+
+# oracle row fraction per workload: bounded CPU samples (roughly 3-30 s each on 8-16 cores)
+ORACLE_ROW_FRAC = {0: 1.0, 1: 0.125, 2: 1.0 / 256, 3: 1.0 / 1024, 4: 1.0 / 1024}
+CPU_BASELINE_ROW_FRAC = {0: 1.0, 1: 1.0, 2: 1.0 / 64, 3: 1.0 / 512, 4: 1.0 / 512}
+
+
+# ------------------------------------------------------------------------------ arms
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    import torch
+    cores = len(os.sched_getaffinity(0))
+    wl, layers = build_layers(args.config, "cpu")
+    frac = ORACLE_ROW_FRAC[args.config]
+    time_oracle(args.config, layers, frac, reps=min(args.warmup, 1))
+    v = statistics.mean(time_oracle(args.config, layers, frac, reps=args.steps))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "ms", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": v, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": {"workload": wl.name, "config_index": args.config},
+        "cpu_baseline": {"value": v, "unit": "ms", "cores": cores, "kind": "oracle",
+                         "sample": cpu_sample_desc(args.config, frac)},
+        "e2e": {"value": v, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    import torch.distributed as dist
+    import post_weight_quantization_04_gb300 as lib
+    from post_weight_quantization_04_gb300 import build as B
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    B.build()
+    lib.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+
+    wl, layers = build_layers(args.config, dev)
+    runner = Runner(lib, layers, dev)
+    in_bytes = sum(L.X.numel() * L.X.element_size() + sum(W.numel() * 4 for W in L.Ws) for L in layers)
+    flush = in_bytes < 2 * L2_BYTES
+    fbuf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        runner.step()
+    torch.cuda.synchronize()
+
+    clocks = Clocks(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    n0 = lib.gptq_launch_count()
+    times = []
+    t_wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        if flush:
+            flush_l2(fbuf)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        runner.step()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    torch.cuda.synchronize()
+    barrier()
+    wall = (time.perf_counter() - t_wall0) * 1e3
+    launches = lib.gptq_launch_count() - n0
+    ck = clocks.stop()
+    ms = statistics.mean(times)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- profiled pass: per-stage and per-kernel CUDA events over the same steps ----
+    stages, kernels, roof = {}, {}, None
+    if not args.no_profile:
+        lib.gptq_profile_enable(True)
+        lib.gptq_profile_read()
+        evs = []
+        for _ in range(args.steps):
+            if flush:
+                flush_l2(fbuf)
+            runner.step(events=evs)
+        torch.cuda.synchronize()
+        lib.gptq_profile_enable(False)
+        prof = lib.gptq_profile_read()
+        for name, idx in (("hessian", (0, 1)), ("prepare", (1, 2)), ("quantize", (2, 3))):
+            stages[name] = sum(e[idx[0]].elapsed_time(e[idx[1]]) for e in evs) / args.steps
+        tot = sum(v[1] for v in prof.values())
+        work = algorithmic(layers)
+        for name, (cnt, t) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
+            kernels[name] = {"launches_per_step": cnt / args.steps, "ms_per_step": t / args.steps,
+                             "share": t / tot if tot else None}
+            if name in work and name in ROOF:
+                bound, unit = ROOF[name]
+                per_step = work[name]
+                sec = t / args.steps / 1e3
+                if unit == "TFLOP/s":
+                    ach = per_step / sec / 1e12
+                    peak = pk["bf16_tflops"] if bound == "tensor" else FFMA_PEAK_TFLOPS
+                else:
+                    ach = per_step / sec / 1e9
+                    peak = pk["hbm_gbs"]
+                kernels[name].update({"bound": bound, "achieved": ach, "peak": peak, "unit": unit,
+                                      "frac": ach / peak})
+        top = max(kernels.items(), key=lambda kv: kv[1]["ms_per_step"])[0] if kernels else None
+        if top and "achieved" in kernels[top]:
+            k = kernels[top]
+            per_launch = k["ms_per_step"] / max(1.0, k["launches_per_step"])
+            roof = {"kernel": top, "bound": k["bound"], "achieved": k["achieved"], "peak": k["peak"],
+                    "unit": k["unit"], "frac": k["frac"], "traffic": None,
+                    "peak_source": ("measured" if k["bound"] != "alu" and pk["source"] == "measured" else
+                                    "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz" if k["bound"] == "alu"
+                                    else "fallback"),
+                    "avg_launch_ms": per_launch}
+        elif top:
+            k = kernels[top]
+            roof = {"kernel": top, "bound": "latency", "achieved": None, "peak": None, "unit": None, "frac": None,
+                    "traffic": None, "avg_launch_ms": k["ms_per_step"] / max(1.0, k["launches_per_step"])}
+        # the tensor-core Hessian against its roofline, always reported
+        if "hessian_tc_kernel" in kernels:
+            stages["hessian_tc_frac_of_bf16_peak"] = kernels["hessian_tc_kernel"].get("frac")
+
+    # ---- e2e: pinned host inputs -> device -> same pass -> quantised artefacts back ----
+    e2e = None
+    if not args.no_e2e:
+        hX = [L.X.to("cpu").pin_memory() for L in layers]
+        hW = [[W.to("cpu").pin_memory() for W in L.Ws] for L in layers]
+        dX = [torch.empty_like(L.X) for L in layers]
+        dW = [[torch.empty_like(W) for W in L.Ws] for L in layers]
+        h_out = [[{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in o.items()
+                   if k in ("packed", "scales", "zeros", "g_idx")} for o in outs] for outs in runner.outs]
+        bi = sum(x.numel() * x.element_size() for x in hX) + sum(w.numel() * 4 for ws_ in hW for w in ws_)
+        bo = sum(v.numel() * v.element_size() for outs in h_out for o in outs for v in o.values())
+
+        def e2e_step():
+            for i in range(len(layers)):
+                dX[i].copy_(hX[i], non_blocking=True)
+                for j in range(len(hW[i])):
+                    dW[i][j].copy_(hW[i][j], non_blocking=True)
+            outs = runner.step(Xs=dX, Wss=dW)
+            for i, o_l in enumerate(outs):
+                for j, o in enumerate(o_l):
+                    for k in h_out[i][j]:
+                        h_out[i][j][k].copy_(o[k], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        et = []
+        for _ in range(args.steps):
+            if flush:
+                flush_l2(fbuf)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            e2e_step()
+            et.append((time.perf_counter() - t0) * 1e3)
+        e2e = {"value": statistics.mean(et), "unit": "ms", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only) ----
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and ws == 1:
+        frac = CPU_BASELINE_ROW_FRAC[args.config]
+        t = time_oracle(args.config, layers, frac, reps=1)
+        cpu = {"value": statistics.mean(t), "unit": "ms", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": cpu_sample_desc(args.config, frac)}
+
+    if rank == 0:
+        value = ms / ws   # weak scaling over independent layer replicas: ms per layer pass
+        line = {
+            "metric": METRIC, "value": value, "unit": "ms", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16xbf16->f32 (Hessian), f32 (rest)", "data": "synthetic",
+            "config": {"workload": wl.name, "config_index": args.config,
+                       "layers": [[L.names, list(L.X.shape)] for L in layers],
+                       "l2": ("flushed between steps (512 MiB write)" if flush else "inputs larger than L2"),
+                       "parallelism": f"replicas x{ws}"},
+            "clocks": ck, "gpu_launches": launches // max(1, args.steps) * args.steps,
+            "gpu_launches_per_step": launches / max(1, args.steps), "wall_ms_timed_region": wall,
+            "stages_ms": stages, "kernels": kernels, "roofline": roof, "e2e": e2e, "cpu_baseline": cpu,
+            "peaks": pk,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_info()
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1 and args.impl != "reference":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

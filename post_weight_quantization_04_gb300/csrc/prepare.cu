@@ -1,0 +1,321 @@
+// prepare.cu — gptq_prepare: dead inputs, damping, act_order permutation and
+// U = upper Cholesky factor of H^-1.
+//
+// The GPTQ guide page ("Source code", `_hessian_inverse_chol`) forms U as
+// cholesky(inv(H)).T. Here the same U comes from one factorisation and one triangular
+// inverse, both blocked and fp32 on the GPU:
+//
+//   Hp  = H[perm][:, perm] with the dead diagonal set to 1 and damping added
+//   D   = diag(Hp),   Hh = D^-1/2 Hp D^-1/2            (unit diagonal: equilibration)
+//   J   = the reversal permutation,  A = J Hh J = L L^T (ordinary lower Cholesky)
+//   then Hh = (J L J)(J L J)^T with J L J upper, so Hh^-1 = Uh^T Uh for Uh = J L^-1 J
+//   and U = Uh D^-1/2  satisfies U^T U = Hp^-1 with U upper and a positive diagonal.
+//
+// Equilibration removes the lognormal per-channel spread of the activations from the
+// fp32 factorisation; damping (0.01 * mean diag) bounds the condition number.
+//
+// Workspace layout (256-byte aligned slabs):
+//   A     d*d fp32   reversed, equilibrated Hp -> L (lower triangle)
+//   Binv  d*d fp32   identity -> L^-1 (lower triangle)
+//   LinvD nblk*NB*NB fp32  inverses of L's diagonal blocks
+//   ddiag d fp32, rr d fp32 (1/sqrt(ddiag)), status int
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "sgemm.cuh"
+
+namespace gptq {
+
+namespace {
+
+constexpr int NB = 128;  // panel width of the blocked factorisation
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct PrepWs {
+    float* A;
+    float* Binv;
+    float* LinvD;
+    float* ddiag;
+    float* rr;
+    int* status;
+    size_t bytes;
+};
+
+PrepWs carve(void* base, int64_t d) {
+    PrepWs w{};
+    size_t off = 0;
+    char* p = static_cast<char*>(base);
+    const int64_t nblk = (d + NB - 1) / NB;
+    w.A = reinterpret_cast<float*>(p + off);
+    off = align256(off + sizeof(float) * d * d);
+    w.Binv = reinterpret_cast<float*>(p + off);
+    off = align256(off + sizeof(float) * d * d);
+    w.LinvD = reinterpret_cast<float*>(p + off);
+    off = align256(off + sizeof(float) * nblk * NB * NB);
+    w.ddiag = reinterpret_cast<float*>(p + off);
+    off = align256(off + sizeof(float) * d);
+    w.rr = reinterpret_cast<float*>(p + off);
+    off = align256(off + sizeof(float) * d);
+    w.status = reinterpret_cast<int*>(p + off);
+    off = align256(off + sizeof(int) * 4);
+    w.bytes = off;
+    return w;
+}
+
+// dead[j] = (H[j][j] == 0); the dead diagonal becomes 1; mean of the fixed diagonal in
+// fp64; damped diagonal and its inverse square root.
+__global__ void __launch_bounds__(1024) prep_diag_kernel(const float* __restrict__ H, int64_t d, float damp,
+                                                        uint8_t* __restrict__ dead, float* __restrict__ ddiag,
+                                                        float* __restrict__ rr) {
+    __shared__ double part[32];
+    double s = 0.0;
+    for (int64_t j = threadIdx.x; j < d; j += blockDim.x) {
+        const float h = H[j * d + j];
+        const bool dj = (h == 0.0f);
+        dead[j] = dj ? 1 : 0;
+        s += dj ? 1.0 : (double)h;
+    }
+    s = warp_sum_d(s);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        double v = (threadIdx.x < (blockDim.x >> 5)) ? part[threadIdx.x] : 0.0;
+        v = warp_sum_d(v);
+        if (threadIdx.x == 0) part[0] = v;
+    }
+    __syncthreads();
+    const double add = (double)damp * (part[0] / (double)d);
+    for (int64_t j = threadIdx.x; j < d; j += blockDim.x) {
+        const float h = H[j * d + j];
+        const double hd = (h == 0.0f ? 1.0 : (double)h) + add;
+        ddiag[j] = (float)hd;
+        rr[j] = (float)(1.0 / sqrt(hd));
+    }
+}
+
+// Stable descending order of the keys: rank(i) = #{k : key_k > key_i} + #{k < i : key_k == key_i};
+// perm[rank(i)] = i.
+__global__ void __launch_bounds__(256) prep_perm_kernel(const float* __restrict__ key, int64_t d,
+                                                       int32_t* __restrict__ perm) {
+    __shared__ float tile[256];
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const float ki = (i < d) ? key[i] : 0.0f;
+    int64_t rank = 0;
+    for (int64_t t0 = 0; t0 < d; t0 += 256) {
+        const int64_t k = t0 + threadIdx.x;
+        tile[threadIdx.x] = (k < d) ? key[k] : 0.0f;
+        __syncthreads();
+        const int lim = (int)(d - t0 < 256 ? d - t0 : 256);
+        for (int u = 0; u < lim; ++u) {
+            const float kk = tile[u];
+            rank += (kk > ki) || (kk == ki && t0 + u < i);
+        }
+        __syncthreads();
+    }
+    if (i < d) perm[rank] = (int32_t)i;
+}
+
+__global__ void iota_kernel(int32_t* __restrict__ perm, int64_t d) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < d) perm[i] = (int32_t)i;
+}
+
+// A[i][j] (j <= i) = Hh[d-1-i][d-1-j], Hh = D^-1/2 Hp D^-1/2, Hp = H[perm][:, perm]
+// (fixed, damped diagonal; H read from its upper triangle).
+__global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restrict__ H, int64_t d,
+                                                         const int32_t* __restrict__ perm,
+                                                         const float* __restrict__ rr, float* __restrict__ A) {
+    const int64_t i = (int64_t)blockIdx.y * 8 + (threadIdx.x >> 5);
+    const int64_t jb = (int64_t)blockIdx.x * 32;
+    if (i >= d || jb > i) return;
+    const int64_t j = jb + (threadIdx.x & 31);
+    if (j > i) return;
+    const int32_t a = perm[d - 1 - i];
+    const int32_t b = perm[d - 1 - j];
+    float v;
+    if (a == b) {
+        v = 1.0f;
+    } else {
+        const int32_t lo = a < b ? a : b, hi = a < b ? b : a;
+        v = H[(int64_t)lo * d + hi] * rr[a] * rr[b];
+    }
+    A[i * d + j] = v;
+}
+
+// One CTA factors the diagonal block A[k0:k0+n, k0:k0+n] = L L^T in place (lower), and
+// writes L^-1 (lower, NB x NB, zeros above) to Linv. A non-positive or non-finite pivot
+// records GPTQ_ERR_NOT_SPD (and is replaced by 1 so the kernel finishes).
+__global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, int64_t lda, int64_t k0, int n,
+                                                        float* __restrict__ Linv, int* __restrict__ status) {
+    extern __shared__ float sm[];
+    float* S = sm;                    // NB x (NB+1)
+    float* X = sm + NB * (NB + 1);    // NB x (NB+1)
+    __shared__ float part[4][NB];
+    const int tid = threadIdx.x, nt = blockDim.x;
+    constexpr int LD = NB + 1;
+
+    for (int idx = tid; idx < NB * NB; idx += nt) {
+        const int i = idx / NB, j = idx % NB;
+        S[i * LD + j] = (i < n && j <= i) ? A[(k0 + i) * lda + k0 + j] : 0.0f;
+        X[i * LD + j] = 0.0f;
+    }
+    __syncthreads();
+
+    for (int k = 0; k < n; ++k) {
+        float piv = S[k * LD + k];
+        if (!(piv > 0.0f) || !isfinite(piv)) {
+            if (tid == 0) set_status(status, GPTQ_ERR_NOT_SPD);
+            piv = 1.0f;
+        }
+        const float lkk = sqrtf(piv);
+        const float inv = 1.0f / lkk;
+        __syncthreads();
+        for (int i = k + 1 + tid; i < n; i += nt) S[i * LD + k] *= inv;
+        if (tid == 0) S[k * LD + k] = lkk;
+        __syncthreads();
+        const int m = n - k - 1;
+        for (int idx = tid; idx < m * m; idx += nt) {
+            const int i = k + 1 + idx / m, j = k + 1 + idx % m;
+            if (j <= i) S[i * LD + j] = fmaf(-S[i * LD + k], S[j * LD + k], S[i * LD + j]);
+        }
+        __syncthreads();
+    }
+
+    for (int idx = tid; idx < n * NB; idx += nt) {
+        const int i = idx / NB, j = idx % NB;
+        if (j <= i) A[(k0 + i) * lda + k0 + j] = S[i * LD + j];
+    }
+
+    // L^-1 by rows: X[i][c] = (delta_ic - sum_{c<=m<i} L[i][m] X[m][c]) / L[i][i];
+    // four threads share each column c's dot product.
+    const int c = tid & (NB - 1), q = tid >> 7;  // q in 0..3
+    for (int i = 0; i < n; ++i) {
+        float s = 0.0f;
+        if (c < i) {
+            const int len = i - c;
+            const int per = (len + 3) >> 2;
+            const int mb = c + q * per, me = min(i, mb + per);
+            for (int m = mb; m < me; ++m) s = fmaf(S[i * LD + m], X[m * LD + c], s);
+        }
+        part[q][c] = s;
+        __syncthreads();
+        if (q == 0 && c <= i) {
+            const float tot = part[0][c] + part[1][c] + part[2][c] + part[3][c];
+            X[i * LD + c] = ((c == i ? 1.0f : 0.0f) - tot) / S[i * LD + i];
+        }
+        __syncthreads();
+    }
+    for (int idx = tid; idx < NB * NB; idx += nt) {
+        const int i = idx / NB, j = idx % NB;
+        Linv[idx] = (i < n && j <= i) ? X[i * LD + j] : 0.0f;
+    }
+}
+
+__global__ void eye_kernel(float* __restrict__ B, int64_t d) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx < d * d) B[idx] = (idx / d == idx % d) ? 1.0f : 0.0f;
+}
+
+// U[i][j] = (i <= j) ? Linv[d-1-i][d-1-j] * rr[perm[j]] : 0
+__global__ void __launch_bounds__(256) prep_scatter_kernel(const float* __restrict__ Binv, int64_t d,
+                                                          const int32_t* __restrict__ perm,
+                                                          const float* __restrict__ rr, float* __restrict__ U) {
+    const int64_t i = blockIdx.y;
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < d; j += (int64_t)gridDim.x * blockDim.x) {
+        U[i * d + j] = (i <= j) ? Binv[(d - 1 - i) * d + (d - 1 - j)] * rr[perm[j]] : 0.0f;
+    }
+}
+
+}  // namespace
+
+}  // namespace gptq
+
+using namespace gptq;
+
+extern "C" size_t gptq_prepare_workspace_bytes(int64_t d, int act_order) {
+    (void)act_order;
+    if (d <= 0) return 0;
+    return carve(nullptr, d).bytes;
+}
+
+extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, float damp, int act_order, float* U,
+                            int32_t* perm, uint8_t* dead, void* ws, size_t ws_bytes, void* stream_) {
+    if (d <= 0 || d > (1 << 20) || !H || !U || !perm || !dead || !ws) return GPTQ_ERR_INVALID_ARG;
+    if (act_order && !diag_xtx) return GPTQ_ERR_INVALID_ARG;
+    if (!(damp >= 0.0f) || !isfinite(damp)) return GPTQ_ERR_INVALID_ARG;
+    PrepWs w = carve(ws, d);
+    if (ws_bytes < w.bytes) return GPTQ_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream_);
+
+    GPTQ_CUDA_TRY(cudaMemsetAsync(w.status, 0, sizeof(int), s));
+    GPTQ_LAUNCH(K_PREP_DIAG, s, prep_diag_kernel<<<1, 1024, 0, s>>>(H, d, damp, dead, w.ddiag, w.rr));
+    GPTQ_LAUNCH_CHECK();
+    const unsigned g1 = (unsigned)ceil_div(d, 256);
+    if (act_order)
+        GPTQ_LAUNCH(K_PREP_PERM, s, prep_perm_kernel<<<g1, 256, 0, s>>>(diag_xtx, d, perm));
+    else
+        GPTQ_LAUNCH(K_PREP_PERM, s, iota_kernel<<<g1, 256, 0, s>>>(perm, d));
+    GPTQ_LAUNCH_CHECK();
+    {
+        dim3 grid((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 8));
+        GPTQ_LAUNCH(K_PREP_GATHER, s, prep_gather_kernel<<<grid, 256, 0, s>>>(H, d, perm, w.rr, w.A));
+        GPTQ_LAUNCH_CHECK();
+    }
+
+    static bool attr_set = false;
+    const size_t potrf_smem = sizeof(float) * 2 * NB * (NB + 1);
+    if (!attr_set) {
+        GPTQ_CUDA_TRY(cudaFuncSetAttribute(potrf_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)potrf_smem));
+        attr_set = true;
+    }
+
+    // blocked right-looking Cholesky of A (lower)
+    const int64_t nblk = ceil_div(d, NB);
+    for (int64_t kb = 0; kb < nblk; ++kb) {
+        const int64_t k0 = kb * NB;
+        const int n = (int)std::min<int64_t>(NB, d - k0);
+        float* LinvK = w.LinvD + kb * NB * NB;
+        GPTQ_LAUNCH(K_POTRF, s, potrf_diag_kernel<<<1, 512, potrf_smem, s>>>(w.A, d, k0, n, LinvK, w.status));
+        GPTQ_LAUNCH_CHECK();
+        const int64_t m = d - k0 - n;
+        if (m > 0) {
+            float* P = w.A + (k0 + n) * d + k0;
+            // panel: P <- P * Linv_kk^T   (in place; N = n <= 128)
+            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, true, (int)m, n, n, 1.0f, P, d, LinvK, NB, 0.0f, P, d, false, s));
+            // trailing: A22 -= P P^T (lower tiles)
+            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, true, (int)m, (int)m, n, -1.0f, P, d, P, d, 1.0f, w.A + (k0 + n) * d + k0 + n, d,
+                                true, s));
+        }
+    }
+
+    // L^-1 by block rows: X[i,:] = Linv_ii * B[i,:];  B[i+1:, :] -= L[i+1:, i] X[i, :]
+    GPTQ_LAUNCH(K_EYE, s, eye_kernel<<<(unsigned)ceil_div(d * d, 256), 256, 0, s>>>(w.Binv, d));
+    GPTQ_LAUNCH_CHECK();
+    for (int64_t ib = 0; ib < nblk; ++ib) {
+        const int64_t i0 = ib * NB;
+        const int n = (int)std::min<int64_t>(NB, d - i0);
+        const int64_t ncols = i0 + n;
+        float* Xi = w.Binv + i0 * d;
+        GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, false, n, (int)ncols, n, 1.0f, w.LinvD + ib * NB * NB, NB, Xi, d, 0.0f, Xi, d, false, s));
+        const int64_t m = d - i0 - n;
+        if (m > 0) {
+            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, false, (int)m, (int)ncols, n, -1.0f, w.A + (i0 + n) * d + i0, d, Xi, d, 1.0f,
+                                w.Binv + (i0 + n) * d, d, false, s));
+        }
+    }
+
+    {
+        dim3 grid((unsigned)std::min<int64_t>(ceil_div(d, 256), 64), (unsigned)d);
+        GPTQ_LAUNCH(K_SCATTER, s, prep_scatter_kernel<<<grid, 256, 0, s>>>(w.Binv, d, perm, w.rr, U));
+        GPTQ_LAUNCH_CHECK();
+    }
+
+    int hstatus = 0;
+    GPTQ_CUDA_TRY(cudaMemcpyAsync(&hstatus, w.status, sizeof(int), cudaMemcpyDeviceToHost, s));
+    GPTQ_CUDA_TRY(cudaStreamSynchronize(s));
+    return hstatus;
+}

@@ -1,0 +1,491 @@
+// quantize.cu — GPTQ's fixed-order column loop, round-to-nearest, g_idx and packing.
+//
+// The column loop (GPTQ's error-compensation loop page, its four steps; GPTQ guide page,
+// "Source code", `gptq`) is run in 128-column blocks, the lazy-batch structure the guide
+// page's "Simplifications" paragraph names (same result, block updates):
+//
+//   for each block [j0, j0+128):
+//     gptq_block_kernel    rows in parallel (4 threads per row, 32 columns each in
+//                          registers); U[blk, blk] in shared memory; for every column j:
+//                          broadcast w_j inside the row's 4 lanes, q = grid(w_j),
+//                          err = (w_j - q) / U[j][j], w_c -= err * U[j][c] for the block's
+//                          columns (U is zero below the diagonal, so columns already done
+//                          are untouched); group scales/zero points at each group start
+//                          from the updated weights; Err[:, blk] kept for the update below
+//     trailing update      W[:, j0+128:] -= Err * U[blk, j0+128:]   (fp32 GEMM)
+//
+// The working copy of W lives in the caller's workspace, permuted into loop order with
+// dead columns zeroed (guide page, "Source code": W[:, dead] = 0, W = W[:, perm]).
+// Outputs go straight to the original column order.
+#include <algorithm>
+
+#include "common.cuh"
+#include "quant.cuh"
+#include "sgemm.cuh"
+
+namespace gptq {
+
+namespace {
+
+constexpr int QB = 128;  // column block width
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct QuantWs {
+    float* W;       // rows x cols working copy (loop order)
+    float* Err;     // rows x QB
+    float* cur_s;   // rows: current scale (per-row grid, or a group wider than a block)
+    float* cur_z;   // rows
+    float* loss;    // rows
+    size_t bytes;
+};
+
+QuantWs carve(void* base, int64_t rows, int64_t cols) {
+    QuantWs w{};
+    char* p = static_cast<char*>(base);
+    size_t off = 0;
+    w.W = reinterpret_cast<float*>(p + off);
+    off = align256(off + sizeof(float) * rows * cols);
+    w.Err = reinterpret_cast<float*>(p + off);
+    off = align256(off + sizeof(float) * rows * QB);
+    w.cur_s = reinterpret_cast<float*>(p + off);
+    off = align256(off + sizeof(float) * rows);
+    w.cur_z = reinterpret_cast<float*>(p + off);
+    off = align256(off + sizeof(float) * rows);
+    w.loss = reinterpret_cast<float*>(p + off);
+    off = align256(off + sizeof(float) * rows);
+    w.bytes = off;
+    return w;
+}
+
+bool group_ok(int group) { return group == 0 || (group > 0 && (group % QB == 0 || QB % group == 0)); }
+
+// Wk[r][k] = dead[perm[k]] ? 0 : W[r][perm[k]]
+__global__ void init_work_kernel(const float* __restrict__ W, int64_t rows, int64_t cols, const int32_t* __restrict__ perm,
+                                 const uint8_t* __restrict__ dead, float* __restrict__ Wk) {
+    const int64_t r = blockIdx.y;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < cols; k += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t c = perm ? perm[k] : k;
+        Wk[r * cols + k] = (dead && dead[c]) ? 0.0f : W[r * cols + c];
+    }
+}
+
+// One warp per row: grid of Wk[r][c0:c1] -> cur_s/cur_z and the (scales, zeros) outputs.
+__global__ void row_params_kernel(const float* __restrict__ Wk, int64_t rows, int64_t cols, int64_t c0, int64_t c1,
+                                  int bits, int sym, float* __restrict__ cur_s, float* __restrict__ cur_z,
+                                  float* __restrict__ scales, uint8_t* __restrict__ zeros, int64_t G, int64_t gi) {
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    const float* row = Wk + r * cols;
+    float mx = -INFINITY, mn = INFINITY, am = 0.0f;
+    for (int64_t c = c0 + lane; c < c1; c += 32) {
+        const float v = row[c];
+        mx = fmaxf(mx, v);
+        mn = fminf(mn, v);
+        am = fmaxf(am, fabsf(v));
+    }
+    Grid g;
+    if (sym) {
+        am = warp_max(am);
+        g = sym_grid(am, (1 << (bits - 1)) - 1);
+    } else {
+        mx = warp_max(mx);
+        mn = warp_min(mn);
+        g = asym_grid(mn, mx, (1 << bits) - 1);
+    }
+    if (lane == 0) {
+        cur_s[r] = g.s;
+        cur_z[r] = g.z;
+        scales[r * G + gi] = g.s;
+        zeros[r * G + gi] = sym ? (uint8_t)(1 << (bits - 1)) : (uint8_t)g.z;
+    }
+}
+
+struct BlockArgs {
+    const float* Wk;
+    int64_t rows, cols, j0;
+    int bw;
+    const float* U;
+    int bits, sym, group;  // group in (0, 128] dividing 128: in-block params; else cur_s/cur_z
+    const float* cur_s;
+    const float* cur_z;
+    float* Err;
+    int8_t* codes;
+    float* Wq;
+    const int32_t* perm;
+    float* scales;
+    uint8_t* zeros;
+    int64_t G;
+    float* loss;
+};
+
+template <int TPR>
+__global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
+    constexpr int CPT = QB / TPR;
+    constexpr int RPC = 128 / TPR;  // rows per CTA
+    extern __shared__ float us[];   // QB x QB block of U (zeros below the diagonal)
+    __shared__ float invd[QB];
+
+    const int bw = a.bw;
+    for (int idx = threadIdx.x; idx < QB * QB; idx += blockDim.x) {
+        const int i = idx / QB, c = idx % QB;
+        us[idx] = (i < bw && c < bw && c >= i) ? a.U[(a.j0 + i) * a.cols + a.j0 + c] : 0.0f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < QB; i += blockDim.x) invd[i] = (i < bw) ? 1.0f / us[i * QB + i] : 0.0f;
+    __syncthreads();
+
+    const int sub = threadIdx.x % TPR;
+    const int64_t row = (int64_t)blockIdx.x * RPC + threadIdx.x / TPR;
+    const bool active = row < a.rows;
+    const bool sym = a.sym != 0;
+    const int qmax = sym ? (1 << (a.bits - 1)) - 1 : (1 << a.bits) - 1;
+    const int lo = sym ? -qmax : 0, hi = qmax;
+    const bool inblock_groups = a.group > 0 && a.group <= QB;
+
+    float w[CPT], er[CPT], qr[CPT];
+    int8_t cr[CPT];
+    const float* wrow = a.Wk + (active ? row : 0) * a.cols + a.j0 + sub * CPT;
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+        w[k] = (active && sub * CPT + k < bw) ? wrow[k] : 0.0f;
+        er[k] = 0.0f;
+        qr[k] = 0.0f;
+        cr[k] = 0;
+    }
+    Grid g{1.0f, 1.0f, 0.0f};
+    if (!inblock_groups && active) {
+        g.s = a.cur_s[row];
+        g.inv_s = 1.0f / g.s;
+        g.z = a.cur_z[row];
+    }
+    float loss = 0.0f;
+
+    for (int o = 0; o < TPR; ++o) {
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            const int jj = o * CPT + k;
+            if (jj >= bw) break;
+            if (inblock_groups && (jj % a.group) == 0) {
+                const int gend = min(jj + a.group, bw);
+                float am = 0.0f, mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+                for (int kk = 0; kk < CPT; ++kk) {
+                    const int c = sub * CPT + kk;
+                    if (c >= jj && c < gend) {
+                        am = fmaxf(am, fabsf(w[kk]));
+                        mx = fmaxf(mx, w[kk]);
+                        mn = fminf(mn, w[kk]);
+                    }
+                }
+#pragma unroll
+                for (int off = TPR / 2; off > 0; off >>= 1) {
+                    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off, TPR));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off, TPR));
+                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off, TPR));
+                }
+                g = sym ? sym_grid(am, qmax) : asym_grid(mn, mx, qmax);
+                if (active && sub == 0) {
+                    const int64_t gi = (a.j0 + jj) / a.group;
+                    a.scales[row * a.G + gi] = g.s;
+                    a.zeros[row * a.G + gi] = sym ? (uint8_t)(1 << (a.bits - 1)) : (uint8_t)g.z;
+                }
+            }
+            const float wj = __shfl_sync(0xffffffffu, w[k], o, TPR);
+            const int c = grid_code(wj, g, sym, lo, hi);
+            const float q = grid_dequant(c, g, sym);
+            const float err = (wj - q) * invd[jj];
+            if (sub == o) {
+                cr[k] = (int8_t)c;
+                qr[k] = q;
+                er[k] = err;
+            }
+            loss = fmaf(err, err, loss);
+            const float* ur = us + jj * QB + sub * CPT;
+#pragma unroll
+            for (int kk = 0; kk < CPT; kk += 4) {
+                const float4 u4 = *reinterpret_cast<const float4*>(ur + kk);
+                w[kk] = fmaf(-err, u4.x, w[kk]);
+                w[kk + 1] = fmaf(-err, u4.y, w[kk + 1]);
+                w[kk + 2] = fmaf(-err, u4.z, w[kk + 2]);
+                w[kk + 3] = fmaf(-err, u4.w, w[kk + 3]);
+            }
+        }
+    }
+
+    if (!active) return;
+    float* erow = a.Err + row * QB + sub * CPT;
+#pragma unroll
+    for (int k = 0; k < CPT; k += 4) *reinterpret_cast<float4*>(erow + k) = make_float4(er[k], er[k + 1], er[k + 2], er[k + 3]);
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+        const int lc = sub * CPT + k;
+        if (lc < bw) {
+            const int64_t oc = a.perm ? (int64_t)a.perm[a.j0 + lc] : a.j0 + lc;
+            a.codes[row * a.cols + oc] = cr[k];
+            if (a.Wq) a.Wq[row * a.cols + oc] = qr[k];
+        }
+    }
+    if (sub == 0) a.loss[row] += loss;
+}
+
+__global__ void g_idx_kernel(const int32_t* __restrict__ perm, int64_t cols, int group, int32_t* __restrict__ g_idx) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= cols) return;
+    const int64_t c = perm ? perm[k] : k;
+    g_idx[c] = group ? (int32_t)(k / group) : 0;
+}
+
+__global__ void copy_loss_kernel(const float* __restrict__ src, int64_t rows, float* __restrict__ dst) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r < rows) dst[r] = src[r];
+}
+
+// One thread per output word: bits [32w, 32w+32) of the row's LSB-first b-bit stream.
+__global__ void pack_kernel(const int8_t* __restrict__ codes, int64_t rows, int64_t cols, int bits, int offset,
+                            int64_t words, uint32_t* __restrict__ packed) {
+    const int64_t r = blockIdx.y;
+    const uint32_t mask = (1u << bits) - 1u;
+    for (int64_t wd = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; wd < words; wd += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t bit0 = wd * 32;
+        const int64_t c0 = bit0 / bits;
+        const int64_t c1 = std::min<int64_t>(cols - 1, (bit0 + 31) / bits);
+        uint64_t acc = 0;
+        for (int64_t c = c0; c <= c1; ++c) {
+            const uint32_t u = (uint32_t)((int)codes[r * cols + c] + offset) & mask;
+            const int64_t pos = c * bits - bit0;
+            acc |= pos >= 0 ? ((uint64_t)u << pos) : ((uint64_t)u >> (-pos));
+        }
+        packed[r * words + wd] = (uint32_t)acc;
+    }
+}
+
+// Round-to-nearest: one warp per (row, group) (group > 0) or one CTA per row (group == 0).
+__global__ void rtn_group_kernel(const float* __restrict__ W, int64_t rows, int64_t cols, const uint8_t* __restrict__ dead,
+                                 int bits, int sym, int group, int64_t G, int8_t* __restrict__ codes,
+                                 float* __restrict__ scales, uint8_t* __restrict__ zeros, float* __restrict__ Wq) {
+    const int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (task >= rows * G) return;
+    const int64_t r = task / G, gi = task % G;
+    const int64_t c0 = gi * group, c1 = std::min<int64_t>(cols, c0 + group);
+    const float* row = W + r * cols;
+    float mx = -INFINITY, mn = INFINITY, am = 0.0f;
+    for (int64_t c = c0 + lane; c < c1; c += 32) {
+        const float v = (dead && dead[c]) ? 0.0f : row[c];
+        mx = fmaxf(mx, v);
+        mn = fminf(mn, v);
+        am = fmaxf(am, fabsf(v));
+    }
+    const int qmax = sym ? (1 << (bits - 1)) - 1 : (1 << bits) - 1;
+    const Grid g = sym ? sym_grid(warp_max(am), qmax) : asym_grid(warp_min(mn), warp_max(mx), qmax);
+    if (lane == 0) {
+        scales[r * G + gi] = g.s;
+        zeros[r * G + gi] = sym ? (uint8_t)(1 << (bits - 1)) : (uint8_t)g.z;
+    }
+    const int lo = sym ? -qmax : 0;
+    for (int64_t c = c0 + lane; c < c1; c += 32) {
+        const float v = (dead && dead[c]) ? 0.0f : row[c];
+        const int code = grid_code(v, g, sym != 0, lo, qmax);
+        codes[r * cols + c] = (int8_t)code;
+        if (Wq) Wq[r * cols + c] = grid_dequant(code, g, sym != 0);
+    }
+}
+
+__global__ void __launch_bounds__(256) rtn_row_kernel(const float* __restrict__ W, int64_t rows, int64_t cols,
+                                                     const uint8_t* __restrict__ dead, int bits, int sym,
+                                                     int8_t* __restrict__ codes, float* __restrict__ scales,
+                                                     uint8_t* __restrict__ zeros, float* __restrict__ Wq) {
+    const int64_t r = blockIdx.x;
+    const float* row = W + r * cols;
+    __shared__ float red[3][8];
+    float mx = -INFINITY, mn = INFINITY, am = 0.0f;
+    for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) {
+        const float v = (dead && dead[c]) ? 0.0f : row[c];
+        mx = fmaxf(mx, v);
+        mn = fminf(mn, v);
+        am = fmaxf(am, fabsf(v));
+    }
+    mx = warp_max(mx);
+    mn = warp_min(mn);
+    am = warp_max(am);
+    const int wid = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        red[0][wid] = mx;
+        red[1][wid] = mn;
+        red[2][wid] = am;
+    }
+    __syncthreads();
+    mx = -INFINITY;
+    mn = INFINITY;
+    am = 0.0f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
+        mx = fmaxf(mx, red[0][i]);
+        mn = fminf(mn, red[1][i]);
+        am = fmaxf(am, red[2][i]);
+    }
+    const int qmax = sym ? (1 << (bits - 1)) - 1 : (1 << bits) - 1;
+    const Grid g = sym ? sym_grid(am, qmax) : asym_grid(mn, mx, qmax);
+    if (threadIdx.x == 0) {
+        scales[r] = g.s;
+        zeros[r] = sym ? (uint8_t)(1 << (bits - 1)) : (uint8_t)g.z;
+    }
+    const int lo = sym ? -qmax : 0;
+    for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) {
+        const float v = (dead && dead[c]) ? 0.0f : row[c];
+        const int code = grid_code(v, g, sym != 0, lo, qmax);
+        codes[r * cols + c] = (int8_t)code;
+        if (Wq) Wq[r * cols + c] = grid_dequant(code, g, sym != 0);
+    }
+}
+
+int launch_pack(const int8_t* codes, int64_t rows, int64_t cols, int bits, int sym, uint32_t* packed, cudaStream_t s) {
+    const int64_t words = gptq_packed_words_per_row(cols, bits);
+    const unsigned gx = (unsigned)std::min<int64_t>(ceil_div(words, 256), 1024);
+    dim3 grid(gx, (unsigned)rows);
+    GPTQ_LAUNCH(K_PACK, s, pack_kernel<<<grid, 256, 0, s>>>(codes, rows, cols, bits, sym ? (1 << (bits - 1)) : 0, words, packed));
+    GPTQ_LAUNCH_CHECK();
+    return GPTQ_OK;
+}
+
+}  // namespace
+}  // namespace gptq
+
+using namespace gptq;
+
+extern "C" int64_t gptq_packed_words_per_row(int64_t cols, int bits) {
+    if (cols < 0 || bits < 1 || bits > 8) return 0;
+    return (cols * bits + 31) / 32;
+}
+
+extern "C" size_t gptq_quantize_workspace_bytes(int64_t rows, int64_t cols, gptq_qconfig q) {
+    (void)q;
+    if (rows <= 0 || cols <= 0) return 0;
+    return carve(nullptr, rows, cols).bytes;
+}
+
+extern "C" int gptq_pack(const int8_t* codes, int64_t rows, int64_t cols, int bits, int sym, uint32_t* packed,
+                         void* stream) {
+    if (rows < 0 || cols < 0) return GPTQ_ERR_INVALID_ARG;
+    if (bits < 2 || bits > 4) return GPTQ_ERR_UNSUPPORTED;
+    if (rows == 0 || cols == 0) return GPTQ_OK;
+    if (!codes || !packed || rows > 65535) return GPTQ_ERR_INVALID_ARG;
+    return launch_pack(codes, rows, cols, bits, sym, packed, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const float* U, const int32_t* perm,
+                             const uint8_t* dead, gptq_qconfig q, int8_t* codes, float* scales, uint8_t* zeros,
+                             int32_t* g_idx, float* Wq, uint32_t* packed, float* row_loss, void* ws, size_t ws_bytes,
+                             void* stream) {
+    if (rows < 0 || cols < 0) return GPTQ_ERR_INVALID_ARG;
+    if (q.bits < 2 || q.bits > 4 || !group_ok(q.group)) return GPTQ_ERR_UNSUPPORTED;
+    if (rows == 0 || cols == 0) return GPTQ_OK;
+    if (!W || !U || !codes || !scales || !zeros || !ws || rows > 65535) return GPTQ_ERR_INVALID_ARG;
+    QuantWs w = carve(ws, rows, cols);
+    if (ws_bytes < w.bytes) return GPTQ_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool sym = q.sym != 0;
+    const int64_t G = q.group ? ceil_div(cols, q.group) : 1;
+
+    {
+        dim3 grid((unsigned)std::min<int64_t>(ceil_div(cols, 256), 64), (unsigned)rows);
+        GPTQ_LAUNCH(K_INIT_WORK, s, init_work_kernel<<<grid, 256, 0, s>>>(W, rows, cols, perm, dead, w.W));
+        GPTQ_LAUNCH_CHECK();
+    }
+    GPTQ_CUDA_TRY(cudaMemsetAsync(w.loss, 0, sizeof(float) * rows, s));
+    const unsigned pgrid = (unsigned)ceil_div(rows, 8);
+    if (q.group == 0) {
+        GPTQ_LAUNCH(K_ROW_PARAMS, s, row_params_kernel<<<pgrid, 256, 0, s>>>(w.W, rows, cols, 0, cols, q.bits, q.sym,
+                                                                             w.cur_s, w.cur_z, scales, zeros, G, 0));
+        GPTQ_LAUNCH_CHECK();
+    }
+
+    constexpr int TPR = 4;
+    const size_t smem = sizeof(float) * QB * QB;
+    GPTQ_CUDA_TRY(cudaFuncSetAttribute(gptq_block_kernel<TPR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    BlockArgs a{};
+    a.Wk = w.W;
+    a.rows = rows;
+    a.cols = cols;
+    a.U = U;
+    a.bits = q.bits;
+    a.sym = q.sym;
+    a.group = q.group;
+    a.cur_s = w.cur_s;
+    a.cur_z = w.cur_z;
+    a.Err = w.Err;
+    a.codes = codes;
+    a.Wq = Wq;
+    a.perm = perm;
+    a.scales = scales;
+    a.zeros = zeros;
+    a.G = G;
+    a.loss = w.loss;
+    const unsigned bgrid = (unsigned)ceil_div(rows, 128 / TPR);
+    for (int64_t j0 = 0; j0 < cols; j0 += QB) {
+        const int bw = (int)std::min<int64_t>(QB, cols - j0);
+        if (q.group > QB && j0 % q.group == 0) {
+            GPTQ_LAUNCH(K_ROW_PARAMS, s,
+                        row_params_kernel<<<pgrid, 256, 0, s>>>(w.W, rows, cols, j0,
+                                                                std::min<int64_t>(cols, j0 + q.group), q.bits, q.sym,
+                                                                w.cur_s, w.cur_z, scales, zeros, G, j0 / q.group));
+            GPTQ_LAUNCH_CHECK();
+        }
+        a.j0 = j0;
+        a.bw = bw;
+        GPTQ_LAUNCH(K_BLOCK, s, gptq_block_kernel<TPR><<<bgrid, 128, smem, s>>>(a));
+        GPTQ_LAUNCH_CHECK();
+        const int64_t e = j0 + bw;
+        if (e < cols) {
+            GPTQ_CUDA_TRY(sgemm(K_SGEMM_TRAIL, false, (int)rows, (int)(cols - e), bw, -1.0f, w.Err, QB, U + j0 * cols + e, cols, 1.0f,
+                                w.W + e, cols, false, s));
+        }
+    }
+    (void)sym;
+
+    if (g_idx) {
+        GPTQ_LAUNCH(K_G_IDX, s, g_idx_kernel<<<(unsigned)ceil_div(cols, 256), 256, 0, s>>>(perm, cols, q.group, g_idx));
+        GPTQ_LAUNCH_CHECK();
+    }
+    if (row_loss) {
+        GPTQ_LAUNCH(K_COPY_LOSS, s, copy_loss_kernel<<<(unsigned)ceil_div(rows, 256), 256, 0, s>>>(w.loss, rows, row_loss));
+        GPTQ_LAUNCH_CHECK();
+    }
+    if (packed) return launch_pack(codes, rows, cols, q.bits, q.sym, packed, s);
+    return GPTQ_OK;
+}
+
+extern "C" int rtn_quantize(const float* W, int64_t rows, int64_t cols, const uint8_t* dead, gptq_qconfig q,
+                            int8_t* codes, float* scales, uint8_t* zeros, float* Wq, uint32_t* packed, void* stream) {
+    if (rows < 0 || cols < 0) return GPTQ_ERR_INVALID_ARG;
+    if (q.bits < 2 || q.bits > 4 || q.group < 0) return GPTQ_ERR_UNSUPPORTED;
+    if (rows == 0 || cols == 0) return GPTQ_OK;
+    if (!W || !codes || !scales || !zeros || rows > 65535) return GPTQ_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (q.group == 0) {
+        GPTQ_LAUNCH(K_RTN, s, rtn_row_kernel<<<(unsigned)rows, 256, 0, s>>>(W, rows, cols, dead, q.bits, q.sym, codes, scales, zeros, Wq));
+    } else {
+        const int64_t G = ceil_div(cols, q.group);
+        const int64_t tasks = rows * G;
+        GPTQ_LAUNCH(K_RTN, s,
+                    rtn_group_kernel<<<(unsigned)ceil_div(tasks, 8), 256, 0, s>>>(W, rows, cols, dead, q.bits, q.sym,
+                                                                                  q.group, G, codes, scales, zeros, Wq));
+    }
+    GPTQ_LAUNCH_CHECK();
+    if (packed) return launch_pack(codes, rows, cols, q.bits, q.sym, packed, s);
+    return GPTQ_OK;
+}
+
+extern "C" const char* gptq_status_string(int status) {
+    switch (status) {
+        case GPTQ_OK: return "ok";
+        case GPTQ_ERR_INVALID_ARG: return "invalid argument";
+        case GPTQ_ERR_UNSUPPORTED: return "unsupported configuration";
+        case GPTQ_ERR_NOT_SPD: return "Hessian not positive definite (Cholesky pivot <= 0)";
+        case GPTQ_ERR_CUDA: return "CUDA error";
+        case GPTQ_ERR_TIMEOUT: return "on-device wait timed out";
+        case GPTQ_ERR_WORKSPACE: return "workspace too small";
+        default: return "unknown status";
+    }
+}

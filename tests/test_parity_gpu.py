@@ -1,0 +1,235 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle, stage by stage.
+
+Tolerances:
+  H        relative Frobenius <= 1e-5 against fp64 H on the same bf16/fp32 bits
+  U        relative Frobenius <= 1e-4, the GPU prepare fed the oracle's H rounded to fp32
+  codes    given the oracle's U: >= 99.99% identical, every mismatch within 1e-4 (code
+           units) of a rounding half-point, checked by the teacher-forced oracle
+  RTN, packing, perm, dead, g_idx: bit-exact
+  end to end: relative output error within 2% of the oracle's
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def rel_fro(a, b):
+    return float(np.linalg.norm(np.asarray(a, np.float64) - b) / np.linalg.norm(b))
+
+
+def npy(t):
+    return t.detach().cpu().numpy()
+
+
+def f32(a):
+    return np.asarray(a, np.float64).astype(np.float32)
+
+
+def x_case(n, d, seed, dead_frac=0.0, kind="scaled", dtype="bf16"):
+    spec = synth.XSpec(n=n, d=d, kind=kind, dtype=dtype, n_outliers=max(1, d // 64), outlier_factor=20.0,
+                       dead_frac=dead_frac, segment=1024)
+    return synth.make_x(spec, seed, device=DEV)
+
+
+# ------------------------------------------------------------------------------ Hessian
+
+@pytest.mark.parametrize("n,d,dtype", [(512, 256, "f32"), (4096, 256, "bf16"), (8192, 768, "bf16"),
+                                       (3000, 384, "bf16"), (1000, 200, "bf16"), (9000, 1024, "bf16"),
+                                       (777, 136, "f32")])
+def test_hessian_matches_oracle(lib, n, d, dtype):
+    X = x_case(n, d, 10 + d, dead_frac=0.02, dtype=dtype)
+    h = lib.Hessian(d)
+    h.accumulate(X)
+    H, diag, nn = h.finalize()
+    Xh = synth.to_numpy_f64(X)
+    S = O.xtx(Xh)
+    Href = O.hessian_from_sum(S, n)
+    assert nn == n
+    assert rel_fro(npy(H), Href) <= 1e-5
+    np.testing.assert_allclose(npy(diag), np.diag(S), rtol=2e-5, atol=0)
+    Hg = npy(H)
+    np.testing.assert_array_equal(Hg, Hg.T)                      # both triangles written
+    dead = np.diag(Href) == 0
+    assert np.all(np.diag(Hg)[dead] == 0)                        # dead channels stay exactly 0
+
+
+def test_hessian_streaming_equals_one_call(lib):
+    d = 512
+    X = x_case(6000, d, 77)
+    a = lib.Hessian(d)
+    a.accumulate(X)
+    Ha, _, _ = a.finalize()
+    b = lib.Hessian(d)
+    for r in range(0, 6000, 2048):
+        b.accumulate(X[r:r + 2048])
+    Hb, _, n = b.finalize()
+    assert n == 6000
+    Href = O.hessian(synth.to_numpy_f64(X))
+    assert rel_fro(npy(Hb), Href) <= 1e-5
+    assert rel_fro(npy(Ha), npy(Hb).astype(np.float64)) <= 1e-5
+    b.reset()
+    b.accumulate(X[:100])
+    Hc, _, n = b.finalize()
+    assert n == 100 and rel_fro(npy(Hc), O.hessian(synth.to_numpy_f64(X[:100]))) <= 1e-5
+
+
+def test_hessian_bf16_unaligned_rows_use_simt_path(lib):
+    d = 200
+    base = x_case(1500, d + 1, 5)
+    X = base[:, :d]                                              # row stride 201 elements: not TMA-addressable
+    h = lib.Hessian(d)
+    h.accumulate(X)
+    H, _, _ = h.finalize()
+    assert rel_fro(npy(H), O.hessian(synth.to_numpy_f64(X))) <= 1e-5
+
+
+# ------------------------------------------------------------------------------ prepare
+
+def _h_for(d, seed, dead_frac=0.02, n=None):
+    X = x_case(n or 4 * d, d, seed, dead_frac=dead_frac)
+    Xh = synth.to_numpy_f64(X)
+    S = O.xtx(Xh)
+    H32 = f32(O.hessian_from_sum(S, Xh.shape[0]))
+    return H32, f32(np.diag(S)), Xh
+
+
+@pytest.mark.parametrize("d,act_order", [(256, False), (768, False), (300, True), (1000, True), (129, False),
+                                         (2048, True)])
+def test_prepare_matches_oracle(lib, d, act_order):
+    H32, diag32, _ = _h_for(d, 100 + d)
+    U, perm, dead = lib.gptq_prepare(torch.tensor(H32, device=DEV), torch.tensor(diag32, device=DEV), 0.01,
+                                     act_order=act_order)
+    Uref, pref, dref = O.prepare(H32.astype(np.float64), 0.01, act_order, diag32.astype(np.float64))
+    np.testing.assert_array_equal(npy(perm), pref)
+    np.testing.assert_array_equal(npy(dead).astype(bool), dref)
+    Ug = npy(U)
+    assert np.all(np.tril(Ug, -1) == 0)
+    assert np.all(np.diag(Ug) > 0)
+    assert rel_fro(Ug, Uref) <= 1e-4
+
+
+def test_prepare_reports_not_spd(lib):
+    H = torch.tensor([[1.0, 2.0], [2.0, 1.0]], device=DEV)
+    with pytest.raises(lib.GptqError) as e:
+        lib.gptq_prepare(H, None, 0.0)
+    assert e.value.status == 3
+
+
+# ----------------------------------------------------------------------------- quantize
+
+QCASES = [
+    # rows, cols, bits, group, sym, act_order
+    (128, 256, 4, 0, True, False),
+    (96, 384, 4, 128, False, False),
+    (64, 300, 3, 32, True, True),
+    (48, 512, 2, 256, True, False),
+    (33, 200, 4, 64, False, True),
+    (130, 640, 3, 128, True, True),
+    (40, 384, 2, 128, False, False),
+]
+
+
+@pytest.mark.parametrize("rows,cols,bits,group,sym,act", QCASES)
+def test_quantize_given_oracle_u(lib, rows, cols, bits, group, sym, act):
+    H32, diag32, _ = _h_for(cols, 200 + cols + rows)
+    Uref, perm, dead = O.prepare(H32.astype(np.float64), 0.01, act, diag32.astype(np.float64))
+    U32 = f32(Uref)
+    W = synth.make_weight(rows, cols, 0.02, 300 + rows, device=DEV)
+    Wh = synth.to_numpy_f64(W)
+    out = lib.gptq_quantize(W, torch.tensor(U32, device=DEV), torch.tensor(perm.astype(np.int32), device=DEV),
+                            torch.tensor(dead.astype(np.uint8), device=DEV), bits, group, sym)
+    codes = npy(out["codes"]).astype(np.int64)
+    zeros = npy(out["zeros"]).astype(np.int64)
+    ref = O.gptq_quantize(Wh, U32.astype(np.float64), perm, dead, bits, group, sym, forced_codes=codes,
+                          forced_zeros=None if sym else zeros)
+    nmis = len([t for t in ref["ties"] if t[2] == "code"])
+    assert nmis <= 1e-4 * codes.size + 0.5, ref["ties"]
+    np.testing.assert_array_equal(codes, ref["codes"])
+    np.testing.assert_allclose(npy(out["scales"]), ref["scales"], rtol=2e-5, atol=0)
+    np.testing.assert_array_equal(zeros, ref["zeros"])
+    np.testing.assert_allclose(npy(out["Wq"]), ref["Wq"], rtol=2e-5, atol=1e-7)
+    np.testing.assert_array_equal(npy(out["g_idx"]), ref["g_idx"])
+    np.testing.assert_array_equal(npy(out["packed"]).view(np.uint32), ref["packed"])
+    np.testing.assert_allclose(npy(out["row_loss"]), ref["err_sq"], rtol=1e-3)
+    assert np.all(npy(out["Wq"])[:, dead] == 0)
+
+
+# ---------------------------------------------------------------------------------- RTN
+
+@pytest.mark.parametrize("rows,cols,bits,group,sym", [(64, 256, 4, 0, True), (64, 256, 4, 128, False),
+                                                      (37, 300, 3, 64, True), (16, 1000, 2, 128, True),
+                                                      (9, 77, 3, 0, False)])
+def test_rtn_bit_exact(lib, rows, cols, bits, group, sym):
+    W = synth.make_weight(rows, cols, 0.05, 400 + cols, device=DEV)
+    dead = torch.zeros(cols, dtype=torch.uint8, device=DEV)
+    dead[::17] = 1
+    out = lib.rtn_quantize(W, bits, group, sym, dead=dead)
+    ref = O.rtn_quantize(synth.to_numpy_f64(W), bits, group, sym, dead=npy(dead).astype(bool))
+    np.testing.assert_array_equal(npy(out["codes"]).astype(np.int64), ref["codes"])
+    np.testing.assert_array_equal(npy(out["scales"]), f32(ref["scales"]))
+    np.testing.assert_array_equal(npy(out["zeros"]).astype(np.int64), ref["zeros"])
+    np.testing.assert_array_equal(npy(out["Wq"]), f32(ref["Wq"]))
+    np.testing.assert_array_equal(npy(out["packed"]).view(np.uint32), ref["packed"])
+
+
+@pytest.mark.parametrize("bits,sym,cols", [(2, True, 64), (3, True, 96), (3, False, 100), (4, False, 33)])
+def test_pack_bit_exact(lib, bits, sym, cols):
+    rng = np.random.default_rng(bits * 100 + cols)
+    lo, hi = (-(2 ** (bits - 1) - 1), 2 ** (bits - 1) - 1) if sym else (0, 2 ** bits - 1)
+    codes = rng.integers(lo, hi + 1, size=(11, cols))
+    p = lib.gptq_pack(torch.tensor(codes.astype(np.int8), device=DEV), bits, sym)
+    np.testing.assert_array_equal(npy(p).view(np.uint32), O.pack_rows(O.unsigned_codes(codes, bits, sym), bits))
+
+
+# ---------------------------------------------------------------------------- end to end
+
+def _layer_gpu(lib, X, Ws, bits, group, sym, act_order, damp=0.01):
+    h = lib.Hessian(X.shape[1])
+    h.accumulate(X)
+    H, diag, _ = h.finalize()
+    U, perm, dead = lib.gptq_prepare(H, diag, damp, act_order=act_order)
+    outs = [lib.gptq_quantize(W, U, perm, dead, bits, group, sym) for W in Ws]
+    return outs, (H, U, perm, dead)
+
+
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_end_to_end_output_error(lib, cfg):
+    wl = synth.workload(cfg)
+    L = wl.layers[0]
+    X = synth.make_x(L.x, synth.x_seed(cfg, L.x), device=DEV)
+    Ws = [synth.make_weight(w.out, w.inp, w.std, synth.weight_seed(cfg, w.name), device=DEV) for w in L.weights]
+    outs, (H, U, perm, dead) = _layer_gpu(lib, X, Ws, L.q.bits, L.q.group, L.q.sym, L.q.act_order)
+    Xh = synth.to_numpy_f64(X)
+    S = O.xtx(Xh)
+    for W, out in zip(Ws, outs):
+        Wh = synth.to_numpy_f64(W)
+        ref = O.gptq_layer(Wh, Xh, L.q.bits, L.q.group, L.q.sym, L.q.damp, L.q.act_order)
+        e_gpu = O.rel_output_error_from_xtx(S, Wh, npy(out["Wq"]))
+        e_ref = O.rel_output_error_from_xtx(S, Wh, ref["Wq"])
+        assert abs(e_gpu - e_ref) <= 0.02 * e_ref, (e_gpu, e_ref)
+        rtn = lib.rtn_quantize(W, L.q.bits, L.q.group, L.q.sym, dead=dead)
+        e_rtn = O.rel_output_error_from_xtx(S, Wh, npy(rtn["Wq"]))
+        assert e_gpu < e_rtn, (e_gpu, e_rtn)
+        np.testing.assert_array_equal(npy(dead).astype(bool), ref["dead"])
+
+
+@pytest.mark.parametrize("group,sym", [(0, True), (64, True), (128, False)])
+def test_diagonal_hessian_gives_rtn_on_gpu(lib, group, sym):
+    """X = Hadamard columns: H = 2I exactly in fp32, U diagonal, GPTQ == RTN bit for bit."""
+    spec = synth.XSpec(n=512, d=256, kind="hadamard", dtype="bf16")
+    X = synth.make_x(spec, 0, device=DEV)
+    W = synth.make_weight(128, 256, 0.1, 7, device=DEV)
+    outs, (H, U, perm, dead) = _layer_gpu(lib, X, [W], 4, group, sym, False)
+    assert torch.equal(H, 2 * torch.eye(256, device=DEV))
+    Ug = npy(U)
+    assert np.count_nonzero(Ug - np.diag(np.diag(Ug))) == 0
+    r = lib.rtn_quantize(W, 4, group, sym)
+    assert torch.equal(outs[0]["codes"], r["codes"])
+    assert torch.equal(outs[0]["packed"], r["packed"])
