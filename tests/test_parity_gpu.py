@@ -29,7 +29,7 @@ def npy(t):
 
 
 def f32(a):
-    return np.asarray(a, np.float64).astype(np.float32)
+    return np.ascontiguousarray(np.asarray(a, np.float64).astype(np.float32))
 
 
 def x_case(n, d, seed, dead_frac=0.0, kind="scaled", dtype="bf16"):
