@@ -109,6 +109,20 @@ size_t gptq_prepare_workspace_bytes(int64_t d, int act_order);
 int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, float damp, int act_order,
                  float* U, int32_t* perm, uint8_t* dead, void* ws, size_t ws_bytes, void* stream);
 
+/* gptq_prepare without a caller workspace, for callers that cannot allocate device
+ * memory (a host framework that owns all device memory through its own pool, or a path
+ * that cannot take cudaMalloc's implicit synchronisation). No counterpart on the pages.
+ * Same arguments, outputs, synchronisation and errors as gptq_prepare, minus ws/ws_bytes.
+ * The scratch is a fixed array compiled into the library (about 8.5 MiB, held on every
+ * GPU that loads the library until the process exits), so d is limited to 1024:
+ * d > 1024 returns GPTQ_ERR_UNSUPPORTED. Allocates nothing (no cudaMalloc/cudaFree).
+ * The first call on a device looks up that device's copy of the array
+ * (cudaGetSymbolAddress); make that first call before any stream capture. All calls share
+ * the one array, so calls that overlap on the GPU (other streams, other threads) race;
+ * serialise them. Errors: INVALID_ARG, UNSUPPORTED, NOT_SPD, CUDA. */
+int gptq_prepare_noalloc(const float* H, const float* diag_xtx, int64_t d, float damp,
+                         int act_order, float* U, int32_t* perm, uint8_t* dead, void* stream);
+
 /* ------------------------------------------------------------------------------------
  * Quantisation.  GPTQ's error-compensation loop page (the four steps); GPTQ guide page,
  * "Source code" (`gptq`), "When it breaks" (clipping; g_idx); AutoGPTQ page

@@ -29,7 +29,8 @@ STATUS = {
 # every symbol include/gptq.h declares
 EXPORTS = [
     "gptq_hessian_create", "gptq_hessian_reset", "gptq_hessian_accumulate", "gptq_hessian_finalize",
-    "gptq_hessian_destroy", "gptq_prepare_workspace_bytes", "gptq_prepare", "gptq_quantize_workspace_bytes",
+    "gptq_hessian_destroy", "gptq_prepare_workspace_bytes", "gptq_prepare", "gptq_prepare_noalloc",
+    "gptq_quantize_workspace_bytes",
     "gptq_quantize", "rtn_quantize", "gptq_packed_words_per_row", "gptq_pack", "gptq_status_string",
     "gptq_launch_count", "gptq_profile_enable", "gptq_profile_read", "gptq_profile_kernel_count",
     "gptq_profile_kernel_name",
@@ -64,6 +65,7 @@ def _declare(lib: ctypes.CDLL) -> None:
         "gptq_hessian_destroy": (_I, [_P]),
         "gptq_prepare_workspace_bytes": (_SZ, [_I64, _I]),
         "gptq_prepare": (_I, [_P, _P, _I64, _F, _I, _P, _P, _P, _P, _SZ, _P]),
+        "gptq_prepare_noalloc": (_I, [_P, _P, _I64, _F, _I, _P, _P, _P, _P]),
         "gptq_quantize_workspace_bytes": (_SZ, [_I64, _I64, QConfig]),
         "gptq_quantize": (_I, [_P, _I64, _I64, _P, _P, _P, QConfig, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
         "rtn_quantize": (_I, [_P, _I64, _I64, _P, QConfig, _P, _P, _P, _P, _P, _P]),

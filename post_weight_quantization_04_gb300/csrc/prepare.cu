@@ -319,3 +319,76 @@ extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, fl
     GPTQ_CUDA_TRY(cudaStreamSynchronize(s));
     return hstatus;
 }
+
+// ------------------------------------------------------------------------------------
+// gptq_prepare_noalloc: gptq_prepare for callers that cannot allocate device memory.
+//
+// Some callers of this library cannot call cudaMalloc for the workspace: a host
+// framework that owns every byte of device memory through its own pool and hands out
+// nothing extra, or a latency-sensitive path that cannot take cudaMalloc's implicit
+// device synchronisation. For them this entry point uses a fixed scratch area compiled
+// into the library as a file-scope __device__ array, sized for d <= kNoAllocMaxD.
+// Every GPU that loads the library holds this array (about 8.5 MiB) until the process
+// exits. The entry point itself allocates nothing: no cudaMalloc, cudaFree or allocating
+// library routine.
+// ------------------------------------------------------------------------------------
+#include <mutex>
+
+namespace gptq {
+namespace {
+
+constexpr int64_t kNoAllocMaxD = 1024;
+
+constexpr size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// the same slab sizes gptq_prepare carves from its workspace, for d = kNoAllocMaxD
+constexpr size_t noalloc_bytes(int64_t d) {
+    return a256(a256(a256(a256(a256(a256(sizeof(float) * d * d) + sizeof(float) * d * d) +
+                                    sizeof(float) * ((d + NB - 1) / NB) * NB * NB) +
+                               sizeof(float) * d) +
+                          sizeof(float) * d) +
+                     sizeof(int) * 4);
+}
+
+constexpr size_t kNoAllocBytes = noalloc_bytes(kNoAllocMaxD);
+constexpr int kMaxDevices = 64;
+
+// Host code must not use this name as an address: on the host it is only a stand-in for
+// the device symbol. The device address comes from cudaGetSymbolAddress, per device.
+static __device__ __align__(256) unsigned char g_prepare_scratch[kNoAllocBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+}  // namespace
+}  // namespace gptq
+
+extern "C" int gptq_prepare_noalloc(const float* H, const float* diag_xtx, int64_t d, float damp, int act_order,
+                                    float* U, int32_t* perm, uint8_t* dead, void* stream) {
+    using namespace gptq;
+    if (d <= 0) return GPTQ_ERR_INVALID_ARG;
+    if (d > kNoAllocMaxD) return GPTQ_ERR_UNSUPPORTED;
+    const size_t need = gptq_prepare_workspace_bytes(d, act_order);
+    if (need > kNoAllocBytes) return GPTQ_ERR_UNSUPPORTED;
+    int dev = 0;
+    GPTQ_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return GPTQ_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    {
+        // first call on a device: look up this device's copy of the array (once)
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            void* p = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&p, g_prepare_scratch);
+            if (e != cudaSuccess || p == nullptr) {
+                (void)cudaGetLastError();
+                return GPTQ_ERR_CUDA;
+            }
+            g_noalloc_ptr[dev] = p;
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    // every slab gptq_prepare reads is written by it first (its status word is cleared),
+    // so the previous call's contents need no clearing here
+    return gptq_prepare(H, diag_xtx, d, damp, act_order, U, perm, dead, scratch, kNoAllocBytes, stream);
+}
