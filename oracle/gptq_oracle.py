@@ -277,7 +277,9 @@ def gptq_loop(W, U, bits: int, group: int = 0, sym: bool = True, scale_dtype=np.
         zeros[:, gi] = zero
         return scale, zero
 
-    scale, zero = take_params(W, 0, 0)          # per row, from the starting weights
+    scale = zero = None
+    if not group:
+        scale, zero = take_params(W, 0, 0)      # per row, from the starting weights
     for j in range(d):
         if group and j % group == 0:            # group scales use the *updated* weights
             scale, zero = take_params(W[:, j:j + group], j // group, j)
