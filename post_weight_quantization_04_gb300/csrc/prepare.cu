@@ -148,22 +148,25 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
 // One CTA factors the diagonal block A[k0:k0+n, k0:k0+n] = L L^T in place (lower), and
 // writes L^-1 (lower, NB x NB, zeros above) to Linv. A non-positive or non-finite pivot
 // records GPTQ_ERR_NOT_SPD (and is replaced by 1 so the kernel finishes).
+// 512 threads: thread t owns row i = t / 4 and the columns j = q (mod 4), q = t % 4.
 __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, int64_t lda, int64_t k0, int n,
                                                         float* __restrict__ Linv, int* __restrict__ status) {
     extern __shared__ float sm[];
-    float* S = sm;                    // NB x (NB+1)
-    float* X = sm + NB * (NB + 1);    // NB x (NB+1)
-    __shared__ float part[4][NB];
-    const int tid = threadIdx.x, nt = blockDim.x;
     constexpr int LD = NB + 1;
+    float* S = sm;              // NB x LD: the block, then L
+    float* X = sm + NB * LD;    // NB x LD: L^-1
+    __shared__ float part[4][NB];
+    const int tid = threadIdx.x;
+    const int i = tid >> 2, q = tid & 3;
 
-    for (int idx = tid; idx < NB * NB; idx += nt) {
-        const int i = idx / NB, j = idx % NB;
+#pragma unroll
+    for (int j = q; j < NB; j += 4) {
         S[i * LD + j] = (i < n && j <= i) ? A[(k0 + i) * lda + k0 + j] : 0.0f;
         X[i * LD + j] = 0.0f;
     }
     __syncthreads();
 
+    // right-looking column Cholesky
     for (int k = 0; k < n; ++k) {
         float piv = S[k * LD + k];
         if (!(piv > 0.0f) || !isfinite(piv)) {
@@ -171,47 +174,41 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, 
             piv = 1.0f;
         }
         const float lkk = sqrtf(piv);
-        const float inv = 1.0f / lkk;
-        __syncthreads();
-        for (int i = k + 1 + tid; i < n; i += nt) S[i * LD + k] *= inv;
+        __syncthreads();                                   // everyone has read the pivot
+        if (q == 0 && i > k && i < n) S[i * LD + k] = S[i * LD + k] / lkk;
         if (tid == 0) S[k * LD + k] = lkk;
         __syncthreads();
-        const int m = n - k - 1;
-        for (int idx = tid; idx < m * m; idx += nt) {
-            const int i = k + 1 + idx / m, j = k + 1 + idx % m;
-            if (j <= i) S[i * LD + j] = fmaf(-S[i * LD + k], S[j * LD + k], S[i * LD + j]);
+        if (i > k && i < n) {
+            const float lik = S[i * LD + k];
+            for (int j = k + 1 + ((q - k - 1) & 3); j <= i; j += 4)
+                S[i * LD + j] = fmaf(-lik, S[j * LD + k], S[i * LD + j]);
         }
         __syncthreads();
     }
+#pragma unroll
+    for (int j = q; j < NB; j += 4)
+        if (i < n && j <= i) A[(k0 + i) * lda + k0 + j] = S[i * LD + j];
 
-    for (int idx = tid; idx < n * NB; idx += nt) {
-        const int i = idx / NB, j = idx % NB;
-        if (j <= i) A[(k0 + i) * lda + k0 + j] = S[i * LD + j];
-    }
-
-    // L^-1 by rows: X[i][c] = (delta_ic - sum_{c<=m<i} L[i][m] X[m][c]) / L[i][i];
-    // four threads share each column c's dot product.
-    const int c = tid & (NB - 1), q = tid >> 7;  // q in 0..3
-    for (int i = 0; i < n; ++i) {
+    // L^-1 by rows: X[r][c] = (delta_rc - sum_{c<=m<r} L[r][m] X[m][c]) / L[r][r];
+    // column c's dot product is split over four threads (cq = 0..3)
+    const int c = tid & (NB - 1), cq = tid >> 7;
+    for (int r = 0; r < n; ++r) {
         float s = 0.0f;
-        if (c < i) {
-            const int len = i - c;
-            const int per = (len + 3) >> 2;
-            const int mb = c + q * per, me = min(i, mb + per);
-            for (int m = mb; m < me; ++m) s = fmaf(S[i * LD + m], X[m * LD + c], s);
+        if (c < r) {
+            const int per = (r - c + 3) >> 2;
+            const int mb = c + cq * per, me = min(r, mb + per);
+            for (int m = mb; m < me; ++m) s = fmaf(S[r * LD + m], X[m * LD + c], s);
         }
-        part[q][c] = s;
+        part[cq][c] = s;
         __syncthreads();
-        if (q == 0 && c <= i) {
-            const float tot = part[0][c] + part[1][c] + part[2][c] + part[3][c];
-            X[i * LD + c] = ((c == i ? 1.0f : 0.0f) - tot) / S[i * LD + i];
+        if (cq == 0 && c <= r) {
+            const float tot = (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
+            X[r * LD + c] = ((c == r ? 1.0f : 0.0f) - tot) / S[r * LD + r];
         }
         __syncthreads();
     }
-    for (int idx = tid; idx < NB * NB; idx += nt) {
-        const int i = idx / NB, j = idx % NB;
-        Linv[idx] = (i < n && j <= i) ? X[i * LD + j] : 0.0f;
-    }
+#pragma unroll
+    for (int j = q; j < NB; j += 4) Linv[i * NB + j] = (i < n && j <= i) ? X[i * LD + j] : 0.0f;
 }
 
 __global__ void eye_kernel(float* __restrict__ B, int64_t d) {

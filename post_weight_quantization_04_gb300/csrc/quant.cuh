@@ -40,17 +40,19 @@ __device__ __forceinline__ Grid asym_grid(float mn, float mx, int maxq) {
     return Grid{s, 1.0f / s, (float)z};
 }
 
+// round(w / s (+ z)) with the quotient taken in fp64 (IEEE division); kept out of line so
+// the rare near-half-point case does not weigh on the common path
+__device__ __noinline__ float quotient_rint_f64(float w, float s, float z, int sym) {
+    double td = (double)w / (double)s;
+    if (!sym) td += (double)z;
+    return (float)rint(td);
+}
+
 // Integer code of w on the grid, clamped to [lo, hi].
 __device__ __forceinline__ int grid_code(float w, const Grid& g, bool sym, int lo, int hi) {
     const float t = sym ? w * g.inv_s : fmaf(w, g.inv_s, g.z);
-    float r;
-    if (fabsf(t - floorf(t) - 0.5f) < 1e-3f) {
-        double td = (double)w / (double)g.s;
-        if (!sym) td += (double)g.z;
-        r = (float)rint(td);
-    } else {
-        r = rintf(t);
-    }
+    float r = rintf(t);
+    if (fabsf(t - floorf(t) - 0.5f) < 1e-3f) r = quotient_rint_f64(w, g.s, g.z, sym ? 1 : 0);
     r = fminf(fmaxf(r, (float)lo), (float)hi);
     return (int)r;
 }

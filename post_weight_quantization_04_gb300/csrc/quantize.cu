@@ -120,20 +120,47 @@ struct BlockArgs {
     float* loss;
 };
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// One 128-column block of the loop. TPR threads share a row; thread `sub` owns the
+// 4-column chunks sub, sub+TPR, sub+2*TPR, ... of the block (CPT columns in registers),
+// so the TPR lanes of a row read one contiguous 16*TPR-byte span of U's row per step.
 template <int TPR>
 __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
-    constexpr int CPT = QB / TPR;
+    constexpr int CPT = QB / TPR;   // columns per thread
+    constexpr int NCH = CPT / 4;    // 4-column chunks per thread
     constexpr int RPC = 128 / TPR;  // rows per CTA
-    extern __shared__ float us[];   // QB x QB block of U (zeros below the diagonal)
+    extern __shared__ __align__(16) float us[];  // QB x QB block of U, zeros below the diagonal
     __shared__ float invd[QB];
 
     const int bw = a.bw;
-    for (int idx = threadIdx.x; idx < QB * QB; idx += blockDim.x) {
-        const int i = idx / QB, c = idx % QB;
-        us[idx] = (i < bw && c < bw && c >= i) ? a.U[(a.j0 + i) * a.cols + a.j0 + c] : 0.0f;
+    const bool full = (bw == QB) && ((a.cols & 3) == 0);
+    if (full) {
+        const float* src = a.U + a.j0 * a.cols + a.j0;
+#pragma unroll 8
+        for (int v = threadIdx.x; v < QB * QB / 4; v += 128) {
+            const int i = v >> 5, c4 = (v & 31) << 2;
+            cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(us + i * QB + c4)), src + i * a.cols + c4);
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        // zero the block left of the diagonal: warp w takes rows w, w+4, ..., lanes the columns
+        for (int i = threadIdx.x >> 5; i < QB; i += 4)
+            for (int c = threadIdx.x & 31; c < i; c += 32) us[i * QB + c] = 0.0f;
+    } else {
+#pragma unroll 4
+        for (int idx = threadIdx.x; idx < QB * QB; idx += blockDim.x) {
+            const int i = idx / QB, c = idx % QB;
+            us[idx] = (i < bw && c < bw && c >= i) ? a.U[(a.j0 + i) * a.cols + a.j0 + c] : 0.0f;
+        }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < QB; i += blockDim.x) invd[i] = (i < bw) ? 1.0f / us[i * QB + i] : 0.0f;
+    invd[threadIdx.x] = (threadIdx.x < bw) ? 1.0f / us[threadIdx.x * QB + threadIdx.x] : 0.0f;
     __syncthreads();
 
     const int sub = threadIdx.x % TPR;
@@ -144,15 +171,31 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
     const int lo = sym ? -qmax : 0, hi = qmax;
     const bool inblock_groups = a.group > 0 && a.group <= QB;
 
+    // block column of this thread's element (m, e): chunk m*TPR + sub, element e
+    auto col_of = [&](int m, int e) { return (m * TPR + sub) * 4 + e; };
+
     float w[CPT], er[CPT], qr[CPT];
     int8_t cr[CPT];
-    const float* wrow = a.Wk + (active ? row : 0) * a.cols + a.j0 + sub * CPT;
+    const float* wrow = a.Wk + (active ? row : 0) * a.cols + a.j0;
 #pragma unroll
-    for (int k = 0; k < CPT; ++k) {
-        w[k] = (active && sub * CPT + k < bw) ? wrow[k] : 0.0f;
-        er[k] = 0.0f;
-        qr[k] = 0.0f;
-        cr[k] = 0;
+    for (int m = 0; m < NCH; ++m) {
+        const int c0 = col_of(m, 0);
+        if (full && active) {
+            const float4 v = *reinterpret_cast<const float4*>(wrow + c0);
+            w[4 * m] = v.x;
+            w[4 * m + 1] = v.y;
+            w[4 * m + 2] = v.z;
+            w[4 * m + 3] = v.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[4 * m + e] = (active && c0 + e < bw) ? wrow[c0 + e] : 0.0f;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            er[4 * m + e] = 0.0f;
+            qr[4 * m + e] = 0.0f;
+            cr[4 * m + e] = 0;
+        }
     }
     Grid g{1.0f, 1.0f, 0.0f};
     if (!inblock_groups && active) {
@@ -161,70 +204,81 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
         g.z = a.cur_z[row];
     }
     float loss = 0.0f;
+    int next_gs = 0;  // next in-block group start
 
-    for (int o = 0; o < TPR; ++o) {
 #pragma unroll
-        for (int k = 0; k < CPT; ++k) {
-            const int jj = o * CPT + k;
-            if (jj >= bw) break;
-            if (inblock_groups && (jj % a.group) == 0) {
-                const int gend = min(jj + a.group, bw);
-                float am = 0.0f, mx = -INFINITY, mn = INFINITY;
+    for (int m = 0; m < NCH; ++m) {
+        for (int o = 0; o < TPR; ++o) {
 #pragma unroll
-                for (int kk = 0; kk < CPT; ++kk) {
-                    const int c = sub * CPT + kk;
-                    if (c >= jj && c < gend) {
-                        am = fmaxf(am, fabsf(w[kk]));
-                        mx = fmaxf(mx, w[kk]);
-                        mn = fminf(mn, w[kk]);
+            for (int e = 0; e < 4; ++e) {
+                const int jj = (m * TPR + o) * 4 + e;
+                if (jj >= bw) break;
+                if (inblock_groups && jj == next_gs) {
+                    next_gs += a.group;
+                    const int gend = min(jj + a.group, bw);
+                    float am = 0.0f, mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+                    for (int mm = 0; mm < NCH; ++mm)
+#pragma unroll
+                        for (int ee = 0; ee < 4; ++ee) {
+                            const int c = col_of(mm, ee);
+                            if (c >= jj && c < gend) {
+                                const float v = w[4 * mm + ee];
+                                am = fmaxf(am, fabsf(v));
+                                mx = fmaxf(mx, v);
+                                mn = fminf(mn, v);
+                            }
+                        }
+#pragma unroll
+                    for (int off = TPR / 2; off > 0; off >>= 1) {
+                        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off, TPR));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off, TPR));
+                        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off, TPR));
+                    }
+                    g = sym ? sym_grid(am, qmax) : asym_grid(mn, mx, qmax);
+                    if (active && sub == 0) {
+                        const int64_t gi = (a.j0 + jj) / a.group;
+                        a.scales[row * a.G + gi] = g.s;
+                        a.zeros[row * a.G + gi] = sym ? (uint8_t)(1 << (a.bits - 1)) : (uint8_t)g.z;
                     }
                 }
-#pragma unroll
-                for (int off = TPR / 2; off > 0; off >>= 1) {
-                    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off, TPR));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off, TPR));
-                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off, TPR));
+                const float wj = __shfl_sync(0xffffffffu, w[4 * m + e], o, TPR);
+                const int c = grid_code(wj, g, sym, lo, hi);
+                const float q = grid_dequant(c, g, sym);
+                const float err = (wj - q) * invd[jj];
+                if (sub == o) {
+                    cr[4 * m + e] = (int8_t)c;
+                    qr[4 * m + e] = q;
+                    er[4 * m + e] = err;
                 }
-                g = sym ? sym_grid(am, qmax) : asym_grid(mn, mx, qmax);
-                if (active && sub == 0) {
-                    const int64_t gi = (a.j0 + jj) / a.group;
-                    a.scales[row * a.G + gi] = g.s;
-                    a.zeros[row * a.G + gi] = sym ? (uint8_t)(1 << (a.bits - 1)) : (uint8_t)g.z;
-                }
-            }
-            const float wj = __shfl_sync(0xffffffffu, w[k], o, TPR);
-            const int c = grid_code(wj, g, sym, lo, hi);
-            const float q = grid_dequant(c, g, sym);
-            const float err = (wj - q) * invd[jj];
-            if (sub == o) {
-                cr[k] = (int8_t)c;
-                qr[k] = q;
-                er[k] = err;
-            }
-            loss = fmaf(err, err, loss);
-            const float* ur = us + jj * QB + sub * CPT;
+                loss = fmaf(err, err, loss);
+                const float* ur = us + jj * QB;
 #pragma unroll
-            for (int kk = 0; kk < CPT; kk += 4) {
-                const float4 u4 = *reinterpret_cast<const float4*>(ur + kk);
-                w[kk] = fmaf(-err, u4.x, w[kk]);
-                w[kk + 1] = fmaf(-err, u4.y, w[kk + 1]);
-                w[kk + 2] = fmaf(-err, u4.z, w[kk + 2]);
-                w[kk + 3] = fmaf(-err, u4.w, w[kk + 3]);
+                for (int mm = 0; mm < NCH; ++mm) {
+                    const float4 u4 = *reinterpret_cast<const float4*>(ur + col_of(mm, 0));
+                    w[4 * mm] = fmaf(-err, u4.x, w[4 * mm]);
+                    w[4 * mm + 1] = fmaf(-err, u4.y, w[4 * mm + 1]);
+                    w[4 * mm + 2] = fmaf(-err, u4.z, w[4 * mm + 2]);
+                    w[4 * mm + 3] = fmaf(-err, u4.w, w[4 * mm + 3]);
+                }
             }
         }
     }
 
     if (!active) return;
-    float* erow = a.Err + row * QB + sub * CPT;
+    float* erow = a.Err + row * QB;
 #pragma unroll
-    for (int k = 0; k < CPT; k += 4) *reinterpret_cast<float4*>(erow + k) = make_float4(er[k], er[k + 1], er[k + 2], er[k + 3]);
+    for (int m = 0; m < NCH; ++m) {
+        const int c0 = col_of(m, 0);
+        *reinterpret_cast<float4*>(erow + c0) = make_float4(er[4 * m], er[4 * m + 1], er[4 * m + 2], er[4 * m + 3]);
 #pragma unroll
-    for (int k = 0; k < CPT; ++k) {
-        const int lc = sub * CPT + k;
-        if (lc < bw) {
-            const int64_t oc = a.perm ? (int64_t)a.perm[a.j0 + lc] : a.j0 + lc;
-            a.codes[row * a.cols + oc] = cr[k];
-            if (a.Wq) a.Wq[row * a.cols + oc] = qr[k];
+        for (int e = 0; e < 4; ++e) {
+            const int lc = c0 + e;
+            if (lc < bw) {
+                const int64_t oc = a.perm ? (int64_t)a.perm[a.j0 + lc] : a.j0 + lc;
+                a.codes[row * a.cols + oc] = cr[4 * m + e];
+                if (a.Wq) a.Wq[row * a.cols + oc] = qr[4 * m + e];
+            }
         }
     }
     if (sub == 0) a.loss[row] += loss;
@@ -401,9 +455,20 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         GPTQ_LAUNCH_CHECK();
     }
 
-    constexpr int TPR = 4;
+    // threads per row: as many as keep every CTA resident at once (<= 2 per SM)
+    const int sms = device_sm_count();
+    int tpr = 4;
+    for (int t : {32, 16, 8}) {
+        if (ceil_div(rows * t, 128) <= 2 * sms) {
+            tpr = t;
+            break;
+        }
+    }
     const size_t smem = sizeof(float) * QB * QB;
-    GPTQ_CUDA_TRY(cudaFuncSetAttribute(gptq_block_kernel<TPR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    GPTQ_CUDA_TRY(cudaFuncSetAttribute(gptq_block_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    GPTQ_CUDA_TRY(cudaFuncSetAttribute(gptq_block_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    GPTQ_CUDA_TRY(cudaFuncSetAttribute(gptq_block_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    GPTQ_CUDA_TRY(cudaFuncSetAttribute(gptq_block_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     BlockArgs a{};
     a.Wk = w.W;
     a.rows = rows;
@@ -422,7 +487,7 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
     a.zeros = zeros;
     a.G = G;
     a.loss = w.loss;
-    const unsigned bgrid = (unsigned)ceil_div(rows, 128 / TPR);
+    const unsigned bgrid = (unsigned)ceil_div(rows, 128 / tpr);
     for (int64_t j0 = 0; j0 < cols; j0 += QB) {
         const int bw = (int)std::min<int64_t>(QB, cols - j0);
         if (q.group > QB && j0 % q.group == 0) {
@@ -434,7 +499,12 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         }
         a.j0 = j0;
         a.bw = bw;
-        GPTQ_LAUNCH(K_BLOCK, s, gptq_block_kernel<TPR><<<bgrid, 128, smem, s>>>(a));
+        switch (tpr) {
+            case 32: GPTQ_LAUNCH(K_BLOCK, s, gptq_block_kernel<32><<<bgrid, 128, smem, s>>>(a)); break;
+            case 16: GPTQ_LAUNCH(K_BLOCK, s, gptq_block_kernel<16><<<bgrid, 128, smem, s>>>(a)); break;
+            case 8: GPTQ_LAUNCH(K_BLOCK, s, gptq_block_kernel<8><<<bgrid, 128, smem, s>>>(a)); break;
+            default: GPTQ_LAUNCH(K_BLOCK, s, gptq_block_kernel<4><<<bgrid, 128, smem, s>>>(a)); break;
+        }
         GPTQ_LAUNCH_CHECK();
         const int64_t e = j0 + bw;
         if (e < cols) {

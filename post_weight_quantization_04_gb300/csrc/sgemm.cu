@@ -19,12 +19,17 @@ namespace gptq {
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 8, PAD = 4, NT = 256;
+constexpr int BK = 8, PAD = 4, NT = 256;
 
-template <bool TRANS_B>
+// BM x BN tile per 256-thread CTA (16 x 16 threads); each thread owns TM x TN outputs
+// as two row halves and two column halves (TM/2 and TN/2 contiguous), so the shared-
+// memory reads of a warp are broadcasts or conflict free.
+template <int BM, int BN, bool TRANS_B>
 __global__ void __launch_bounds__(NT) sgemm_kernel(int M, int N, int K, float alpha, const float* A, int64_t lda,
                                                   const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
                                                   int lower_only) {
+    constexpr int TM = BM / 16, TN = BN / 16, HM = TM / 2, HN = TN / 2;
+    constexpr int LA = BM * BK / NT, LB = BN * BK / NT;  // elements per thread per tile load
     const int m0 = blockIdx.y * BM;
     const int n0 = blockIdx.x * BN;
     if (lower_only && n0 > m0 + BM - 1) return;  // tile entirely above the diagonal
@@ -34,33 +39,29 @@ __global__ void __launch_bounds__(NT) sgemm_kernel(int M, int N, int K, float al
 
     const int tid = threadIdx.x;
     const int tx = tid & 15, ty = tid >> 4;
+    const int ar = tid / (BK / LA), ak = (tid % (BK / LA)) * LA;
+    const int bk = tid / (BN / LB), bn = (tid % (BN / LB)) * LB;
+    const int bn_t = tid / (BK / LB), bk_t = (tid % (BK / LB)) * LB;
 
-    // global -> register staging
-    // A tile (BM x BK): thread loads row ar, k columns ak..ak+3
-    const int ar = tid >> 1, ak = (tid & 1) * 4;
-    // B tile: !TRANS_B: (BK x BN) row bk, cols bn..bn+3 ; TRANS_B: row (n) bn_t, k bk_t..bk_t+3
-    const int bk = tid >> 5, bn = (tid & 31) * 4;
-    const int bn_t = tid >> 1, bk_t = (tid & 1) * 4;
-
-    float ra[4], rb[4];
+    float ra[LA], rb[LB];
     auto load_tile = [&](int k0) {
         const int gm = m0 + ar;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < LA; ++i) {
             const int gk = k0 + ak + i;
             ra[i] = (gm < M && gk < K) ? A[(int64_t)gm * lda + gk] : 0.0f;
         }
         if (!TRANS_B) {
             const int gk = k0 + bk;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < LB; ++i) {
                 const int gn = n0 + bn + i;
                 rb[i] = (gk < K && gn < N) ? B[(int64_t)gk * ldb + gn] : 0.0f;
             }
         } else {
             const int gn = n0 + bn_t;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < LB; ++i) {
                 const int gk = k0 + bk_t + i;
                 rb[i] = (gk < K && gn < N) ? B[(int64_t)gn * ldb + gk] : 0.0f;
             }
@@ -68,20 +69,21 @@ __global__ void __launch_bounds__(NT) sgemm_kernel(int M, int N, int K, float al
     };
     auto store_tile = [&](int buf) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) As[buf][ak + i][ar] = ra[i];
+        for (int i = 0; i < LA; ++i) As[buf][ak + i][ar] = ra[i];
         if (!TRANS_B) {
-            *reinterpret_cast<float4*>(&Bs[buf][bk][bn]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
+#pragma unroll
+            for (int i = 0; i < LB; ++i) Bs[buf][bk][bn + i] = rb[i];
         } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) Bs[buf][bk_t + i][bn_t] = rb[i];
+            for (int i = 0; i < LB; ++i) Bs[buf][bk_t + i][bn_t] = rb[i];
         }
     };
 
-    float acc[8][8];
+    float acc[TM][TN];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
 
     const int ktiles = (K + BK - 1) / BK;
     load_tile(0);
@@ -92,31 +94,33 @@ __global__ void __launch_bounds__(NT) sgemm_kernel(int M, int N, int K, float al
         if (kt + 1 < ktiles) load_tile((kt + 1) * BK);
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
-            float a[8], b[8];
-            const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][ty * 4]);
-            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][64 + ty * 4]);
-            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][tx * 4]);
-            const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][64 + tx * 4]);
-            a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
-            a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
-            b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
-            b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+            float a[TM], b[TN];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < HM; ++i) {
+                a[i] = As[buf][k][ty * HM + i];
+                a[HM + i] = As[buf][k][BM / 2 + ty * HM + i];
+            }
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            for (int j = 0; j < HN; ++j) {
+                b[j] = Bs[buf][k][tx * HN + j];
+                b[HN + j] = Bs[buf][k][BN / 2 + tx * HN + j];
+            }
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
         if (kt + 1 < ktiles) store_tile(buf ^ 1);
         __syncthreads();
     }
 
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int gm = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+    for (int i = 0; i < TM; ++i) {
+        const int gm = m0 + (i < HM ? ty * HM + i : BM / 2 + ty * HM + (i - HM));
         if (gm >= M) continue;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int gn = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
+        for (int j = 0; j < TN; ++j) {
+            const int gn = n0 + (j < HN ? tx * HN + j : BN / 2 + tx * HN + (j - HN));
             if (gn >= N) continue;
             float* c = C + (int64_t)gm * ldc + gn;
             const float v = alpha * acc[i][j];
@@ -125,18 +129,33 @@ __global__ void __launch_bounds__(NT) sgemm_kernel(int M, int N, int K, float al
     }
 }
 
+template <int T>
+void launch(int id, bool trans_b, int M, int N, int K, float alpha, const float* A, int64_t lda, const float* B,
+            int64_t ldb, float beta, float* C, int64_t ldc, bool lower_only, cudaStream_t stream) {
+    dim3 grid((unsigned)((N + T - 1) / T), (unsigned)((M + T - 1) / T));
+    if (trans_b)
+        GPTQ_LAUNCH(id, stream, sgemm_kernel<T, T, true><<<grid, NT, 0, stream>>>(M, N, K, alpha, A, lda, B, ldb,
+                                                                                  beta, C, ldc, lower_only ? 1 : 0));
+    else
+        GPTQ_LAUNCH(id, stream, sgemm_kernel<T, T, false><<<grid, NT, 0, stream>>>(M, N, K, alpha, A, lda, B, ldb,
+                                                                                   beta, C, ldc, lower_only ? 1 : 0));
+}
+
 }  // namespace
 
 cudaError_t sgemm(int id, bool trans_b, int M, int N, int K, float alpha, const float* A, int64_t lda, const float* B,
                   int64_t ldb, float beta, float* C, int64_t ldc, bool lower_only, cudaStream_t stream) {
     if (M <= 0 || N <= 0) return cudaSuccess;
-    dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
-    if (trans_b)
-        GPTQ_LAUNCH(id, stream, sgemm_kernel<true><<<grid, NT, 0, stream>>>(M, N, K, alpha, A, lda, B, ldb, beta, C,
-                                                                            ldc, lower_only ? 1 : 0));
+    // 64 x 64 tiles when 128 x 128 tiles would leave SMs idle; never for in-place calls,
+    // whose safety needs one CTA to own whole rows (C == A) or whole columns (C == B)
+    const bool aliased = (C == A) || (C == B);
+    int64_t tiles = (int64_t)((M + 127) / 128) * ((N + 127) / 128);
+    if (lower_only) tiles = (tiles + (M + 127) / 128) / 2;
+    static const int sms = device_sm_count();
+    if (!aliased && tiles < sms)
+        launch<64>(id, trans_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, lower_only, stream);
     else
-        GPTQ_LAUNCH(id, stream, sgemm_kernel<false><<<grid, NT, 0, stream>>>(M, N, K, alpha, A, lda, B, ldb, beta, C,
-                                                                             ldc, lower_only ? 1 : 0));
+        launch<128>(id, trans_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, lower_only, stream);
     return cudaGetLastError();
 }
 
