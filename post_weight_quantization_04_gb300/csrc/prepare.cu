@@ -148,25 +148,31 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
 // One CTA factors the diagonal block A[k0:k0+n, k0:k0+n] = L L^T in place (lower), and
 // writes L^-1 (lower, NB x NB, zeros above) to Linv. A non-positive or non-finite pivot
 // records GPTQ_ERR_NOT_SPD (and is replaced by 1 so the kernel finishes).
+//
+// One loop over k does both: column k of L (right-looking Cholesky) and the matching
+// Gauss-Jordan step on [L | I] (row k of X divided by L[k][k], then X[i][:] -= L[i][k] *
+// X[k][:] for i > k), which turns I into L^-1. Column k of L and the scaled row k of X
+// are staged in their own shared arrays so the update loop's loads never alias its stores.
 // 512 threads: thread t owns row i = t / 4 and the columns j = q (mod 4), q = t % 4.
 __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, int64_t lda, int64_t k0, int n,
                                                         float* __restrict__ Linv, int* __restrict__ status) {
     extern __shared__ float sm[];
     constexpr int LD = NB + 1;
-    float* S = sm;              // NB x LD: the block, then L
-    float* X = sm + NB * LD;    // NB x LD: L^-1
-    __shared__ float part[4][NB];
+    float* S = sm;              // NB x LD: the block, then L (diagonal kept in dg)
+    float* X = sm + NB * LD;    // NB x LD: I, then L^-1
+    __shared__ float colk[NB];  // L[:, k]
+    __shared__ float xk[NB];    // X[k, :] / L[k][k]
+    __shared__ float dg[NB];    // diag(L)
     const int tid = threadIdx.x;
     const int i = tid >> 2, q = tid & 3;
 
 #pragma unroll
     for (int j = q; j < NB; j += 4) {
         S[i * LD + j] = (i < n && j <= i) ? A[(k0 + i) * lda + k0 + j] : 0.0f;
-        X[i * LD + j] = 0.0f;
+        X[i * LD + j] = (i == j && i < n) ? 1.0f : 0.0f;
     }
     __syncthreads();
 
-    // right-looking column Cholesky
     for (int k = 0; k < n; ++k) {
         float piv = S[k * LD + k];
         if (!(piv > 0.0f) || !isfinite(piv)) {
@@ -174,41 +180,36 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, 
             piv = 1.0f;
         }
         const float lkk = sqrtf(piv);
-        __syncthreads();                                   // everyone has read the pivot
-        if (q == 0 && i > k && i < n) S[i * LD + k] = S[i * LD + k] / lkk;
-        if (tid == 0) S[k * LD + k] = lkk;
+        const float inv = 1.0f / lkk;
+        if (q == 0 && i > k && i < n) {
+            const float v = S[i * LD + k] * inv;
+            colk[i] = v;
+            S[i * LD + k] = v;
+        }
+        if (i == k) {
+            for (int c = q; c <= k; c += 4) {
+                const float v = X[k * LD + c] * inv;
+                xk[c] = v;
+                X[k * LD + c] = v;
+            }
+            if (q == 0) dg[k] = lkk;
+        }
         __syncthreads();
         if (i > k && i < n) {
-            const float lik = S[i * LD + k];
+            const float lik = colk[i];
+#pragma unroll 4
             for (int j = k + 1 + ((q - k - 1) & 3); j <= i; j += 4)
-                S[i * LD + j] = fmaf(-lik, S[j * LD + k], S[i * LD + j]);
+                S[i * LD + j] = fmaf(-lik, colk[j], S[i * LD + j]);
+#pragma unroll 4
+            for (int c = q; c <= k; c += 4) X[i * LD + c] = fmaf(-lik, xk[c], X[i * LD + c]);
         }
         __syncthreads();
     }
 #pragma unroll
-    for (int j = q; j < NB; j += 4)
-        if (i < n && j <= i) A[(k0 + i) * lda + k0 + j] = S[i * LD + j];
-
-    // L^-1 by rows: X[r][c] = (delta_rc - sum_{c<=m<r} L[r][m] X[m][c]) / L[r][r];
-    // column c's dot product is split over four threads (cq = 0..3)
-    const int c = tid & (NB - 1), cq = tid >> 7;
-    for (int r = 0; r < n; ++r) {
-        float s = 0.0f;
-        if (c < r) {
-            const int per = (r - c + 3) >> 2;
-            const int mb = c + cq * per, me = min(r, mb + per);
-            for (int m = mb; m < me; ++m) s = fmaf(S[r * LD + m], X[m * LD + c], s);
-        }
-        part[cq][c] = s;
-        __syncthreads();
-        if (cq == 0 && c <= r) {
-            const float tot = (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
-            X[r * LD + c] = ((c == r ? 1.0f : 0.0f) - tot) / S[r * LD + r];
-        }
-        __syncthreads();
+    for (int j = q; j < NB; j += 4) {
+        if (i < n && j <= i) A[(k0 + i) * lda + k0 + j] = (j == i) ? dg[i] : S[i * LD + j];
+        Linv[i * NB + j] = (i < n && j <= i) ? X[i * LD + j] : 0.0f;
     }
-#pragma unroll
-    for (int j = q; j < NB; j += 4) Linv[i * NB + j] = (i < n && j <= i) ? X[i * LD + j] : 0.0f;
 }
 
 __global__ void eye_kernel(float* __restrict__ B, int64_t d) {
@@ -262,13 +263,9 @@ extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, fl
         GPTQ_LAUNCH_CHECK();
     }
 
-    static bool attr_set = false;
     const size_t potrf_smem = sizeof(float) * 2 * NB * (NB + 1);
-    if (!attr_set) {
-        GPTQ_CUDA_TRY(cudaFuncSetAttribute(potrf_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)potrf_smem));
-        attr_set = true;
-    }
+    GPTQ_CUDA_TRY(cudaFuncSetAttribute(potrf_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)potrf_smem));
 
     // blocked right-looking Cholesky of A (lower)
     const int64_t nblk = ceil_div(d, NB);

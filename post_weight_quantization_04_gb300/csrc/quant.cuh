@@ -57,6 +57,20 @@ __device__ __forceinline__ int grid_code(float w, const Grid& g, bool sym, int l
     return (int)r;
 }
 
+// The same decision as grid_code, returned as an integer-valued float (no float<->int
+// conversions on the caller's dependency chain). |t - rint(t)| > 0.499 is the same
+// 1e-3-wide band around the half-points as grid_code's test.
+__device__ __forceinline__ float grid_code_f(float w, const Grid& g, bool sym, float lo, float hi) {
+    const float t = sym ? w * g.inv_s : fmaf(w, g.inv_s, g.z);
+    float r = rintf(t);
+    if (fabsf(t - r) > 0.499f) r = quotient_rint_f64(w, g.s, g.z, sym ? 1 : 0);
+    return fminf(fmaxf(r, lo), hi);
+}
+
+__device__ __forceinline__ float grid_dequant_f(float code, const Grid& g, bool sym) {
+    return sym ? code * g.s : g.s * (code - g.z);
+}
+
 __device__ __forceinline__ float grid_dequant(int code, const Grid& g, bool sym) {
     return sym ? (float)code * g.s : g.s * ((float)code - g.z);
 }

@@ -130,7 +130,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // One 128-column block of the loop. TPR threads share a row; thread `sub` owns the
 // 4-column chunks sub, sub+TPR, sub+2*TPR, ... of the block (CPT columns in registers),
 // so the TPR lanes of a row read one contiguous 16*TPR-byte span of U's row per step.
-template <int TPR>
+template <int TPR, bool SMALL_GROUPS>
 __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
     constexpr int CPT = QB / TPR;   // columns per thread
     constexpr int NCH = CPT / 4;    // 4-column chunks per thread
@@ -197,73 +197,104 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
             cr[4 * m + e] = 0;
         }
     }
+    // grid of the group starting at block column jj (ending before gend), from the updated
+    // weights: a TPR-lane reduction of max|w| (symmetric) or min/max (asymmetric)
+    auto group_grid = [&](int jj, int gend) {
+        float am = 0.0f, mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+        for (int mm = 0; mm < NCH; ++mm)
+#pragma unroll
+            for (int ee = 0; ee < 4; ++ee) {
+                const int c = col_of(mm, ee);
+                if (c >= jj && c < gend) {
+                    const float v = w[4 * mm + ee];
+                    am = fmaxf(am, fabsf(v));
+                    mx = fmaxf(mx, v);
+                    mn = fminf(mn, v);
+                }
+            }
+#pragma unroll
+        for (int off = TPR / 2; off > 0; off >>= 1) {
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off, TPR));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off, TPR));
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off, TPR));
+        }
+        const Grid gg = sym ? sym_grid(am, qmax) : asym_grid(mn, mx, qmax);
+        if (active && sub == 0) {
+            const int64_t gi = (a.j0 + jj) / a.group;
+            a.scales[row * a.G + gi] = gg.s;
+            a.zeros[row * a.G + gi] = sym ? (uint8_t)(1 << (a.bits - 1)) : (uint8_t)gg.z;
+        }
+        return gg;
+    };
+
     Grid g{1.0f, 1.0f, 0.0f};
-    if (!inblock_groups && active) {
-        g.s = a.cur_s[row];
-        g.inv_s = 1.0f / g.s;
-        g.z = a.cur_z[row];
+    if (!inblock_groups) {
+        if (active) {
+            g.s = a.cur_s[row];
+            g.inv_s = 1.0f / g.s;
+            g.z = a.cur_z[row];
+        }
+    } else if (!SMALL_GROUPS) {
+        g = group_grid(0, bw);   // one group per block (group == 128)
     }
     float loss = 0.0f;
-    int next_gs = 0;  // next in-block group start
+    int next_gs = 0;  // next in-block group start (groups smaller than the block)
+    const float flo = (float)lo, fhi = (float)hi;
 
+    // one column step: broadcast w_j, quantise, error, update this thread's columns
+    auto step = [&](int m, int o, int e, int jj) {
+        const float wj = __shfl_sync(0xffffffffu, w[4 * m + e], o, TPR);
+        const float cf = grid_code_f(wj, g, sym, flo, fhi);
+        const float q = grid_dequant_f(cf, g, sym);
+        const float err = (wj - q) * invd[jj];
+        if (sub == o) {
+            cr[4 * m + e] = (int8_t)(int)cf;
+            qr[4 * m + e] = q;
+            er[4 * m + e] = err;
+        }
+        loss = fmaf(err, err, loss);
+        const float* ur = us + jj * QB;
 #pragma unroll
-    for (int m = 0; m < NCH; ++m) {
-        for (int o = 0; o < TPR; ++o) {
+        for (int mm = 0; mm < NCH; ++mm) {
+            const float4 u4 = *reinterpret_cast<const float4*>(ur + col_of(mm, 0));
+            w[4 * mm] = fmaf(-err, u4.x, w[4 * mm]);
+            w[4 * mm + 1] = fmaf(-err, u4.y, w[4 * mm + 1]);
+            w[4 * mm + 2] = fmaf(-err, u4.z, w[4 * mm + 2]);
+            w[4 * mm + 3] = fmaf(-err, u4.w, w[4 * mm + 3]);
+        }
+    };
+
+    if (SMALL_GROUPS) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int jj = (m * TPR + o) * 4 + e;
-                if (jj >= bw) break;
-                if (inblock_groups && jj == next_gs) {
-                    next_gs += a.group;
-                    const int gend = min(jj + a.group, bw);
-                    float am = 0.0f, mx = -INFINITY, mn = INFINITY;
+        for (int m = 0; m < NCH; ++m) {
+            for (int o = 0; o < TPR; ++o) {
 #pragma unroll
-                    for (int mm = 0; mm < NCH; ++mm)
-#pragma unroll
-                        for (int ee = 0; ee < 4; ++ee) {
-                            const int c = col_of(mm, ee);
-                            if (c >= jj && c < gend) {
-                                const float v = w[4 * mm + ee];
-                                am = fmaxf(am, fabsf(v));
-                                mx = fmaxf(mx, v);
-                                mn = fminf(mn, v);
-                            }
-                        }
-#pragma unroll
-                    for (int off = TPR / 2; off > 0; off >>= 1) {
-                        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off, TPR));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off, TPR));
-                        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off, TPR));
+                for (int e = 0; e < 4; ++e) {
+                    const int jj = (m * TPR + o) * 4 + e;
+                    if (jj >= bw) break;
+                    if (jj == next_gs) {
+                        next_gs += a.group;
+                        g = group_grid(jj, min(jj + a.group, bw));
                     }
-                    g = sym ? sym_grid(am, qmax) : asym_grid(mn, mx, qmax);
-                    if (active && sub == 0) {
-                        const int64_t gi = (a.j0 + jj) / a.group;
-                        a.scales[row * a.G + gi] = g.s;
-                        a.zeros[row * a.G + gi] = sym ? (uint8_t)(1 << (a.bits - 1)) : (uint8_t)g.z;
-                    }
+                    step(m, o, e, jj);
                 }
-                const float wj = __shfl_sync(0xffffffffu, w[4 * m + e], o, TPR);
-                const int c = grid_code(wj, g, sym, lo, hi);
-                const float q = grid_dequant(c, g, sym);
-                const float err = (wj - q) * invd[jj];
-                if (sub == o) {
-                    cr[4 * m + e] = (int8_t)c;
-                    qr[4 * m + e] = q;
-                    er[4 * m + e] = err;
-                }
-                loss = fmaf(err, err, loss);
-                const float* ur = us + jj * QB;
+            }
+        }
+    } else {
 #pragma unroll
-                for (int mm = 0; mm < NCH; ++mm) {
-                    const float4 u4 = *reinterpret_cast<const float4*>(ur + col_of(mm, 0));
-                    w[4 * mm] = fmaf(-err, u4.x, w[4 * mm]);
-                    w[4 * mm + 1] = fmaf(-err, u4.y, w[4 * mm + 1]);
-                    w[4 * mm + 2] = fmaf(-err, u4.z, w[4 * mm + 2]);
-                    w[4 * mm + 3] = fmaf(-err, u4.w, w[4 * mm + 3]);
+        for (int m = 0; m < NCH; ++m) {
+#pragma unroll
+            for (int o = 0; o < TPR; ++o) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int jj = (m * TPR + o) * 4 + e;
+                    if (jj < bw) step(m, o, e, jj);
                 }
             }
         }
     }
+    (void)next_gs;
 
     if (!active) return;
     float* erow = a.Err + row * QB;
@@ -465,10 +496,17 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         }
     }
     const size_t smem = sizeof(float) * QB * QB;
-    GPTQ_CUDA_TRY(cudaFuncSetAttribute(gptq_block_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    GPTQ_CUDA_TRY(cudaFuncSetAttribute(gptq_block_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    GPTQ_CUDA_TRY(cudaFuncSetAttribute(gptq_block_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    GPTQ_CUDA_TRY(cudaFuncSetAttribute(gptq_block_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    const bool small_groups = q.group > 0 && q.group < QB;
+    auto block_fn = [&](int t) -> void (*)(BlockArgs) {
+        switch (t) {
+            case 32: return small_groups ? gptq_block_kernel<32, true> : gptq_block_kernel<32, false>;
+            case 16: return small_groups ? gptq_block_kernel<16, true> : gptq_block_kernel<16, false>;
+            case 8: return small_groups ? gptq_block_kernel<8, true> : gptq_block_kernel<8, false>;
+            default: return small_groups ? gptq_block_kernel<4, true> : gptq_block_kernel<4, false>;
+        }
+    };
+    void (*kblock)(BlockArgs) = block_fn(tpr);
+    GPTQ_CUDA_TRY(cudaFuncSetAttribute(kblock, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     BlockArgs a{};
     a.Wk = w.W;
     a.rows = rows;
@@ -499,12 +537,7 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         }
         a.j0 = j0;
         a.bw = bw;
-        switch (tpr) {
-            case 32: GPTQ_LAUNCH(K_BLOCK, s, gptq_block_kernel<32><<<bgrid, 128, smem, s>>>(a)); break;
-            case 16: GPTQ_LAUNCH(K_BLOCK, s, gptq_block_kernel<16><<<bgrid, 128, smem, s>>>(a)); break;
-            case 8: GPTQ_LAUNCH(K_BLOCK, s, gptq_block_kernel<8><<<bgrid, 128, smem, s>>>(a)); break;
-            default: GPTQ_LAUNCH(K_BLOCK, s, gptq_block_kernel<4><<<bgrid, 128, smem, s>>>(a)); break;
-        }
+        GPTQ_LAUNCH(K_BLOCK, s, kblock<<<bgrid, 128, smem, s>>>(a));
         GPTQ_LAUNCH_CHECK();
         const int64_t e = j0 + bw;
         if (e < cols) {
