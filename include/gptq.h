@@ -113,7 +113,7 @@ int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, float damp, i
  * memory (a host framework that owns all device memory through its own pool, or a path
  * that cannot take cudaMalloc's implicit synchronisation). No counterpart on the pages.
  * Same arguments, outputs, synchronisation and errors as gptq_prepare, minus ws/ws_bytes.
- * The scratch is a fixed array compiled into the library (about 8.5 MiB, held on every
+ * The scratch is a fixed array compiled into the library (about 10.5 MiB, held on every
  * GPU that loads the library until the process exits), so d is limited to 1024:
  * d > 1024 returns GPTQ_ERR_UNSUPPORTED. Allocates nothing (no cudaMalloc/cudaFree).
  * The first call on a device looks up that device's copy of the array
@@ -142,7 +142,8 @@ int gptq_prepare_noalloc(const float* H, const float* diag_xtx, int64_t d, float
  *           LSB-first bitstream of unsigned codes u (sym u = code + 2^(bits-1))
  *   row_loss rows fp32 (may be NULL): sum_k err_k^2 per row
  * ws: device workspace of at least gptq_quantize_workspace_bytes(rows, cols, q) bytes.
- * Asynchronous. Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+ * Synchronises `stream` at the end to report a device-side timeout.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, TIMEOUT, CUDA. */
 size_t gptq_quantize_workspace_bytes(int64_t rows, int64_t cols, gptq_qconfig q);
 int gptq_quantize(const float* W, int64_t rows, int64_t cols, const float* U,
                   const int32_t* perm, const uint8_t* dead, gptq_qconfig q,

@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "sgemm.cuh"
+#include "tc_gemm.cuh"
 
 namespace gptq {
 
@@ -32,36 +33,53 @@ namespace {
 
 constexpr int NB = 128;  // panel width of the blocked factorisation
 
-inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
 struct PrepWs {
     float* A;
     float* Binv;
     float* LinvD;
+    float* ahi;   // d x NB: TF32 split of the GEMM's first operand
+    float* alo;
+    float* bhi;   // d x NB: TF32 split of the second operand
+    float* blo;
     float* ddiag;
     float* rr;
     int* status;
     size_t bytes;
 };
 
+constexpr size_t align256c(size_t x) { return (x + 255) & ~size_t(255); }
+
+// slab sizes, in carve order; the total is also the size of the allocation-free scratch
+constexpr size_t prep_slab(int64_t d, int i) {
+    return i < 2 ? sizeof(float) * d * d
+         : i == 2 ? sizeof(float) * ((d + NB - 1) / NB) * NB * NB
+         : i < 7 ? sizeof(float) * d * NB
+         : i < 9 ? sizeof(float) * d
+         : sizeof(int) * 4;
+}
+constexpr int kPrepSlabs = 10;
+constexpr size_t prep_ws_bytes(int64_t d) {
+    size_t off = 0;
+    for (int i = 0; i < kPrepSlabs; ++i) off = align256c(off + prep_slab(d, i));
+    return off;
+}
+
 PrepWs carve(void* base, int64_t d) {
     PrepWs w{};
-    size_t off = 0;
     char* p = static_cast<char*>(base);
-    const int64_t nblk = (d + NB - 1) / NB;
-    w.A = reinterpret_cast<float*>(p + off);
-    off = align256(off + sizeof(float) * d * d);
-    w.Binv = reinterpret_cast<float*>(p + off);
-    off = align256(off + sizeof(float) * d * d);
-    w.LinvD = reinterpret_cast<float*>(p + off);
-    off = align256(off + sizeof(float) * nblk * NB * NB);
-    w.ddiag = reinterpret_cast<float*>(p + off);
-    off = align256(off + sizeof(float) * d);
-    w.rr = reinterpret_cast<float*>(p + off);
-    off = align256(off + sizeof(float) * d);
-    w.status = reinterpret_cast<int*>(p + off);
-    off = align256(off + sizeof(int) * 4);
-    w.bytes = off;
+    size_t off[kPrepSlabs + 1] = {0};
+    for (int i = 0; i < kPrepSlabs; ++i) off[i + 1] = align256c(off[i] + prep_slab(d, i));
+    w.A = reinterpret_cast<float*>(p + off[0]);
+    w.Binv = reinterpret_cast<float*>(p + off[1]);
+    w.LinvD = reinterpret_cast<float*>(p + off[2]);
+    w.ahi = reinterpret_cast<float*>(p + off[3]);
+    w.alo = reinterpret_cast<float*>(p + off[4]);
+    w.bhi = reinterpret_cast<float*>(p + off[5]);
+    w.blo = reinterpret_cast<float*>(p + off[6]);
+    w.ddiag = reinterpret_cast<float*>(p + off[7]);
+    w.rr = reinterpret_cast<float*>(p + off[8]);
+    w.status = reinterpret_cast<int*>(p + off[9]);
+    w.bytes = off[kPrepSlabs];
     return w;
 }
 
@@ -149,66 +167,87 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
 // writes L^-1 (lower, NB x NB, zeros above) to Linv. A non-positive or non-finite pivot
 // records GPTQ_ERR_NOT_SPD (and is replaced by 1 so the kernel finishes).
 //
-// One loop over k does both: column k of L (right-looking Cholesky) and the matching
-// Gauss-Jordan step on [L | I] (row k of X divided by L[k][k], then X[i][:] -= L[i][k] *
-// X[k][:] for i > k), which turns I into L^-1. Column k of L and the scaled row k of X
-// are staged in their own shared arrays so the update loop's loads never alias its stores.
-// 512 threads: thread t owns row i = t / 4 and the columns j = q (mod 4), q = t % 4.
+// One loop over k produces column k of L (right-looking Cholesky) and applies the matching
+// Gauss-Jordan step to X = [I -> L^-1]: X[i][:] -= L[i][k] * X[k][:] / L[k][k] for i > k and
+// X[k][:] /= L[k][k]. Everything a thread updates lives in its registers: thread (j, q)
+// holds rows 32q..32q+31 of column j of the block, and columns 32q..32q+31 of row j of X.
+// At step k the four threads of column k publish the (raw) pivot column, and of row k of X,
+// to double-buffered shared arrays; after one barrier every thread updates its registers
+// with broadcast reads. Entries above the diagonal of the block are updated too (unused),
+// so the update needs no per-element predicate; columns of X beyond k read zeros.
 __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, int64_t lda, int64_t k0, int n,
                                                         float* __restrict__ Linv, int* __restrict__ status) {
-    extern __shared__ float sm[];
-    constexpr int LD = NB + 1;
-    float* S = sm;              // NB x LD: the block, then L (diagonal kept in dg)
-    float* X = sm + NB * LD;    // NB x LD: I, then L^-1
-    __shared__ float colk[NB];  // L[:, k]
-    __shared__ float xk[NB];    // X[k, :] / L[k][k]
-    __shared__ float dg[NB];    // diag(L)
+    __shared__ __align__(16) float colraw[2][NB];
+    __shared__ __align__(16) float xraw[2][NB];
+    __shared__ float dg[NB];
     const int tid = threadIdx.x;
-    const int i = tid >> 2, q = tid & 3;
+    const int q = tid >> 7;                                 // row / column slab 32q..32q+31
+    const int j = ((tid & 31) << 2) | ((tid >> 5) & 3);     // column of L, row of X (spread over SMSPs)
+    const int r0 = 32 * q;
 
+    float sc[32], xr[32];
 #pragma unroll
-    for (int j = q; j < NB; j += 4) {
-        S[i * LD + j] = (i < n && j <= i) ? A[(k0 + i) * lda + k0 + j] : 0.0f;
-        X[i * LD + j] = (i == j && i < n) ? 1.0f : 0.0f;
+    for (int t = 0; t < 32; ++t) {
+        const int i = r0 + t;
+        sc[t] = (i < n && j < n && i >= j) ? A[(k0 + i) * lda + k0 + j] : 0.0f;
+        xr[t] = (i == j && j < n) ? 1.0f : 0.0f;
     }
-    __syncthreads();
 
     for (int k = 0; k < n; ++k) {
-        float piv = S[k * LD + k];
+        const int b = k & 1;
+        if (j == k) {
+#pragma unroll
+            for (int t = 0; t < 32; t += 4) {
+                *reinterpret_cast<float4*>(&colraw[b][r0 + t]) = make_float4(sc[t], sc[t + 1], sc[t + 2], sc[t + 3]);
+                *reinterpret_cast<float4*>(&xraw[b][r0 + t]) = make_float4(xr[t], xr[t + 1], xr[t + 2], xr[t + 3]);
+            }
+        }
+        __syncthreads();
+        float piv = colraw[b][k];
         if (!(piv > 0.0f) || !isfinite(piv)) {
             if (tid == 0) set_status(status, GPTQ_ERR_NOT_SPD);
             piv = 1.0f;
         }
         const float lkk = sqrtf(piv);
         const float inv = 1.0f / lkk;
-        if (q == 0 && i > k && i < n) {
-            const float v = S[i * LD + k] * inv;
-            colk[i] = v;
-            S[i * LD + k] = v;
-        }
-        if (i == k) {
-            for (int c = q; c <= k; c += 4) {
-                const float v = X[k * LD + c] * inv;
-                xk[c] = v;
-                X[k * LD + c] = v;
+        if (j > k && j < n) {
+            const float f = colraw[b][j] * (inv * inv);     // L[j][k] / L[k][k]
+#pragma unroll
+            for (int t = 0; t < 32; t += 4) {
+                const float4 c4 = *reinterpret_cast<const float4*>(&colraw[b][r0 + t]);
+                const float4 x4 = *reinterpret_cast<const float4*>(&xraw[b][r0 + t]);
+                sc[t] = fmaf(-c4.x, f, sc[t]);
+                sc[t + 1] = fmaf(-c4.y, f, sc[t + 1]);
+                sc[t + 2] = fmaf(-c4.z, f, sc[t + 2]);
+                sc[t + 3] = fmaf(-c4.w, f, sc[t + 3]);
+                xr[t] = fmaf(-f, x4.x, xr[t]);
+                xr[t + 1] = fmaf(-f, x4.y, xr[t + 1]);
+                xr[t + 2] = fmaf(-f, x4.z, xr[t + 2]);
+                xr[t + 3] = fmaf(-f, x4.w, xr[t + 3]);
+            }
+        } else if (j == k) {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                sc[t] *= inv;
+                xr[t] *= inv;
             }
             if (q == 0) dg[k] = lkk;
         }
-        __syncthreads();
-        if (i > k && i < n) {
-            const float lik = colk[i];
-#pragma unroll 4
-            for (int j = k + 1 + ((q - k - 1) & 3); j <= i; j += 4)
-                S[i * LD + j] = fmaf(-lik, colk[j], S[i * LD + j]);
-#pragma unroll 4
-            for (int c = q; c <= k; c += 4) X[i * LD + c] = fmaf(-lik, xk[c], X[i * LD + c]);
-        }
-        __syncthreads();
+    }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+        const int i = r0 + t;
+        if (i < n && j < n && i >= j) A[(k0 + i) * lda + k0 + j] = (i == j) ? dg[j] : sc[t];
     }
 #pragma unroll
-    for (int j = q; j < NB; j += 4) {
-        if (i < n && j <= i) A[(k0 + i) * lda + k0 + j] = (j == i) ? dg[i] : S[i * LD + j];
-        Linv[i * NB + j] = (i < n && j <= i) ? X[i * LD + j] : 0.0f;
+    for (int t = 0; t < 32; t += 4) {
+        float4 v;
+        v.x = (j < n && r0 + t <= j) ? xr[t] : 0.0f;
+        v.y = (j < n && r0 + t + 1 <= j) ? xr[t + 1] : 0.0f;
+        v.z = (j < n && r0 + t + 2 <= j) ? xr[t + 2] : 0.0f;
+        v.w = (j < n && r0 + t + 3 <= j) ? xr[t + 3] : 0.0f;
+        *reinterpret_cast<float4*>(&Linv[j * NB + r0 + t]) = v;
     }
 }
 
@@ -263,9 +302,11 @@ extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, fl
         GPTQ_LAUNCH_CHECK();
     }
 
-    const size_t potrf_smem = sizeof(float) * 2 * NB * (NB + 1);
-    GPTQ_CUDA_TRY(cudaFuncSetAttribute(potrf_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)potrf_smem));
+    const size_t potrf_smem = 0;
+
+    // The trailing contractions run on the tensor cores (3xTF32, operands split into
+    // TF32 hi/lo first) when every matrix row is 16-byte aligned, else on the FFMA GEMM.
+    const bool tc = (d % 4 == 0) && tc_gemm_nt_ok(w.A, d);
 
     // blocked right-looking Cholesky of A (lower)
     const int64_t nblk = ceil_div(d, NB);
@@ -276,13 +317,22 @@ extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, fl
         GPTQ_LAUNCH(K_POTRF, s, potrf_diag_kernel<<<1, 512, potrf_smem, s>>>(w.A, d, k0, n, LinvK, w.status));
         GPTQ_LAUNCH_CHECK();
         const int64_t m = d - k0 - n;
-        if (m > 0) {
-            float* P = w.A + (k0 + n) * d + k0;
-            // panel: P <- P * Linv_kk^T   (in place; N = n <= 128)
-            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, true, (int)m, n, n, 1.0f, P, d, LinvK, NB, 0.0f, P, d, false, s));
+        if (m <= 0) continue;
+        float* P = w.A + (k0 + n) * d + k0;
+        float* A22 = w.A + (k0 + n) * d + k0 + n;
+        if (tc) {
+            // panel: P <- P * Linv_kk^T
+            GPTQ_CUDA_TRY(split_rows(K_SPLIT, P, d, (int)m, n, w.ahi, w.alo, NB, s));
+            GPTQ_CUDA_TRY(split_rows(K_SPLIT, LinvK, NB, n, n, w.bhi, w.blo, NB, s));
+            GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, n, n, 1.0f, w.ahi, w.alo, w.bhi, w.blo, NB, 0.0f, P, d, false,
+                                     w.status, s));
             // trailing: A22 -= P P^T (lower tiles)
-            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, true, (int)m, (int)m, n, -1.0f, P, d, P, d, 1.0f, w.A + (k0 + n) * d + k0 + n, d,
-                                true, s));
+            GPTQ_CUDA_TRY(split_rows(K_SPLIT, P, d, (int)m, n, w.ahi, w.alo, NB, s));
+            GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, (int)m, n, -1.0f, w.ahi, w.alo, w.ahi, w.alo, NB, 1.0f, A22, d,
+                                     true, w.status, s));
+        } else {
+            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, true, (int)m, n, n, 1.0f, P, d, LinvK, NB, 0.0f, P, d, false, s));
+            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, true, (int)m, (int)m, n, -1.0f, P, d, P, d, 1.0f, A22, d, true, s));
         }
     }
 
@@ -294,11 +344,26 @@ extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, fl
         const int n = (int)std::min<int64_t>(NB, d - i0);
         const int64_t ncols = i0 + n;
         float* Xi = w.Binv + i0 * d;
-        GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, false, n, (int)ncols, n, 1.0f, w.LinvD + ib * NB * NB, NB, Xi, d, 0.0f, Xi, d, false, s));
+        float* LinvI = w.LinvD + ib * NB * NB;
         const int64_t m = d - i0 - n;
-        if (m > 0) {
-            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, false, (int)m, (int)ncols, n, -1.0f, w.A + (i0 + n) * d + i0, d, Xi, d, 1.0f,
-                                w.Binv + (i0 + n) * d, d, false, s));
+        if (tc) {
+            // X[i,:] = Linv_ii * X[i,:]: second operand is X[i, 0:ncols]^T (ncols x n)
+            GPTQ_CUDA_TRY(split_rows(K_SPLIT, LinvI, NB, n, n, w.ahi, w.alo, NB, s));
+            GPTQ_CUDA_TRY(split_cols(K_SPLIT, Xi, d, n, (int)ncols, w.bhi, w.blo, NB, s));
+            GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, n, (int)ncols, n, 1.0f, w.ahi, w.alo, w.bhi, w.blo, NB, 0.0f, Xi, d,
+                                     false, w.status, s));
+            if (m > 0) {
+                GPTQ_CUDA_TRY(split_rows(K_SPLIT, w.A + (i0 + n) * d + i0, d, (int)m, n, w.ahi, w.alo, NB, s));
+                GPTQ_CUDA_TRY(split_cols(K_SPLIT, Xi, d, n, (int)ncols, w.bhi, w.blo, NB, s));
+                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, (int)ncols, n, -1.0f, w.ahi, w.alo, w.bhi, w.blo, NB, 1.0f,
+                                         w.Binv + (i0 + n) * d, d, false, w.status, s));
+            }
+        } else {
+            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, false, n, (int)ncols, n, 1.0f, LinvI, NB, Xi, d, 0.0f, Xi, d, false, s));
+            if (m > 0) {
+                GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, false, (int)m, (int)ncols, n, -1.0f, w.A + (i0 + n) * d + i0, d, Xi,
+                                    d, 1.0f, w.Binv + (i0 + n) * d, d, false, s));
+            }
         }
     }
 
@@ -322,7 +387,7 @@ extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, fl
 // nothing extra, or a latency-sensitive path that cannot take cudaMalloc's implicit
 // device synchronisation. For them this entry point uses a fixed scratch area compiled
 // into the library as a file-scope __device__ array, sized for d <= kNoAllocMaxD.
-// Every GPU that loads the library holds this array (about 8.5 MiB) until the process
+// Every GPU that loads the library holds this array (about 10.5 MiB) until the process
 // exits. The entry point itself allocates nothing: no cudaMalloc, cudaFree or allocating
 // library routine.
 // ------------------------------------------------------------------------------------
@@ -333,18 +398,8 @@ namespace {
 
 constexpr int64_t kNoAllocMaxD = 1024;
 
-constexpr size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
-
-// the same slab sizes gptq_prepare carves from its workspace, for d = kNoAllocMaxD
-constexpr size_t noalloc_bytes(int64_t d) {
-    return a256(a256(a256(a256(a256(a256(sizeof(float) * d * d) + sizeof(float) * d * d) +
-                                    sizeof(float) * ((d + NB - 1) / NB) * NB * NB) +
-                               sizeof(float) * d) +
-                          sizeof(float) * d) +
-                     sizeof(int) * 4);
-}
-
-constexpr size_t kNoAllocBytes = noalloc_bytes(kNoAllocMaxD);
+// the workspace gptq_prepare carves for d = kNoAllocMaxD
+constexpr size_t kNoAllocBytes = prep_ws_bytes(kNoAllocMaxD);
 constexpr int kMaxDevices = 64;
 
 // Host code must not use this name as an address: on the host it is only a stand-in for

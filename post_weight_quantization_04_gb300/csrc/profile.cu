@@ -46,7 +46,8 @@ const char* kNames[K_COUNT] = {
     "prep_perm_kernel",    "prep_gather_kernel",  "potrf_diag_kernel", "sgemm_kernel[prepare]",
     "eye_kernel",          "prep_scatter_kernel", "init_work_kernel",  "row_params_kernel",
     "gptq_block_kernel",   "sgemm_kernel[trailing]", "g_idx_kernel",   "copy_loss_kernel",
-    "pack_kernel",         "rtn_kernel",
+    "pack_kernel",         "rtn_kernel",          "split_kernel",      "tc_gemm_nt_kernel[prepare]",
+    "tc_gemm_nt_kernel[trailing]",
 };
 
 }  // namespace

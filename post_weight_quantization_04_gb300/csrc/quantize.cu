@@ -22,6 +22,7 @@
 #include "common.cuh"
 #include "quant.cuh"
 #include "sgemm.cuh"
+#include "tc_gemm.cuh"
 
 namespace gptq {
 
@@ -34,9 +35,14 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct QuantWs {
     float* W;       // rows x cols working copy (loop order)
     float* Err;     // rows x QB
+    float* ehi;     // rows x QB: TF32 split of Err
+    float* elo;
+    float* uhi;     // cols x QB: TF32 split of U[blk, e:]^T
+    float* ulo;
     float* cur_s;   // rows: current scale (per-row grid, or a group wider than a block)
     float* cur_z;   // rows
     float* loss;    // rows
+    int* status;
     size_t bytes;
 };
 
@@ -44,16 +50,21 @@ QuantWs carve(void* base, int64_t rows, int64_t cols) {
     QuantWs w{};
     char* p = static_cast<char*>(base);
     size_t off = 0;
-    w.W = reinterpret_cast<float*>(p + off);
-    off = align256(off + sizeof(float) * rows * cols);
-    w.Err = reinterpret_cast<float*>(p + off);
-    off = align256(off + sizeof(float) * rows * QB);
-    w.cur_s = reinterpret_cast<float*>(p + off);
-    off = align256(off + sizeof(float) * rows);
-    w.cur_z = reinterpret_cast<float*>(p + off);
-    off = align256(off + sizeof(float) * rows);
-    w.loss = reinterpret_cast<float*>(p + off);
-    off = align256(off + sizeof(float) * rows);
+    auto take = [&](size_t bytes) {
+        char* q = p + off;
+        off = align256(off + bytes);
+        return q;
+    };
+    w.W = reinterpret_cast<float*>(take(sizeof(float) * rows * cols));
+    w.Err = reinterpret_cast<float*>(take(sizeof(float) * rows * QB));
+    w.ehi = reinterpret_cast<float*>(take(sizeof(float) * rows * QB));
+    w.elo = reinterpret_cast<float*>(take(sizeof(float) * rows * QB));
+    w.uhi = reinterpret_cast<float*>(take(sizeof(float) * cols * QB));
+    w.ulo = reinterpret_cast<float*>(take(sizeof(float) * cols * QB));
+    w.cur_s = reinterpret_cast<float*>(take(sizeof(float) * rows));
+    w.cur_z = reinterpret_cast<float*>(take(sizeof(float) * rows));
+    w.loss = reinterpret_cast<float*>(take(sizeof(float) * rows));
+    w.status = reinterpret_cast<int*>(take(sizeof(int) * 4));
     w.bytes = off;
     return w;
 }
@@ -479,6 +490,9 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         GPTQ_LAUNCH_CHECK();
     }
     GPTQ_CUDA_TRY(cudaMemsetAsync(w.loss, 0, sizeof(float) * rows, s));
+    GPTQ_CUDA_TRY(cudaMemsetAsync(w.status, 0, sizeof(int), s));
+    // tensor-core trailing update when every row of W and U is 16-byte aligned
+    const bool tc = (cols % 4 == 0) && tc_gemm_nt_ok(w.W, cols);
     const unsigned pgrid = (unsigned)ceil_div(rows, 8);
     if (q.group == 0) {
         GPTQ_LAUNCH(K_ROW_PARAMS, s, row_params_kernel<<<pgrid, 256, 0, s>>>(w.W, rows, cols, 0, cols, q.bits, q.sym,
@@ -541,9 +555,18 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         GPTQ_LAUNCH_CHECK();
         const int64_t e = j0 + bw;
         if (e < cols) {
-            GPTQ_CUDA_TRY(sgemm(K_SGEMM_TRAIL, false, (int)rows, (int)(cols - e), bw, -1.0f, w.Err, QB, U + j0 * cols + e, cols, 1.0f,
-                                w.W + e, cols, false, s));
+            if (tc) {
+                // W[:, e:] -= Err * U[blk, e:] as (Err) * (U[blk, e:]^T)^T on the tensor cores
+                GPTQ_CUDA_TRY(split_rows(K_SPLIT, w.Err, QB, (int)rows, bw, w.ehi, w.elo, QB, s));
+                GPTQ_CUDA_TRY(split_cols(K_SPLIT, U + j0 * cols + e, cols, bw, (int)(cols - e), w.uhi, w.ulo, QB, s));
+                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_TRAIL, (int)rows, (int)(cols - e), bw, -1.0f, w.ehi, w.elo, w.uhi, w.ulo,
+                                         QB, 1.0f, w.W + e, cols, false, w.status, s));
+            } else {
+                GPTQ_CUDA_TRY(sgemm(K_SGEMM_TRAIL, false, (int)rows, (int)(cols - e), bw, -1.0f, w.Err, QB,
+                                    U + j0 * cols + e, cols, 1.0f, w.W + e, cols, false, s));
+            }
         }
+
     }
     (void)sym;
 
@@ -555,8 +578,14 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         GPTQ_LAUNCH(K_COPY_LOSS, s, copy_loss_kernel<<<(unsigned)ceil_div(rows, 256), 256, 0, s>>>(w.loss, rows, row_loss));
         GPTQ_LAUNCH_CHECK();
     }
-    if (packed) return launch_pack(codes, rows, cols, q.bits, q.sym, packed, s);
-    return GPTQ_OK;
+    if (packed) {
+        const int rc = launch_pack(codes, rows, cols, q.bits, q.sym, packed, s);
+        if (rc != GPTQ_OK) return rc;
+    }
+    int hstatus = 0;
+    GPTQ_CUDA_TRY(cudaMemcpyAsync(&hstatus, w.status, sizeof(int), cudaMemcpyDeviceToHost, s));
+    GPTQ_CUDA_TRY(cudaStreamSynchronize(s));
+    return hstatus;
 }
 
 extern "C" int rtn_quantize(const float* W, int64_t rows, int64_t cols, const uint8_t* dead, gptq_qconfig q,

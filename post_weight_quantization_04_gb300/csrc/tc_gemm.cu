@@ -1,0 +1,402 @@
+// tc_gemm.cu — fp32-accurate NT GEMM on the 5th-generation tensor cores (3xTF32).
+//
+// C = beta * C + alpha * A * B^T for fp32 A (M x K) and B (N x K), both K-major. Each
+// operand comes pre-split into hi (the fp32 value with its low 13 mantissa bits cleared,
+// so exactly a TF32 number) and lo = value - hi (exact in fp32); the product is
+// Ahi*Bhi + Ahi*Blo + Alo*Bhi, which leaves an error of order 2^-20 relative per term
+// (the dropped Alo*Blo and the TF32 rounding of the lo parts), against 2^-11 for one TF32
+// pass. Accumulation is fp32 in TMEM.
+//
+// Structure (one CTA per SM, persistent over 128 x 128 output tiles):
+//   warp 0      TMA producer: per 32-wide K step, the four 128 x 32 fp32 boxes
+//               (Ahi, Alo, Bhi, Blo; 128-byte swizzle, K-major) into a 3-stage ring
+//   warp 1      single-thread tcgen05.mma issuer, kind::tf32, M = N = 128, K = 8 per
+//               instruction, three products per K step, into one of two TMEM
+//               accumulators (128 columns each)
+//   warps 2..5  epilogue: TMEM -> registers -> C read-modify-write in global memory,
+//               overlapping the MMAs of the next tile in the other accumulator
+// Every mbarrier wait is bounded (GPTQ_ERR_TIMEOUT into *status, then unwind).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "tc_gemm.cuh"
+
+namespace gptq {
+
+namespace {
+
+constexpr int G_BM = 128, G_BN = 128, G_BK = 32, G_STAGES = 3, G_THREADS = 192;
+constexpr int G_BOX = G_BM * G_BK * 4;         // 16 KB: one 128 x 32 fp32 box
+constexpr int G_STAGE = 4 * G_BOX;             // Ahi, Alo, Bhi, Blo
+constexpr int G_SMEM = G_STAGES * G_STAGE + 1024 + 256;
+constexpr uint32_t G_TMEM_COLS = 2 * G_BN;
+
+// kind::tf32: D fp32 (bits 4-5 = 1), A/B TF32 (2), both K-major, N >> 3, M >> 4
+constexpr uint32_t G_IDESC = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(G_BN >> 3) << 17) |
+                             ((uint32_t)(G_BM >> 4) << 24);
+
+struct GParams {
+    int M, N, K;
+    float alpha, beta;
+    float* C;
+    int64_t ldc;
+    int tiles_m, tiles_n, ntiles, lower_only;
+    int* status;
+};
+
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, int* status) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            set_status(status, GPTQ_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// linear tile index -> (tm, tn); with lower_only the tiles tn <= tm, row by row
+__device__ __forceinline__ void tile_of(const GParams& p, int t, int& tm, int& tn) {
+    if (!p.lower_only) {
+        tm = t / p.tiles_n;
+        tn = t % p.tiles_n;
+        return;
+    }
+    int r = 0;
+    for (;;) {
+        const int c = min(r + 1, p.tiles_n);
+        if (t < c) break;
+        t -= c;
+        ++r;
+    }
+    tm = r;
+    tn = t;
+}
+
+__global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_constant__ CUtensorMap tAh,
+                                                                  const __grid_constant__ CUtensorMap tAl,
+                                                                  const __grid_constant__ CUtensorMap tBh,
+                                                                  const __grid_constant__ CUtensorMap tBl,
+                                                                  const GParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G_STAGES * G_STAGE);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t sbase = smem_u32(smem), bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (G_STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * G_STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * G_STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * G_STAGES + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < G_STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tAh);
+        tma_prefetch_desc(&tAl);
+        tma_prefetch_desc(&tBh);
+        tma_prefetch_desc(&tBl);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), G_TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int ktiles = (p.K + G_BK - 1) / G_BK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_par = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
+                int tm, tn;
+                tile_of(p, t, tm, tn);
+                for (int kt = 0; kt < ktiles; ++kt) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(full_bar(stage), G_STAGE);
+                    const uint32_t sa = sbase + stage * G_STAGE;
+                    const int x = kt * G_BK;
+                    tma_load_2d(sa, &tAh, full_bar(stage), x, tm * G_BM);
+                    tma_load_2d(sa + G_BOX, &tAl, full_bar(stage), x, tm * G_BM);
+                    tma_load_2d(sa + 2 * G_BOX, &tBh, full_bar(stage), x, tn * G_BN);
+                    tma_load_2d(sa + 3 * G_BOX, &tBl, full_bar(stage), x, tn * G_BN);
+                    issued |= 1u << stage;
+                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == G_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (int s = 0; s < G_STAGES; ++s)
+                if (issued & (1u << s)) drain_wait(full_bar(s), (issued_par >> s) & 1u, p.status);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0, abuf = 0;
+            uint32_t phase = 0, aphase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
+                if (!mbar_wait(tempty_bar(abuf), aphase ^ 1u, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t dt = tmem_base + (uint32_t)(abuf * G_BN);
+                for (int kt = 0; kt < ktiles; ++kt) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = sbase + stage * G_STAGE;
+#pragma unroll
+                    for (int kk = 0; kk < G_BK / 8; ++kk) {
+                        // 8 TF32 = 32 bytes along K inside the 128-byte swizzle row
+                        const uint32_t off = kk * 32;
+                        const uint64_t ah = smem_desc(sa + off, 16, 1024, kSwizzle128B);
+                        const uint64_t al = smem_desc(sa + G_BOX + off, 16, 1024, kSwizzle128B);
+                        const uint64_t bh = smem_desc(sa + 2 * G_BOX + off, 16, 1024, kSwizzle128B);
+                        const uint64_t bl = smem_desc(sa + 3 * G_BOX + off, 16, 1024, kSwizzle128B);
+                        umma_tf32(dt, ah, bh, G_IDESC, (kt > 0 || kk > 0) ? 1u : 0u);
+                        umma_tf32(dt, ah, bl, G_IDESC, 1u);
+                        umma_tf32(dt, al, bh, G_IDESC, 1u);
+                    }
+                    umma_commit(empty_bar(stage));
+                    if (++stage == G_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull_bar(abuf));
+                if (++abuf == 2) {
+                    abuf = 0;
+                    aphase ^= 1u;
+                }
+            }
+            umma_commit(drain_bar);
+            drain_wait(drain_bar, 0, p.status);
+        }
+    } else {
+        const int q = warp & 3;
+        int abuf = 0;
+        uint32_t aphase = 0;
+        for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+            int tm, tn;
+            tile_of(p, t, tm, tn);
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(abuf), aphase, abort_flag, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            const int row = tm * G_BM + 32 * q + lane;
+            float* crow = p.C + (int64_t)(row < p.M ? row : 0) * p.ldc;
+            const uint32_t ta = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(abuf * G_BN);
+#pragma unroll 1
+            for (int c = 0; c < G_BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(ta + 32 * c, v);
+                tmem_ld_wait();
+                if (row < p.M) {
+                    const int gc0 = tn * G_BN + 32 * c;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const int gc = gc0 + i;
+                        if (gc + 3 < p.N) {
+                            float4* ptr = reinterpret_cast<float4*>(crow + gc);
+                            float4 o = make_float4(p.alpha * __uint_as_float(v[i]), p.alpha * __uint_as_float(v[i + 1]),
+                                                   p.alpha * __uint_as_float(v[i + 2]),
+                                                   p.alpha * __uint_as_float(v[i + 3]));
+                            if (p.beta != 0.0f) {
+                                const float4 cv = *ptr;
+                                o.x = fmaf(p.beta, cv.x, o.x);
+                                o.y = fmaf(p.beta, cv.y, o.y);
+                                o.z = fmaf(p.beta, cv.z, o.z);
+                                o.w = fmaf(p.beta, cv.w, o.w);
+                            }
+                            *ptr = o;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if (gc + e < p.N) {
+                                    const float o = p.alpha * __uint_as_float(v[i + e]);
+                                    crow[gc + e] = (p.beta != 0.0f) ? fmaf(p.beta, crow[gc + e], o) : o;
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(abuf));
+            if (++abuf == 2) {
+                abuf = 0;
+                aphase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, G_TMEM_COLS);
+    }
+}
+
+__device__ __forceinline__ void split1(float a, float& hi, float& lo) {
+    hi = __uint_as_float(__float_as_uint(a) & 0xFFFFE000u);
+    lo = a - hi;
+}
+
+__global__ void split_rows_kernel(const float* __restrict__ A, int64_t lda, int rows, int K, float* __restrict__ hi,
+                                  float* __restrict__ lo, int ldk) {
+    const int r = blockIdx.y;
+    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < K; k += gridDim.x * blockDim.x) {
+        float h, l;
+        split1(A[(int64_t)r * lda + k], h, l);
+        hi[(int64_t)r * ldk + k] = h;
+        lo[(int64_t)r * ldk + k] = l;
+    }
+}
+
+// B (K x N block, row stride ld) -> hi/lo (N x ldk), transposed through a 32 x 33 tile
+__global__ void __launch_bounds__(256) split_cols_kernel(const float* __restrict__ B, int64_t ld, int K, int N,
+                                                        float* __restrict__ hi, float* __restrict__ lo, int ldk) {
+    __shared__ float tile[32][33];
+    const int k0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int r = ty; r < 32; r += 8) {
+        const int k = k0 + r, n = n0 + tx;
+        tile[r][tx] = (k < K && n < N) ? B[(int64_t)k * ld + n] : 0.0f;
+    }
+    __syncthreads();
+    for (int r = ty; r < 32; r += 8) {
+        const int n = n0 + r, k = k0 + tx;
+        if (n < N && k < K) {
+            float h, l;
+            split1(tile[tx][r], h, l);
+            hi[(int64_t)n * ldk + k] = h;
+            lo[(int64_t)n * ldk + k] = l;
+        }
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, const float* base, int rows, int K, int ldk) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ldk * 4};
+    cuuint32_t box[2] = {(cuuint32_t)G_BK, (cuuint32_t)G_BM};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t split_rows(int id, const float* A, int64_t lda, int rows, int K, float* hi, float* lo, int ldk,
+                       cudaStream_t s) {
+    if (rows <= 0 || K <= 0) return cudaSuccess;
+    dim3 grid((unsigned)std::min((K + 255) / 256, 8), (unsigned)rows);
+    GPTQ_LAUNCH(id, s, split_rows_kernel<<<grid, 256, 0, s>>>(A, lda, rows, K, hi, lo, ldk));
+    return cudaGetLastError();
+}
+
+cudaError_t split_cols(int id, const float* B, int64_t ld, int K, int N, float* hi, float* lo, int ldk,
+                       cudaStream_t s) {
+    if (K <= 0 || N <= 0) return cudaSuccess;
+    dim3 grid((unsigned)((N + 31) / 32), (unsigned)((K + 31) / 32));
+    GPTQ_LAUNCH(id, s, split_cols_kernel<<<grid, 256, 0, s>>>(B, ld, K, N, hi, lo, ldk));
+    return cudaGetLastError();
+}
+
+bool tc_gemm_nt_ok(const float* C, int64_t ldc) {
+    return (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0) && encoder() != nullptr;
+}
+
+cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ahi, const float* Alo, const float* Bhi,
+                       const float* Blo, int ldk, float beta, float* C, int64_t ldc, bool lower_only, int* status,
+                       cudaStream_t s) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    CUtensorMap tah, tal, tbh, tbl;
+    if (!make_map(&tah, Ahi, M, K, ldk) || !make_map(&tal, Alo, M, K, ldk) || !make_map(&tbh, Bhi, N, K, ldk) ||
+        !make_map(&tbl, Blo, N, K, ldk))
+        return cudaErrorInvalidValue;
+    GParams p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = C;
+    p.ldc = ldc;
+    p.tiles_m = (M + G_BM - 1) / G_BM;
+    p.tiles_n = (N + G_BN - 1) / G_BN;
+    p.lower_only = lower_only ? 1 : 0;
+    if (lower_only) {
+        int cnt = 0;
+        for (int r = 0; r < p.tiles_m; ++r) cnt += std::min(r + 1, p.tiles_n);
+        p.ntiles = cnt;
+    } else {
+        p.ntiles = p.tiles_m * p.tiles_n;
+    }
+    p.status = status;
+    if (p.ntiles == 0) return cudaSuccess;
+    static const int sms = device_sm_count();
+    const int grid = std::min(p.ntiles, sms);
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_nt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
+    if (e != cudaSuccess) return e;
+    GPTQ_LAUNCH(id, s, tc_gemm_nt_kernel<<<grid, G_THREADS, G_SMEM, s>>>(tah, tal, tbh, tbl, p));
+    return cudaGetLastError();
+}
+
+}  // namespace gptq

@@ -1,0 +1,31 @@
+// tc_gemm.cuh — fp32-accurate NT GEMM on the tensor cores (3xTF32), and the operand splits.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gptq {
+
+// A (rows x K, row stride lda) -> hi, lo (rows x ldk, dense), hi = A with the low 13
+// mantissa bits cleared (exactly representable in TF32), lo = A - hi (exact in fp32).
+// Columns K..ldk-1 of hi/lo are left untouched (the GEMM never reads them).
+cudaError_t split_rows(int id, const float* A, int64_t lda, int rows, int K, float* hi, float* lo, int ldk,
+                       cudaStream_t s);
+
+// The same for the transpose of a (K x N, row stride ld) block: hi/lo are (N x ldk) with
+// hi[n][k] = split(B[k][n]).
+cudaError_t split_cols(int id, const float* B, int64_t ld, int K, int N, float* hi, float* lo, int ldk,
+                       cudaStream_t s);
+
+// C[M x N] (ldc) = beta * C + alpha * (A * B^T) with A given as (Ahi, Alo) M x K and B as
+// (Bhi, Blo) N x K, both K-major with row stride ldk (ldk % 4 == 0, 16-byte aligned).
+// Products Ahi*Bhi + Ahi*Blo + Alo*Bhi on tcgen05 (kind::tf32), fp32 accumulation in TMEM.
+// lower_only skips 128 x 128 C tiles entirely above the diagonal. C must not overlap the
+// operands. Returns false (nothing launched) if C's stride or alignment rules out the
+// vectorised epilogue; the caller then uses the FFMA path.
+bool tc_gemm_nt_ok(const float* C, int64_t ldc);
+cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ahi, const float* Alo, const float* Bhi,
+                       const float* Blo, int ldk, float beta, float* C, int64_t ldc, bool lower_only, int* status,
+                       cudaStream_t s);
+
+}  // namespace gptq
