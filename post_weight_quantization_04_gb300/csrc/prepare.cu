@@ -37,10 +37,16 @@ struct PrepWs {
     float* A;
     float* Binv;
     float* LinvD;
-    float* ahi;   // d x NB: TF32 split of the GEMM's first operand
+    float* ahi;   // d x NB TF32 splits: the panel before its triangular solve,
     float* alo;
-    float* bhi;   // d x NB: TF32 split of the second operand
+    float* bhi;   //   the block row of the inverse (transposed),
     float* blo;
+    float* phi;   //   L21 (the solved panel),
+    float* plo;
+    float* xhi;   //   the new block row of L^-1 (transposed),
+    float* xlo;
+    float* lhi;   // NB x NB: L_kk^-1
+    float* llo;
     float* ddiag;
     float* rr;
     int* status;
@@ -50,14 +56,15 @@ struct PrepWs {
 constexpr size_t align256c(size_t x) { return (x + 255) & ~size_t(255); }
 
 // slab sizes, in carve order; the total is also the size of the allocation-free scratch
+constexpr int kPrepSlabs = 16;
 constexpr size_t prep_slab(int64_t d, int i) {
     return i < 2 ? sizeof(float) * d * d
          : i == 2 ? sizeof(float) * ((d + NB - 1) / NB) * NB * NB
-         : i < 7 ? sizeof(float) * d * NB
-         : i < 9 ? sizeof(float) * d
+         : i < 11 ? sizeof(float) * d * NB
+         : i < 13 ? sizeof(float) * NB * NB
+         : i < 15 ? sizeof(float) * d
          : sizeof(int) * 4;
 }
-constexpr int kPrepSlabs = 10;
 constexpr size_t prep_ws_bytes(int64_t d) {
     size_t off = 0;
     for (int i = 0; i < kPrepSlabs; ++i) off = align256c(off + prep_slab(d, i));
@@ -69,16 +76,10 @@ PrepWs carve(void* base, int64_t d) {
     char* p = static_cast<char*>(base);
     size_t off[kPrepSlabs + 1] = {0};
     for (int i = 0; i < kPrepSlabs; ++i) off[i + 1] = align256c(off[i] + prep_slab(d, i));
-    w.A = reinterpret_cast<float*>(p + off[0]);
-    w.Binv = reinterpret_cast<float*>(p + off[1]);
-    w.LinvD = reinterpret_cast<float*>(p + off[2]);
-    w.ahi = reinterpret_cast<float*>(p + off[3]);
-    w.alo = reinterpret_cast<float*>(p + off[4]);
-    w.bhi = reinterpret_cast<float*>(p + off[5]);
-    w.blo = reinterpret_cast<float*>(p + off[6]);
-    w.ddiag = reinterpret_cast<float*>(p + off[7]);
-    w.rr = reinterpret_cast<float*>(p + off[8]);
-    w.status = reinterpret_cast<int*>(p + off[9]);
+    float** f[] = {&w.A, &w.Binv, &w.LinvD, &w.ahi, &w.alo, &w.bhi, &w.blo, &w.phi, &w.plo,
+                   &w.xhi, &w.xlo, &w.lhi, &w.llo, &w.ddiag, &w.rr};
+    for (int i = 0; i < 15; ++i) *f[i] = reinterpret_cast<float*>(p + off[i]);
+    w.status = reinterpret_cast<int*>(p + off[15]);
     w.bytes = off[kPrepSlabs];
     return w;
 }
@@ -163,91 +164,184 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
     A[i * d + j] = v;
 }
 
-// One CTA factors the diagonal block A[k0:k0+n, k0:k0+n] = L L^T in place (lower), and
-// writes L^-1 (lower, NB x NB, zeros above) to Linv. A non-positive or non-finite pivot
-// records GPTQ_ERR_NOT_SPD (and is replaced by 1 so the kernel finishes).
-//
-// One loop over k produces column k of L (right-looking Cholesky) and applies the matching
-// Gauss-Jordan step to X = [I -> L^-1]: X[i][:] -= L[i][k] * X[k][:] / L[k][k] for i > k and
-// X[k][:] /= L[k][k]. Everything a thread updates lives in its registers: thread (j, q)
-// holds rows 32q..32q+31 of column j of the block, and columns 32q..32q+31 of row j of X.
-// At step k the four threads of column k publish the (raw) pivot column, and of row k of X,
-// to double-buffered shared arrays; after one barrier every thread updates its registers
-// with broadcast reads. Entries above the diagonal of the block are updated too (unused),
-// so the update needs no per-element predicate; columns of X beyond k read zeros.
-__global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, int64_t lda, int64_t k0, int n,
-                                                        float* __restrict__ Linv, int* __restrict__ status) {
-    __shared__ __align__(16) float colraw[2][NB];
-    __shared__ __align__(16) float xraw[2][NB];
-    __shared__ float dg[NB];
-    const int tid = threadIdx.x;
-    const int q = tid >> 7;                                 // row / column slab 32q..32q+31
-    const int j = ((tid & 31) << 2) | ((tid >> 5) & 3);     // column of L, row of X (spread over SMSPs)
-    const int r0 = 32 * q;
-
-    float sc[32], xr[32];
+// Warp-level Cholesky + inverse of a (nb <= 32)-square block held in shared memory (row
+// stride LD): lane r keeps row r of the block and row r of X in registers; column k of L
+// and row k of X are broadcast with shuffles. On return the lower triangles hold L and
+// X = L^-1. One Gauss-Jordan step on [L | I] accompanies each Cholesky column step.
+template <int LD>
+__device__ __forceinline__ void chol_inv_32(float* Sb, float* Xb, int nb, int* status) {
+    const int r = threadIdx.x & 31;
+    float a[32], x[32];
 #pragma unroll
-    for (int t = 0; t < 32; ++t) {
-        const int i = r0 + t;
-        sc[t] = (i < n && j < n && i >= j) ? A[(k0 + i) * lda + k0 + j] : 0.0f;
-        xr[t] = (i == j && j < n) ? 1.0f : 0.0f;
+    for (int c = 0; c < 32; ++c) {
+        a[c] = (r < nb && c <= r) ? Sb[r * LD + c] : 0.0f;
+        x[c] = (r < nb && c == r) ? 1.0f : 0.0f;
     }
-
-    for (int k = 0; k < n; ++k) {
-        const int b = k & 1;
-        if (j == k) {
 #pragma unroll
-            for (int t = 0; t < 32; t += 4) {
-                *reinterpret_cast<float4*>(&colraw[b][r0 + t]) = make_float4(sc[t], sc[t + 1], sc[t + 2], sc[t + 3]);
-                *reinterpret_cast<float4*>(&xraw[b][r0 + t]) = make_float4(xr[t], xr[t + 1], xr[t + 2], xr[t + 3]);
-            }
-        }
-        __syncthreads();
-        float piv = colraw[b][k];
+    for (int k = 0; k < 32; ++k) {
+        if (k >= nb) break;
+        float piv = __shfl_sync(0xffffffffu, a[k], k);
         if (!(piv > 0.0f) || !isfinite(piv)) {
-            if (tid == 0) set_status(status, GPTQ_ERR_NOT_SPD);
+            if (r == 0) set_status(status, GPTQ_ERR_NOT_SPD);
             piv = 1.0f;
         }
         const float lkk = sqrtf(piv);
         const float inv = 1.0f / lkk;
-        if (j > k && j < n) {
-            const float f = colraw[b][j] * (inv * inv);     // L[j][k] / L[k][k]
+        const float l = a[k] * inv;  // L[r][k] (lanes r > k)
 #pragma unroll
-            for (int t = 0; t < 32; t += 4) {
-                const float4 c4 = *reinterpret_cast<const float4*>(&colraw[b][r0 + t]);
-                const float4 x4 = *reinterpret_cast<const float4*>(&xraw[b][r0 + t]);
-                sc[t] = fmaf(-c4.x, f, sc[t]);
-                sc[t + 1] = fmaf(-c4.y, f, sc[t + 1]);
-                sc[t + 2] = fmaf(-c4.z, f, sc[t + 2]);
-                sc[t + 3] = fmaf(-c4.w, f, sc[t + 3]);
-                xr[t] = fmaf(-f, x4.x, xr[t]);
-                xr[t + 1] = fmaf(-f, x4.y, xr[t + 1]);
-                xr[t + 2] = fmaf(-f, x4.z, xr[t + 2]);
-                xr[t + 3] = fmaf(-f, x4.w, xr[t + 3]);
-            }
-        } else if (j == k) {
+        for (int c = k + 1; c < 32; ++c) a[c] = fmaf(-l, __shfl_sync(0xffffffffu, l, c), a[c]);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                sc[t] *= inv;
-                xr[t] *= inv;
-            }
-            if (q == 0) dg[k] = lkk;
+        for (int c = 0; c <= k; ++c) {
+            const float xkc = __shfl_sync(0xffffffffu, x[c], k) * inv;  // X[k][c] / L[k][k]
+            x[c] = (r == k) ? xkc : (r > k ? fmaf(-l, xkc, x[c]) : x[c]);
+        }
+        a[k] = (r == k) ? lkk : l;
+    }
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        if (r < nb && c <= r) {
+            Sb[r * LD + c] = a[c];
+            Xb[r * LD + c] = x[c];
         }
     }
-    __syncthreads();
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-        const int i = r0 + t;
-        if (i < n && j < n && i >= j) A[(k0 + i) * lda + k0 + j] = (i == j) ? dg[j] : sc[t];
+}
+
+// One CTA factors the diagonal block A[k0:k0+n, k0:k0+n] = L L^T in place (lower), and
+// writes L^-1 (lower, NB x NB, zeros above) to Linv. A non-positive or non-finite pivot
+// records GPTQ_ERR_NOT_SPD (and is replaced by 1 so the kernel finishes).
+//
+// Blocked by 32 columns inside shared memory: for each 32-column panel, warp 0 factors
+// and inverts the 32 x 32 diagonal block (chol_inv_32), then all threads form the panel
+// below it (L21 = A21 * X11^T) and update the trailing block (A22 -= L21 L21^T). The
+// off-diagonal 32 x 32 blocks of L^-1 follow block row by block row:
+// X_ij = -X_ii * sum_{j<=k<i} L_ik X_kj.
+__global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, int64_t lda, int64_t k0, int n,
+                                                        float* __restrict__ Linv, float* __restrict__ Lhi,
+                                                        float* __restrict__ Llo, int* __restrict__ status) {
+    extern __shared__ float sm[];
+    constexpr int LD = NB + 1;
+    float* S = sm;              // NB x LD: the block, then L
+    float* X = sm + NB * LD;    // NB x LD: L^-1
+    const int tid = threadIdx.x, warp = tid >> 5;
+
+    for (int idx = tid; idx < NB * NB; idx += 512) {
+        const int i = idx >> 7, j = idx & (NB - 1);
+        S[i * LD + j] = (i < n && j <= i) ? A[(k0 + i) * lda + k0 + j] : 0.0f;
+        X[i * LD + j] = 0.0f;
     }
+    __syncthreads();
+
+    for (int b = 0; b < n; b += 32) {
+        const int nb = min(32, n - b);
+        if (warp == 0) chol_inv_32<LD>(S + b * LD + b, X + b * LD + b, nb, status);
+        __syncthreads();
+        const int rb = b + 32, m = n - rb;
+        if (m <= 0) break;
+        // panel: S[r][b+c] = sum_{k<=c} S[r][b+k] * X[b+c][b+k], rows rb..n-1; 4 threads per row
+        {
+            const int r = rb + (tid >> 2), cq = (tid & 3) * 8;
+            float in[32], out[8];
+            if (r < n) {
 #pragma unroll
-    for (int t = 0; t < 32; t += 4) {
-        float4 v;
-        v.x = (j < n && r0 + t <= j) ? xr[t] : 0.0f;
-        v.y = (j < n && r0 + t + 1 <= j) ? xr[t + 1] : 0.0f;
-        v.z = (j < n && r0 + t + 2 <= j) ? xr[t + 2] : 0.0f;
-        v.w = (j < n && r0 + t + 3 <= j) ? xr[t + 3] : 0.0f;
-        *reinterpret_cast<float4*>(&Linv[j * NB + r0 + t]) = v;
+                for (int k = 0; k < 32; ++k) in[k] = S[r * LD + b + k];
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const float* xr = X + (b + cq + cc) * LD + b;
+                    float acc = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) acc = fmaf(in[k], xr[k], acc);
+                    out[cc] = acc;
+                }
+            }
+            __syncthreads();
+            if (r < n) {
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) S[r * LD + b + cq + cc] = out[cc];
+            }
+        }
+        __syncthreads();
+        // trailing: S[r][c] -= sum_k L[r][b+k] L[c][b+k], rb <= c <= r < n, 4 x 4 tiles
+        {
+            const int tdim = (m + 3) >> 2;
+            for (int t = tid; t < tdim * tdim; t += 512) {
+                const int ti = t / tdim, tj = t % tdim;
+                if (tj > ti) continue;
+                const int r0 = rb + 4 * ti, c0 = rb + 4 * tj;
+                float acc[4][4] = {};
+#pragma unroll 8
+                for (int k = 0; k < 32; ++k) {
+                    float ar[4], bc[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        ar[u] = (r0 + u < n) ? S[(r0 + u) * LD + b + k] : 0.0f;
+                        bc[u] = (c0 + u < n) ? S[(c0 + u) * LD + b + k] : 0.0f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(ar[u], bc[v], acc[u][v]);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        if (r0 + u < n && c0 + v <= r0 + u) S[(r0 + u) * LD + c0 + v] -= acc[u][v];
+            }
+        }
+        __syncthreads();
+    }
+
+    // off-diagonal blocks of L^-1, one 32-row block row at a time
+    for (int bi = 32; bi < n; bi += 32) {
+        const int ni = min(32, n - bi);
+        const int nj = bi / 32;  // blocks j = 0 .. nj-1 to fill in this block row
+        // T_j = sum_{k=j}^{i-1} L_ik X_kj, kept in registers, one element per thread per pass
+        float tv[6];
+        int cnt = 0;
+        for (int e = tid; e < nj * 1024; e += 512, ++cnt) {
+            const int jb = e >> 10, rr = (e >> 5) & 31, cc = e & 31;
+            const int row = bi + rr, col = jb * 32 + cc;
+            float acc = 0.0f;
+            if (rr < ni)
+                for (int k = col; k < bi; ++k) acc = fmaf(S[row * LD + k], X[k * LD + col], acc);
+            tv[cnt] = acc;
+        }
+        __syncthreads();
+        cnt = 0;
+        for (int e = tid; e < nj * 1024; e += 512, ++cnt) {
+            const int jb = e >> 10, rr = (e >> 5) & 31, cc = e & 31;
+            const int col = jb * 32 + cc;
+            if (rr < ni) X[(bi + rr) * LD + col] = tv[cnt];   // stage T in place
+        }
+        __syncthreads();
+        cnt = 0;
+        for (int e = tid; e < nj * 1024; e += 512, ++cnt) {
+            const int jb = e >> 10, rr = (e >> 5) & 31, cc = e & 31;
+            const int col = jb * 32 + cc;
+            float acc = 0.0f;
+            if (rr < ni)
+                for (int k = 0; k <= rr; ++k) acc = fmaf(X[(bi + rr) * LD + bi + k], X[(bi + k) * LD + col], acc);
+            tv[cnt] = -acc;
+        }
+        __syncthreads();
+        cnt = 0;
+        for (int e = tid; e < nj * 1024; e += 512, ++cnt) {
+            const int jb = e >> 10, rr = (e >> 5) & 31, cc = e & 31;
+            if (rr < ni) X[(bi + rr) * LD + jb * 32 + cc] = tv[cnt];
+        }
+        __syncthreads();
+    }
+
+    for (int idx = tid; idx < NB * NB; idx += 512) {
+        const int i = idx >> 7, j = idx & (NB - 1);
+        if (i < n && j <= i) A[(k0 + i) * lda + k0 + j] = S[i * LD + j];
+        const float v = (i < n && j <= i) ? X[i * LD + j] : 0.0f;
+        Linv[idx] = v;
+        if (Lhi) {  // TF32 split for the tensor-core products that use L_kk^-1
+            const float h = __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+            Lhi[idx] = h;
+            Llo[idx] = v - h;
+        }
     }
 }
 
@@ -302,68 +396,84 @@ extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, fl
         GPTQ_LAUNCH_CHECK();
     }
 
-    const size_t potrf_smem = 0;
+    const size_t potrf_smem = sizeof(float) * 2 * NB * (NB + 1);
+    GPTQ_CUDA_TRY(cudaFuncSetAttribute(potrf_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)potrf_smem));
 
     // The trailing contractions run on the tensor cores (3xTF32, operands split into
-    // TF32 hi/lo first) when every matrix row is 16-byte aligned, else on the FFMA GEMM.
+    // TF32 hi/lo) when every matrix row is 16-byte aligned, else on the FFMA GEMM.
     const bool tc = (d % 4 == 0) && tc_gemm_nt_ok(w.A, d);
 
-    // blocked right-looking Cholesky of A (lower)
     const int64_t nblk = ceil_div(d, NB);
-    for (int64_t kb = 0; kb < nblk; ++kb) {
-        const int64_t k0 = kb * NB;
-        const int n = (int)std::min<int64_t>(NB, d - k0);
-        float* LinvK = w.LinvD + kb * NB * NB;
-        GPTQ_LAUNCH(K_POTRF, s, potrf_diag_kernel<<<1, 512, potrf_smem, s>>>(w.A, d, k0, n, LinvK, w.status));
-        GPTQ_LAUNCH_CHECK();
-        const int64_t m = d - k0 - n;
-        if (m <= 0) continue;
-        float* P = w.A + (k0 + n) * d + k0;
-        float* A22 = w.A + (k0 + n) * d + k0 + n;
-        if (tc) {
-            // panel: P <- P * Linv_kk^T
-            GPTQ_CUDA_TRY(split_rows(K_SPLIT, P, d, (int)m, n, w.ahi, w.alo, NB, s));
-            GPTQ_CUDA_TRY(split_rows(K_SPLIT, LinvK, NB, n, n, w.bhi, w.blo, NB, s));
-            GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, n, n, 1.0f, w.ahi, w.alo, w.bhi, w.blo, NB, 0.0f, P, d, false,
-                                     w.status, s));
-            // trailing: A22 -= P P^T (lower tiles)
-            GPTQ_CUDA_TRY(split_rows(K_SPLIT, P, d, (int)m, n, w.ahi, w.alo, NB, s));
-            GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, (int)m, n, -1.0f, w.ahi, w.alo, w.ahi, w.alo, NB, 1.0f, A22, d,
-                                     true, w.status, s));
-        } else {
-            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, true, (int)m, n, n, 1.0f, P, d, LinvK, NB, 0.0f, P, d, false, s));
-            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, true, (int)m, (int)m, n, -1.0f, P, d, P, d, 1.0f, A22, d, true, s));
-        }
-    }
-
-    // L^-1 by block rows: X[i,:] = Linv_ii * B[i,:];  B[i+1:, :] -= L[i+1:, i] X[i, :]
     GPTQ_LAUNCH(K_EYE, s, eye_kernel<<<(unsigned)ceil_div(d * d, 256), 256, 0, s>>>(w.Binv, d));
     GPTQ_LAUNCH_CHECK();
-    for (int64_t ib = 0; ib < nblk; ++ib) {
-        const int64_t i0 = ib * NB;
-        const int n = (int)std::min<int64_t>(NB, d - i0);
-        const int64_t ncols = i0 + n;
-        float* Xi = w.Binv + i0 * d;
-        float* LinvI = w.LinvD + ib * NB * NB;
-        const int64_t m = d - i0 - n;
-        if (tc) {
-            // X[i,:] = Linv_ii * X[i,:]: second operand is X[i, 0:ncols]^T (ncols x n)
-            GPTQ_CUDA_TRY(split_rows(K_SPLIT, LinvI, NB, n, n, w.ahi, w.alo, NB, s));
-            GPTQ_CUDA_TRY(split_cols(K_SPLIT, Xi, d, n, (int)ncols, w.bhi, w.blo, NB, s));
-            GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, n, (int)ncols, n, 1.0f, w.ahi, w.alo, w.bhi, w.blo, NB, 0.0f, Xi, d,
-                                     false, w.status, s));
+    if (tc) {
+        // Blocked right-looking Cholesky of A (lower) with the block-row inverse step of
+        // L^-1 interleaved: after panel k is factored, X[k,:] = L_kk^-1 B[k,:] and
+        // B[k+1:, :] -= L21 X[k, :] reuse the panel's TF32 splits.
+        for (int64_t kb = 0; kb < nblk; ++kb) {
+            const int64_t k0 = kb * NB;
+            const int n = (int)std::min<int64_t>(NB, d - k0);
+            const int64_t m = d - k0 - n, ncols = k0 + n;
+            float* LinvK = w.LinvD + kb * NB * NB;
+            GPTQ_LAUNCH(K_POTRF, s, potrf_diag_kernel<<<1, 512, potrf_smem, s>>>(w.A, d, k0, n, LinvK, w.lhi, w.llo,
+                                                                                 w.status));
+            GPTQ_LAUNCH_CHECK();
+            float* P = w.A + (k0 + n) * d + k0;
             if (m > 0) {
-                GPTQ_CUDA_TRY(split_rows(K_SPLIT, w.A + (i0 + n) * d + i0, d, (int)m, n, w.ahi, w.alo, NB, s));
-                GPTQ_CUDA_TRY(split_cols(K_SPLIT, Xi, d, n, (int)ncols, w.bhi, w.blo, NB, s));
-                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, (int)ncols, n, -1.0f, w.ahi, w.alo, w.bhi, w.blo, NB, 1.0f,
-                                         w.Binv + (i0 + n) * d, d, false, w.status, s));
+                SplitOut l21;  // L21 split for the trailing update and the inverse step
+                l21.hi = w.phi;
+                l21.lo = w.plo;
+                l21.ld = NB;
+                l21.mode = 1;
+                GPTQ_CUDA_TRY(split_rows(K_SPLIT, P, d, (int)m, n, w.ahi, w.alo, NB, s));
+                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, n, n, 1.0f, w.ahi, w.alo, w.lhi, w.llo, NB, 0.0f, P, d,
+                                         false, w.status, s, l21));
+                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, (int)m, n, -1.0f, w.phi, w.plo, w.phi, w.plo, NB, 1.0f,
+                                         w.A + (k0 + n) * d + k0 + n, d, true, w.status, s));
             }
-        } else {
-            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, false, n, (int)ncols, n, 1.0f, LinvI, NB, Xi, d, 0.0f, Xi, d, false, s));
+            float* Xi = w.Binv + k0 * d;
+            SplitOut xt;  // X[k, 0:ncols]^T split for the inverse's trailing update
+            xt.hi = w.xhi;
+            xt.lo = w.xlo;
+            xt.ld = NB;
+            xt.mode = 2;
+            GPTQ_CUDA_TRY(split_cols(K_SPLIT, Xi, d, n, (int)ncols, w.bhi, w.blo, NB, s));
+            GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, n, (int)ncols, n, 1.0f, w.lhi, w.llo, w.bhi, w.blo, NB, 0.0f, Xi, d,
+                                     false, w.status, s, xt));
             if (m > 0) {
+                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, (int)ncols, n, -1.0f, w.phi, w.plo, w.xhi, w.xlo, NB, 1.0f,
+                                         w.Binv + (k0 + n) * d, d, false, w.status, s));
+            }
+        }
+    } else {
+        // blocked right-looking Cholesky of A (lower), FFMA trailing products
+        for (int64_t kb = 0; kb < nblk; ++kb) {
+            const int64_t k0 = kb * NB;
+            const int n = (int)std::min<int64_t>(NB, d - k0);
+            float* LinvK = w.LinvD + kb * NB * NB;
+            GPTQ_LAUNCH(K_POTRF, s, potrf_diag_kernel<<<1, 512, potrf_smem, s>>>(w.A, d, k0, n, LinvK, nullptr,
+                                                                                 nullptr, w.status));
+            GPTQ_LAUNCH_CHECK();
+            const int64_t m = d - k0 - n;
+            if (m <= 0) continue;
+            float* P = w.A + (k0 + n) * d + k0;
+            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, true, (int)m, n, n, 1.0f, P, d, LinvK, NB, 0.0f, P, d, false, s));
+            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, true, (int)m, (int)m, n, -1.0f, P, d, P, d, 1.0f,
+                                w.A + (k0 + n) * d + k0 + n, d, true, s));
+        }
+        // L^-1 by block rows: X[i,:] = Linv_ii * B[i,:];  B[i+1:, :] -= L[i+1:, i] X[i, :]
+        for (int64_t ib = 0; ib < nblk; ++ib) {
+            const int64_t i0 = ib * NB;
+            const int n = (int)std::min<int64_t>(NB, d - i0);
+            const int64_t ncols = i0 + n;
+            float* Xi = w.Binv + i0 * d;
+            const int64_t m = d - i0 - n;
+            GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, false, n, (int)ncols, n, 1.0f, w.LinvD + ib * NB * NB, NB, Xi, d, 0.0f,
+                                Xi, d, false, s));
+            if (m > 0)
                 GPTQ_CUDA_TRY(sgemm(K_SGEMM_PREP, false, (int)m, (int)ncols, n, -1.0f, w.A + (i0 + n) * d + i0, d, Xi,
                                     d, 1.0f, w.Binv + (i0 + n) * d, d, false, s));
-            }
         }
     }
 

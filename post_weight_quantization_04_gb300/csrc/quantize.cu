@@ -37,7 +37,7 @@ struct QuantWs {
     float* Err;     // rows x QB
     float* ehi;     // rows x QB: TF32 split of Err
     float* elo;
-    float* uhi;     // cols x QB: TF32 split of U[blk, e:]^T
+    float* uhi;     // cols x cols: TF32 split of U^T
     float* ulo;
     float* cur_s;   // rows: current scale (per-row grid, or a group wider than a block)
     float* cur_z;   // rows
@@ -59,8 +59,8 @@ QuantWs carve(void* base, int64_t rows, int64_t cols) {
     w.Err = reinterpret_cast<float*>(take(sizeof(float) * rows * QB));
     w.ehi = reinterpret_cast<float*>(take(sizeof(float) * rows * QB));
     w.elo = reinterpret_cast<float*>(take(sizeof(float) * rows * QB));
-    w.uhi = reinterpret_cast<float*>(take(sizeof(float) * cols * QB));
-    w.ulo = reinterpret_cast<float*>(take(sizeof(float) * cols * QB));
+    w.uhi = reinterpret_cast<float*>(take(sizeof(float) * cols * cols));
+    w.ulo = reinterpret_cast<float*>(take(sizeof(float) * cols * cols));
     w.cur_s = reinterpret_cast<float*>(take(sizeof(float) * rows));
     w.cur_z = reinterpret_cast<float*>(take(sizeof(float) * rows));
     w.loss = reinterpret_cast<float*>(take(sizeof(float) * rows));
@@ -122,6 +122,8 @@ struct BlockArgs {
     const float* cur_s;
     const float* cur_z;
     float* Err;
+    float* ehi;  // optional TF32 split of Err (rows x QB)
+    float* elo;
     int8_t* codes;
     float* Wq;
     const int32_t* perm;
@@ -313,6 +315,19 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
     for (int m = 0; m < NCH; ++m) {
         const int c0 = col_of(m, 0);
         *reinterpret_cast<float4*>(erow + c0) = make_float4(er[4 * m], er[4 * m + 1], er[4 * m + 2], er[4 * m + 3]);
+        if (a.ehi) {
+            float4 h, l;
+            h.x = __uint_as_float(__float_as_uint(er[4 * m]) & 0xFFFFE000u);
+            h.y = __uint_as_float(__float_as_uint(er[4 * m + 1]) & 0xFFFFE000u);
+            h.z = __uint_as_float(__float_as_uint(er[4 * m + 2]) & 0xFFFFE000u);
+            h.w = __uint_as_float(__float_as_uint(er[4 * m + 3]) & 0xFFFFE000u);
+            l.x = er[4 * m] - h.x;
+            l.y = er[4 * m + 1] - h.y;
+            l.z = er[4 * m + 2] - h.z;
+            l.w = er[4 * m + 3] - h.w;
+            *reinterpret_cast<float4*>(a.ehi + row * QB + c0) = h;
+            *reinterpret_cast<float4*>(a.elo + row * QB + c0) = l;
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int lc = c0 + e;
@@ -493,6 +508,7 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
     GPTQ_CUDA_TRY(cudaMemsetAsync(w.status, 0, sizeof(int), s));
     // tensor-core trailing update when every row of W and U is 16-byte aligned
     const bool tc = (cols % 4 == 0) && tc_gemm_nt_ok(w.W, cols);
+    if (tc) GPTQ_CUDA_TRY(split_cols(K_SPLIT, U, cols, (int)cols, (int)cols, w.uhi, w.ulo, (int)cols, s));
     const unsigned pgrid = (unsigned)ceil_div(rows, 8);
     if (q.group == 0) {
         GPTQ_LAUNCH(K_ROW_PARAMS, s, row_params_kernel<<<pgrid, 256, 0, s>>>(w.W, rows, cols, 0, cols, q.bits, q.sym,
@@ -532,6 +548,8 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
     a.cur_s = w.cur_s;
     a.cur_z = w.cur_z;
     a.Err = w.Err;
+    a.ehi = tc ? w.ehi : nullptr;
+    a.elo = tc ? w.elo : nullptr;
     a.codes = codes;
     a.Wq = Wq;
     a.perm = perm;
@@ -556,11 +574,12 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         const int64_t e = j0 + bw;
         if (e < cols) {
             if (tc) {
-                // W[:, e:] -= Err * U[blk, e:] as (Err) * (U[blk, e:]^T)^T on the tensor cores
-                GPTQ_CUDA_TRY(split_rows(K_SPLIT, w.Err, QB, (int)rows, bw, w.ehi, w.elo, QB, s));
-                GPTQ_CUDA_TRY(split_cols(K_SPLIT, U + j0 * cols + e, cols, bw, (int)(cols - e), w.uhi, w.ulo, QB, s));
-                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_TRAIL, (int)rows, (int)(cols - e), bw, -1.0f, w.ehi, w.elo, w.uhi, w.ulo,
-                                         QB, 1.0f, w.W + e, cols, false, w.status, s));
+                // W[:, e:] -= Err * U[blk, e:] = Err * (U^T[e:, blk])^T on the tensor cores
+                SplitOut o;
+                o.ldb = cols;
+                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_TRAIL, (int)rows, (int)(cols - e), bw, -1.0f, w.ehi, w.elo,
+                                         w.uhi + e * cols + j0, w.ulo + e * cols + j0, QB, 1.0f, w.W + e, cols, false,
+                                         w.status, s, o));
             } else {
                 GPTQ_CUDA_TRY(sgemm(K_SGEMM_TRAIL, false, (int)rows, (int)(cols - e), bw, -1.0f, w.Err, QB,
                                     U + j0 * cols + e, cols, 1.0f, w.W + e, cols, false, s));

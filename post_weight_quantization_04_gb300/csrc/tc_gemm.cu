@@ -9,12 +9,13 @@
 //
 // Structure (one CTA per SM, persistent over 128 x 128 output tiles):
 //   warp 0      TMA producer: per 32-wide K step, the four 128 x 32 fp32 boxes
-//               (Ahi, Alo, Bhi, Blo; 128-byte swizzle, K-major) into a 3-stage ring
+//               (Ahi, Alo, Bhi, Blo; 128-byte swizzle, K-major) into a 2-stage ring
 //   warp 1      single-thread tcgen05.mma issuer, kind::tf32, M = N = 128, K = 8 per
 //               instruction, three products per K step, into one of two TMEM
 //               accumulators (128 columns each)
-//   warps 2..5  epilogue: TMEM -> registers -> C read-modify-write in global memory,
-//               overlapping the MMAs of the next tile in the other accumulator
+//   warps 2..5  epilogue: TMEM -> registers, combined with the C tile that the producer
+//               brought into shared memory by TMA, stored back by TMA; overlaps the MMAs
+//               of the next tile in the other accumulator
 // Every mbarrier wait is bounded (GPTQ_ERR_TIMEOUT into *status, then unwind).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -29,10 +30,11 @@ namespace gptq {
 
 namespace {
 
-constexpr int G_BM = 128, G_BN = 128, G_BK = 32, G_STAGES = 3, G_THREADS = 192;
+constexpr int G_BM = 128, G_BN = 128, G_BK = 32, G_STAGES = 2, G_THREADS = 192;
 constexpr int G_BOX = G_BM * G_BK * 4;         // 16 KB: one 128 x 32 fp32 box
 constexpr int G_STAGE = 4 * G_BOX;             // Ahi, Alo, Bhi, Blo
-constexpr int G_SMEM = G_STAGES * G_STAGE + 1024 + 256;
+constexpr int G_CBUF = 4 * G_BOX;              // the 128 x 128 C tile as four 32-column boxes
+constexpr int G_SMEM = G_STAGES * G_STAGE + G_CBUF + 1024 + 256;
 constexpr uint32_t G_TMEM_COLS = 2 * G_BN;
 
 // kind::tf32: D fp32 (bits 4-5 = 1), A/B TF32 (2), both K-major, N >> 3, M >> 4
@@ -42,10 +44,13 @@ constexpr uint32_t G_IDESC = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(G_
 struct GParams {
     int M, N, K;
     float alpha, beta;
-    float* C;
-    int64_t ldc;
     int tiles_m, tiles_n, ntiles, lower_only;
     int* status;
+    // optional TF32 split of the result: mode 1 hi[r][c], mode 2 (transposed) hi[c][r]
+    float* ohi;
+    float* olo;
+    int64_t old_;
+    int omode;
 };
 
 __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -56,6 +61,31 @@ __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint6
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// barrier over the 128 epilogue threads that also ANDs a predicate across them, so that
+// all epilogue warps take the same branch after a bounded wait
+__device__ __forceinline__ bool epi_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %1, 0;\n\t"
+        "barrier.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)(v ? 1 : 0))
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, int* status) {
@@ -87,24 +117,32 @@ __device__ __forceinline__ void tile_of(const GParams& p, int t, int& tm, int& t
     tn = t;
 }
 
+// The C tile moves through shared memory by TMA in both directions: the producer loads it
+// (when beta != 0) while the MMAs of the tile run, the epilogue combines it with the
+// accumulator in place and stores it back with TMA, so no thread waits on a global load.
 __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_constant__ CUtensorMap tAh,
                                                                   const __grid_constant__ CUtensorMap tAl,
                                                                   const __grid_constant__ CUtensorMap tBh,
                                                                   const __grid_constant__ CUtensorMap tBl,
+                                                                  const __grid_constant__ CUtensorMap tC,
                                                                   const GParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G_STAGES * G_STAGE);
+    uint8_t* cbuf = smem + G_STAGES * G_STAGE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(cbuf + G_CBUF);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t sbase = smem_u32(smem), bar0 = smem_u32(bars);
+    const uint32_t sbase = smem_u32(smem), cbase = smem_u32(cbuf), bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (G_STAGES + s); };
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * G_STAGES + b); };
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * G_STAGES + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * G_STAGES + 4);
+    const uint32_t cfull_bar = bar0 + 8u * (2 * G_STAGES + 4);
+    const uint32_t cempty_bar = bar0 + 8u * (2 * G_STAGES + 5);
+    const uint32_t drain_bar = bar0 + 8u * (2 * G_STAGES + 6);
+    const bool load_c = p.beta != 0.0f;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < G_STAGES; ++s) {
@@ -115,6 +153,8 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
             mbar_init(tfull_bar(b), 1);
             mbar_init(tempty_bar(b), 4);
         }
+        mbar_init(cfull_bar, 1);
+        mbar_init(cempty_bar, 1);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -124,6 +164,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
         tma_prefetch_desc(&tAl);
         tma_prefetch_desc(&tBh);
         tma_prefetch_desc(&tBl);
+        tma_prefetch_desc(&tC);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), G_TMEM_COLS);
@@ -136,9 +177,11 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
     const int ktiles = (p.K + G_BK - 1) / G_BK;
 
     if (warp == 0) {
+        // ------------------------------- TMA producer -------------------------------
         if (lane == 0) {
             int stage = 0;
-            uint32_t phase = 0, issued = 0, issued_par = 0;
+            uint32_t phase = 0, issued = 0, issued_par = 0, cph = 0;
+            bool c_issued = false;
             bool ok = true;
             for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
                 int tm, tn;
@@ -162,11 +205,23 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                         phase ^= 1u;
                     }
                 }
+                if (!ok) break;
+                if (load_c) {
+                    // the C buffer is free once the previous tile's stores have read it
+                    if (!mbar_wait(cempty_bar, cph ^ 1u, abort_flag, p.status)) break;
+                    mbar_expect_tx(cfull_bar, G_CBUF);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tma_load_2d(cbase + c * G_BOX, &tC, cfull_bar, tn * G_BN + 32 * c, tm * G_BM);
+                    c_issued = true;
+                    cph ^= 1u;
+                }
             }
             for (int s = 0; s < G_STAGES; ++s)
                 if (issued & (1u << s)) drain_wait(full_bar(s), (issued_par >> s) & 1u, p.status);
+            if (c_issued) drain_wait(cfull_bar, cph ^ 1u, p.status);
         }
     } else if (warp == 1) {
+        // ------------------------------- MMA issuer ---------------------------------
         if (lane == 0) {
             int stage = 0, abuf = 0;
             uint32_t phase = 0, aphase = 0;
@@ -211,48 +266,52 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
             drain_wait(drain_bar, 0, p.status);
         }
     } else {
+        // ------------------------------- epilogue (4 warps) -------------------------
         const int q = warp & 3;
+        const int rl = 32 * q + lane;            // row of the tile this thread owns
+        const bool storer = (threadIdx.x == 64);
         int abuf = 0;
-        uint32_t aphase = 0;
+        uint32_t aphase = 0, cph = 0;
         for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
             int tm, tn;
             tile_of(p, t, tm, tn);
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(abuf), aphase, abort_flag, p.status));
-            if (!ok) break;
+            bool ok = mbar_wait(tfull_bar(abuf), aphase, abort_flag, p.status);
+            if (ok && load_c) ok = mbar_wait(cfull_bar, cph, abort_flag, p.status);
+            if (!epi_all(ok)) break;
             tc_fence_after();
-            const int row = tm * G_BM + 32 * q + lane;
-            float* crow = p.C + (int64_t)(row < p.M ? row : 0) * p.ldc;
+            const int row = tm * G_BM + rl;
             const uint32_t ta = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(abuf * G_BN);
 #pragma unroll 1
-            for (int c = 0; c < G_BN / 32; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(ta + 32 * c, v);
                 tmem_ld_wait();
-                if (row < p.M) {
-                    const int gc0 = tn * G_BN + 32 * c;
+                uint8_t* brow = cbuf + c * G_BOX + rl * 128;
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const int gc = gc0 + i;
-                        if (gc + 3 < p.N) {
-                            float4* ptr = reinterpret_cast<float4*>(crow + gc);
-                            float4 o = make_float4(p.alpha * __uint_as_float(v[i]), p.alpha * __uint_as_float(v[i + 1]),
-                                                   p.alpha * __uint_as_float(v[i + 2]),
-                                                   p.alpha * __uint_as_float(v[i + 3]));
-                            if (p.beta != 0.0f) {
-                                const float4 cv = *ptr;
-                                o.x = fmaf(p.beta, cv.x, o.x);
-                                o.y = fmaf(p.beta, cv.y, o.y);
-                                o.z = fmaf(p.beta, cv.z, o.z);
-                                o.w = fmaf(p.beta, cv.w, o.w);
-                            }
-                            *ptr = o;
-                        } else {
+                for (int j = 0; j < 8; ++j) {
+                    float4* ptr = reinterpret_cast<float4*>(brow + ((j ^ (rl & 7)) << 4));
+                    float4 o = make_float4(p.alpha * __uint_as_float(v[4 * j]), p.alpha * __uint_as_float(v[4 * j + 1]),
+                                           p.alpha * __uint_as_float(v[4 * j + 2]),
+                                           p.alpha * __uint_as_float(v[4 * j + 3]));
+                    if (load_c) {
+                        const float4 cv = *ptr;
+                        o.x = fmaf(p.beta, cv.x, o.x);
+                        o.y = fmaf(p.beta, cv.y, o.y);
+                        o.z = fmaf(p.beta, cv.z, o.z);
+                        o.w = fmaf(p.beta, cv.w, o.w);
+                    }
+                    *ptr = o;
+                    if (p.omode && row < p.M) {
+                        const float o4[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                if (gc + e < p.N) {
-                                    const float o = p.alpha * __uint_as_float(v[i + e]);
-                                    crow[gc + e] = (p.beta != 0.0f) ? fmaf(p.beta, crow[gc + e], o) : o;
-                                }
+                        for (int e = 0; e < 4; ++e) {
+                            const int gc = tn * G_BN + 32 * c + 4 * j + e;
+                            if (gc < p.N) {
+                                const float h = __uint_as_float(__float_as_uint(o4[e]) & 0xFFFFE000u);
+                                const int64_t at = (p.omode == 1) ? (int64_t)row * p.old_ + gc
+                                                                  : (int64_t)gc * p.old_ + row;
+                                p.ohi[at] = h;
+                                p.olo[at] = o4[e] - h;
                             }
                         }
                     }
@@ -260,12 +319,24 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(abuf));
+            if (lane == 0) mbar_arrive(tempty_bar(abuf));   // the accumulator is free again
+            fence_proxy_async_smem();                        // make the tile visible to TMA
+            epi_barrier();
+            if (storer) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tma_store_2d(&tC, cbase + c * G_BOX, tn * G_BN + 32 * c, tm * G_BM);
+                bulk_commit();
+                bulk_wait_read0();
+                if (load_c) mbar_arrive(cempty_bar);
+            }
+            epi_barrier();                                   // the buffer may be written again
             if (++abuf == 2) {
                 abuf = 0;
                 aphase ^= 1u;
             }
+            if (load_c) cph ^= 1u;
         }
+        if (storer) bulk_wait0();
     }
 
     tc_fence_before();
@@ -329,7 +400,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return fn;
 }
 
-bool make_map(CUtensorMap* m, const float* base, int rows, int K, int ldk) {
+bool make_map(CUtensorMap* m, const float* base, int rows, int K, int64_t ldk) {
     auto enc = encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
@@ -365,11 +436,12 @@ bool tc_gemm_nt_ok(const float* C, int64_t ldc) {
 
 cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ahi, const float* Alo, const float* Bhi,
                        const float* Blo, int ldk, float beta, float* C, int64_t ldc, bool lower_only, int* status,
-                       cudaStream_t s) {
+                       cudaStream_t s, SplitOut out) {
     if (M <= 0 || N <= 0) return cudaSuccess;
-    CUtensorMap tah, tal, tbh, tbl;
-    if (!make_map(&tah, Ahi, M, K, ldk) || !make_map(&tal, Alo, M, K, ldk) || !make_map(&tbh, Bhi, N, K, ldk) ||
-        !make_map(&tbl, Blo, N, K, ldk))
+    if (out.ldb == 0) out.ldb = ldk;
+    CUtensorMap tah, tal, tbh, tbl, tcm;
+    if (!make_map(&tah, Ahi, M, K, ldk) || !make_map(&tal, Alo, M, K, ldk) || !make_map(&tbh, Bhi, N, K, out.ldb) ||
+        !make_map(&tbl, Blo, N, K, out.ldb) || !make_map(&tcm, C, M, N, ldc))
         return cudaErrorInvalidValue;
     GParams p;
     p.M = M;
@@ -377,8 +449,6 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
     p.K = K;
     p.alpha = alpha;
     p.beta = beta;
-    p.C = C;
-    p.ldc = ldc;
     p.tiles_m = (M + G_BM - 1) / G_BM;
     p.tiles_n = (N + G_BN - 1) / G_BN;
     p.lower_only = lower_only ? 1 : 0;
@@ -390,12 +460,16 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
         p.ntiles = p.tiles_m * p.tiles_n;
     }
     p.status = status;
+    p.ohi = out.hi;
+    p.olo = out.lo;
+    p.old_ = out.ld;
+    p.omode = out.hi ? out.mode : 0;
     if (p.ntiles == 0) return cudaSuccess;
     static const int sms = device_sm_count();
     const int grid = std::min(p.ntiles, sms);
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_nt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
     if (e != cudaSuccess) return e;
-    GPTQ_LAUNCH(id, s, tc_gemm_nt_kernel<<<grid, G_THREADS, G_SMEM, s>>>(tah, tal, tbh, tbl, p));
+    GPTQ_LAUNCH(id, s, tc_gemm_nt_kernel<<<grid, G_THREADS, G_SMEM, s>>>(tah, tal, tbh, tbl, tcm, p));
     return cudaGetLastError();
 }
 

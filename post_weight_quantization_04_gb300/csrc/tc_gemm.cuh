@@ -23,9 +23,19 @@ cudaError_t split_cols(int id, const float* B, int64_t ld, int K, int N, float* 
 // lower_only skips 128 x 128 C tiles entirely above the diagonal. C must not overlap the
 // operands. Returns false (nothing launched) if C's stride or alignment rules out the
 // vectorised epilogue; the caller then uses the FFMA path.
+// Extra options: ldb, the row stride of Bhi/Blo (0 = same as ldk, the stride of Ahi/Alo);
+// and an optional TF32 split of the result, written by the epilogue: mode 1 hi[r][c],
+// mode 2 (transposed) hi[c][r], with row stride ld.
+struct SplitOut {
+    float* hi = nullptr;
+    float* lo = nullptr;
+    int64_t ld = 0;
+    int mode = 0;
+    int64_t ldb = 0;
+};
 bool tc_gemm_nt_ok(const float* C, int64_t ldc);
 cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ahi, const float* Alo, const float* Bhi,
                        const float* Blo, int ldk, float beta, float* C, int64_t ldc, bool lower_only, int* status,
-                       cudaStream_t s);
+                       cudaStream_t s, SplitOut out = SplitOut());
 
 }  // namespace gptq
