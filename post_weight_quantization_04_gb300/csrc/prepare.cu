@@ -222,18 +222,30 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, 
     constexpr int LD = NB + 1;
     float* S = sm;              // NB x LD: the block, then L
     float* X = sm + NB * LD;    // NB x LD: L^-1
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x;
 
-    for (int idx = tid; idx < NB * NB; idx += 512) {
-        const int i = idx >> 7, j = idx & (NB - 1);
-        S[i * LD + j] = (i < n && j <= i) ? A[(k0 + i) * lda + k0 + j] : 0.0f;
-        X[i * LD + j] = 0.0f;
+    {
+        // all 32 loads of a thread in flight at once
+        float v[NB * NB / 512];
+#pragma unroll
+        for (int u = 0; u < NB * NB / 512; ++u) {
+            const int idx = tid + 512 * u;
+            const int i = idx >> 7, j = idx & (NB - 1);
+            v[u] = (i < n && j <= i) ? A[(k0 + i) * lda + k0 + j] : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < NB * NB / 512; ++u) {
+            const int idx = tid + 512 * u;
+            const int i = idx >> 7, j = idx & (NB - 1);
+            S[i * LD + j] = v[u];
+            X[i * LD + j] = 0.0f;
+        }
     }
     __syncthreads();
 
     for (int b = 0; b < n; b += 32) {
         const int nb = min(32, n - b);
-        if (warp == 0) chol_inv_32<LD>(S + b * LD + b, X + b * LD + b, nb, status);
+        if (tid < 32) chol_inv_32<LD>(S + b * LD + b, X + b * LD + b, nb, status);
         __syncthreads();
         const int rb = b + 32, m = n - rb;
         if (m <= 0) break;
@@ -291,47 +303,60 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, 
         __syncthreads();
     }
 
-    // off-diagonal blocks of L^-1, one 32-row block row at a time
-    for (int bi = 32; bi < n; bi += 32) {
-        const int ni = min(32, n - bi);
-        const int nj = bi / 32;  // blocks j = 0 .. nj-1 to fill in this block row
-        // T_j = sum_{k=j}^{i-1} L_ik X_kj, kept in registers, one element per thread per pass
-        float tv[6];
-        int cnt = 0;
-        for (int e = tid; e < nj * 1024; e += 512, ++cnt) {
-            const int jb = e >> 10, rr = (e >> 5) & 31, cc = e & 31;
-            const int row = bi + rr, col = jb * 32 + cc;
-            float acc = 0.0f;
-            if (rr < ni)
-                for (int k = col; k < bi; ++k) acc = fmaf(S[row * LD + k], X[k * LD + col], acc);
-            tv[cnt] = acc;
+    // Off-diagonal blocks of L^-1 by 2 x 2 block recursion, [[X11, 0], [X21, X22]] with
+    // X21 = -X22 (L21 X11): first inside each 64-row half (32-blocks), then for the whole
+    // 128 block (64-blocks). Products are 4 x 4 register tiles over shared memory; the
+    // intermediate T = L21 X11 is staged in the place X21 will occupy.
+    auto tile4 = [&](const float* Am, const float* Bm, int r0, int c0, int kb, int ke, float (&acc)[4][4]) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) acc[u][v] = 0.0f;
+#pragma unroll 4
+        for (int k = kb; k < ke; ++k) {
+            float ar[4], bc[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                ar[u] = Am[(r0 + u) * LD + k];
+                bc[u] = Bm[k * LD + c0 + u];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(ar[u], bc[v], acc[u][v]);
+        }
+    };
+    for (int h = 32; h <= 64; h *= 2) {               // block size of the level: 32, then 64
+        const int tiles = (h / 4) * (h / 4);         // 4 x 4 tiles of one h x h block
+        const int nblocks = NB / (2 * h);            // independent 2h x 2h diagonal blocks
+        const bool act = tid < tiles * nblocks;
+        const int blk = act ? tid / tiles : 0, tt = tid % tiles;
+        const int b = blk * 2 * h;                   // top-left of this 2h x 2h block
+        const int r0 = b + h + 4 * (tt / (h / 4)), c0 = b + 4 * (tt % (h / 4));
+        float acc[4][4];
+        // T = L21 X11: rows b+h.., cols b.., k over [b, b+h)
+        if (act) tile4(S, X, r0, c0, b, b + h, acc);
+        __syncthreads();
+        if (act) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) X[(r0 + u) * LD + c0 + v] = acc[u][v];
         }
         __syncthreads();
-        cnt = 0;
-        for (int e = tid; e < nj * 1024; e += 512, ++cnt) {
-            const int jb = e >> 10, rr = (e >> 5) & 31, cc = e & 31;
-            const int col = jb * 32 + cc;
-            if (rr < ni) X[(bi + rr) * LD + col] = tv[cnt];   // stage T in place
-        }
+        // X21 = -X22 T: k over [b+h, b+2h)
+        if (act) tile4(X, X, r0, c0, b + h, b + 2 * h, acc);
         __syncthreads();
-        cnt = 0;
-        for (int e = tid; e < nj * 1024; e += 512, ++cnt) {
-            const int jb = e >> 10, rr = (e >> 5) & 31, cc = e & 31;
-            const int col = jb * 32 + cc;
-            float acc = 0.0f;
-            if (rr < ni)
-                for (int k = 0; k <= rr; ++k) acc = fmaf(X[(bi + rr) * LD + bi + k], X[(bi + k) * LD + col], acc);
-            tv[cnt] = -acc;
-        }
-        __syncthreads();
-        cnt = 0;
-        for (int e = tid; e < nj * 1024; e += 512, ++cnt) {
-            const int jb = e >> 10, rr = (e >> 5) & 31, cc = e & 31;
-            if (rr < ni) X[(bi + rr) * LD + jb * 32 + cc] = tv[cnt];
+        if (act) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) X[(r0 + u) * LD + c0 + v] = -acc[u][v];
         }
         __syncthreads();
     }
 
+#pragma unroll 4
     for (int idx = tid; idx < NB * NB; idx += 512) {
         const int i = idx >> 7, j = idx & (NB - 1);
         if (i < n && j <= i) A[(k0 + i) * lda + k0 + j] = S[i * LD + j];
