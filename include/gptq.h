@@ -113,7 +113,7 @@ int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, float damp, i
  * memory (a host framework that owns all device memory through its own pool, or a path
  * that cannot take cudaMalloc's implicit synchronisation). No counterpart on the pages.
  * Same arguments, outputs, synchronisation and errors as gptq_prepare, minus ws/ws_bytes.
- * The scratch is a fixed array compiled into the library (about 10.5 MiB, held on every
+ * The scratch is a fixed array compiled into the library (about 14 MiB, held on every
  * GPU that loads the library until the process exits), so d is limited to 1024:
  * d > 1024 returns GPTQ_ERR_UNSUPPORTED. Allocates nothing (no cudaMalloc/cudaFree).
  * The first call on a device looks up that device's copy of the array

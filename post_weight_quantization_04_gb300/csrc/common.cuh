@@ -50,6 +50,34 @@ int device_sm_count();
 static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ------------------------------------------------------------------------------------
+// Programmatic dependent launch. A kernel launched with launch_pdl may start while the
+// kernel before it in the stream is still running; it must call pdl_wait() before it
+// touches any global memory that an earlier kernel writes or reads (everything before
+// that point is prologue: shared memory set-up, TMEM allocation, descriptor prefetch,
+// loads of data no earlier kernel of the call writes). pdl_trigger() lets the next
+// kernel begin its own prologue. In a kernel launched without the attribute both are
+// no-ops.
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
+// ------------------------------------------------------------------------------------
 // device-side status: kernels record failures into a device int (first error wins)
 // ------------------------------------------------------------------------------------
 __device__ __forceinline__ void set_status(int* status, int code) {

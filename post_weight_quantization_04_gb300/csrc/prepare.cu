@@ -18,10 +18,13 @@
 //   A     d*d fp32   reversed, equilibrated Hp -> L (lower triangle)
 //   Binv  d*d fp32   identity -> L^-1 (lower triangle)
 //   LinvD nblk*NB*NB fp32  inverses of L's diagonal blocks
+//   TF32 hi/lo splits of the GEMM operands (d x NB; the solved panel and L_kk^-1 twice,
+//   for even and odd panels, so the next panel can start while the last is still read)
 //   ddiag d fp32, rr d fp32 (1/sqrt(ddiag)), status int
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "sgemm.cuh"
@@ -41,11 +44,11 @@ struct PrepWs {
     float* alo;
     float* bhi;   //   the block row of the inverse (transposed),
     float* blo;
-    float* phi;   //   L21 (the solved panel),
+    float* phi;   //   L21 (the solved panel), two buffers (even / odd panels),
     float* plo;
     float* xhi;   //   the new block row of L^-1 (transposed),
     float* xlo;
-    float* lhi;   // NB x NB: L_kk^-1
+    float* lhi;   // NB x NB: L_kk^-1, two buffers (even / odd panels)
     float* llo;
     float* ddiag;
     float* rr;
@@ -60,8 +63,9 @@ constexpr int kPrepSlabs = 16;
 constexpr size_t prep_slab(int64_t d, int i) {
     return i < 2 ? sizeof(float) * d * d
          : i == 2 ? sizeof(float) * ((d + NB - 1) / NB) * NB * NB
+         : (i == 7 || i == 8) ? sizeof(float) * 2 * d * NB
          : i < 11 ? sizeof(float) * d * NB
-         : i < 13 ? sizeof(float) * NB * NB
+         : i < 13 ? sizeof(float) * 2 * NB * NB
          : i < 15 ? sizeof(float) * d
          : sizeof(int) * 4;
 }
@@ -165,45 +169,72 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
 }
 
 // Warp-level Cholesky + inverse of a (nb <= 32)-square block held in shared memory (row
-// stride LD): lane r keeps row r of the block and row r of X in registers; column k of L
-// and row k of X are broadcast with shuffles. On return the lower triangles hold L and
-// X = L^-1. One Gauss-Jordan step on [L | I] accompanies each Cholesky column step.
+// stride LD). Lane r keeps row r of the block in registers. Step k publishes column k of
+// the partly reduced block as row k of `lt` (32 x LT_LD floats, 16-byte aligned rows): the
+// pivot lt[k][k] and lt[k][i] = L[i][k] * L[k][k] for i > k, which every lane then reads
+// with broadcast vector loads. Afterwards lane c forms column c of X = L^-1 by forward
+// substitution over the same rows of lt. On return the lower triangles of Sb and Xb hold L
+// and L^-1.
+constexpr int LT_LD = 36;
 template <int LD>
-__device__ __forceinline__ void chol_inv_32(float* Sb, float* Xb, int nb, int* status) {
+__device__ __forceinline__ void chol_inv_32(float* Sb, float* Xb, int nb, float* lt, int* status) {
     const int r = threadIdx.x & 31;
-    float a[32], x[32];
+    float dinv[32];
+    {
+        float a[32];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-        a[c] = (r < nb && c <= r) ? Sb[r * LD + c] : 0.0f;
-        x[c] = (r < nb && c == r) ? 1.0f : 0.0f;
+        for (int c = 0; c < 32; ++c) a[c] = (r < nb && c <= r) ? Sb[r * LD + c] : 0.0f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            if (k >= nb) break;
+            lt[k * LT_LD + r] = a[k];
+            __syncwarp();
+            float piv = lt[k * LT_LD + k];
+            if (!(piv > 0.0f) || !isfinite(piv)) {
+                if (r == 0) set_status(status, GPTQ_ERR_NOT_SPD);
+                piv = 1.0f;
+            }
+            const float inv = rsqrtf(piv);  // 1 / L[k][k] (hardware approximation, ~2 ulp)
+            const float lkk = piv * inv;
+            dinv[k] = inv;
+            const float t = a[k] * (inv * inv);  // L[r][k] / L[k][k]
+#pragma unroll
+            for (int q = (k + 1) >> 2; q < 8; ++q) {
+                const float4 v = *reinterpret_cast<const float4*>(lt + k * LT_LD + 4 * q);
+                if (4 * q + 0 > k) a[4 * q + 0] = fmaf(-t, v.x, a[4 * q + 0]);
+                if (4 * q + 1 > k) a[4 * q + 1] = fmaf(-t, v.y, a[4 * q + 1]);
+                if (4 * q + 2 > k) a[4 * q + 2] = fmaf(-t, v.z, a[4 * q + 2]);
+                if (4 * q + 3 > k) a[4 * q + 3] = fmaf(-t, v.w, a[4 * q + 3]);
+            }
+            a[k] = (r == k) ? lkk : a[k] * inv;
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+            if (r < nb && c <= r) Sb[r * LD + c] = a[c];
     }
+    // column r of X: X[k][r] = acc[k] / L[k][k], then acc[i] -= L[i][k] X[k][r] for i > k
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = (i == r) ? 1.0f : 0.0f;
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
         if (k >= nb) break;
-        float piv = __shfl_sync(0xffffffffu, a[k], k);
-        if (!(piv > 0.0f) || !isfinite(piv)) {
-            if (r == 0) set_status(status, GPTQ_ERR_NOT_SPD);
-            piv = 1.0f;
-        }
-        const float lkk = sqrtf(piv);
-        const float inv = 1.0f / lkk;
-        const float l = a[k] * inv;  // L[r][k] (lanes r > k)
+        const float xk = acc[k] * dinv[k];
+        acc[k] = xk;
+        const float t = xk * dinv[k];
 #pragma unroll
-        for (int c = k + 1; c < 32; ++c) a[c] = fmaf(-l, __shfl_sync(0xffffffffu, l, c), a[c]);
-#pragma unroll
-        for (int c = 0; c <= k; ++c) {
-            const float xkc = __shfl_sync(0xffffffffu, x[c], k) * inv;  // X[k][c] / L[k][k]
-            x[c] = (r == k) ? xkc : (r > k ? fmaf(-l, xkc, x[c]) : x[c]);
-        }
-        a[k] = (r == k) ? lkk : l;
-    }
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-        if (r < nb && c <= r) {
-            Sb[r * LD + c] = a[c];
-            Xb[r * LD + c] = x[c];
+        for (int q = (k + 1) >> 2; q < 8; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(lt + k * LT_LD + 4 * q);
+            if (4 * q + 0 > k) acc[4 * q + 0] = fmaf(-t, v.x, acc[4 * q + 0]);
+            if (4 * q + 1 > k) acc[4 * q + 1] = fmaf(-t, v.y, acc[4 * q + 1]);
+            if (4 * q + 2 > k) acc[4 * q + 2] = fmaf(-t, v.z, acc[4 * q + 2]);
+            if (4 * q + 3 > k) acc[4 * q + 3] = fmaf(-t, v.w, acc[4 * q + 3]);
         }
     }
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (i < nb && r < nb && i >= r) Xb[i * LD + r] = acc[i];
+    __syncwarp();  // lt is reused by the next call
 }
 
 // One CTA factors the diagonal block A[k0:k0+n, k0:k0+n] = L L^T in place (lower), and
@@ -219,10 +250,13 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, 
                                                         float* __restrict__ Linv, float* __restrict__ Lhi,
                                                         float* __restrict__ Llo, int* __restrict__ status) {
     extern __shared__ float sm[];
+    __shared__ __align__(16) float lt[32 * LT_LD];
     constexpr int LD = NB + 1;
     float* S = sm;              // NB x LD: the block, then L
     float* X = sm + NB * LD;    // NB x LD: L^-1
     const int tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
 
     {
         // all 32 loads of a thread in flight at once
@@ -245,7 +279,7 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, 
 
     for (int b = 0; b < n; b += 32) {
         const int nb = min(32, n - b);
-        if (tid < 32) chol_inv_32<LD>(S + b * LD + b, X + b * LD + b, nb, status);
+        if (tid < 32) chol_inv_32<LD>(S + b * LD + b, X + b * LD + b, nb, lt, status);
         __syncthreads();
         const int rb = b + 32, m = n - rb;
         if (m <= 0) break;
@@ -397,13 +431,50 @@ extern "C" size_t gptq_prepare_workspace_bytes(int64_t d, int act_order) {
     return carve(nullptr, d).bytes;
 }
 
-extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, float damp, int act_order, float* U,
-                            int32_t* perm, uint8_t* dead, void* ws, size_t ws_bytes, void* stream_) {
+namespace gptq {
+namespace {
+
+// Streams and events for the two-stream factorisation, one set per device, created on
+// first use and kept for the life of the process. The mutex is held for the whole call, so
+// calls from several host threads on one device take the streams in turn.
+constexpr int kChainSMs = 32;
+constexpr int kMaxPrepDevices = 64;
+struct PrepConcurrency {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t crit = nullptr, side = nullptr;
+    cudaEvent_t fork = nullptr, trsm = nullptr, rest = nullptr, side_done[2] = {nullptr, nullptr},
+                join_side = nullptr, join_crit = nullptr;
+};
+PrepConcurrency g_conc[kMaxPrepDevices];
+
+cudaError_t conc_init(PrepConcurrency& c) {
+    if (c.ready) return cudaSuccess;
+    int least = 0, greatest = 0;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.crit, cudaStreamNonBlocking, greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.side, cudaStreamNonBlocking, least);
+    cudaEvent_t* evs[] = {&c.fork, &c.trsm, &c.rest, &c.side_done[0], &c.side_done[1], &c.join_side, &c.join_crit};
+    for (cudaEvent_t* ev : evs)
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) c.ready = true;
+    return e;
+}
+
+int check_args(const float* H, const float* diag_xtx, int64_t d, float damp, int act_order, const float* U,
+               const int32_t* perm, const uint8_t* dead, const void* ws, size_t ws_bytes) {
     if (d <= 0 || d > (1 << 20) || !H || !U || !perm || !dead || !ws) return GPTQ_ERR_INVALID_ARG;
     if (act_order && !diag_xtx) return GPTQ_ERR_INVALID_ARG;
     if (!(damp >= 0.0f) || !isfinite(damp)) return GPTQ_ERR_INVALID_ARG;
+    if (ws_bytes < carve(nullptr, d).bytes) return GPTQ_ERR_WORKSPACE;
+    return GPTQ_OK;
+}
+
+int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, int act_order, float* U,
+                 int32_t* perm, uint8_t* dead, void* ws, size_t ws_bytes, void* stream_, PrepConcurrency* conc) {
+    const int arg = check_args(H, diag_xtx, d, damp, act_order, U, perm, dead, ws, ws_bytes);
+    if (arg != GPTQ_OK) return arg;
     PrepWs w = carve(ws, d);
-    if (ws_bytes < w.bytes) return GPTQ_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream_);
 
     GPTQ_CUDA_TRY(cudaMemsetAsync(w.status, 0, sizeof(int), s));
@@ -434,42 +505,128 @@ extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, fl
     GPTQ_LAUNCH_CHECK();
     if (tc) {
         // Blocked right-looking Cholesky of A (lower) with the block-row inverse step of
-        // L^-1 interleaved: after panel k is factored, X[k,:] = L_kk^-1 B[k,:] and
-        // B[k+1:, :] -= L21 X[k, :] reuse the panel's TF32 splits.
+        // L^-1 interleaved, in two streams. The critical chain (stream `cs`) is
+        //   potrf(k) -> panel solve L21 = P L_kk^-T -> SYRK of the next panel's columns
+        //   -> potrf(k+1) ...
+        // while the side stream (`ss`) applies the rest of panel k's SYRK and the inverse
+        // step X_k = L_kk^-1 B_k, B[k+1:, :] -= L21 X_k, reading panel k's TF32 splits.
+        // The splits of L21 and L_kk^-1 alternate between two buffers by panel parity; the
+        // chain waits for the side stream to finish panel k-2 before it overwrites them.
+        // kChainSMs SMs are kept for the chain, the rest for the side stream.
+        const bool two = conc != nullptr;
+        cudaStream_t cs = two ? conc->crit : s, ss = two ? conc->side : s;
+        auto record = [&](cudaEvent_t e, cudaStream_t st) -> cudaError_t {
+            return two ? cudaEventRecord(e, st) : cudaSuccess;
+        };
+        auto wait = [&](cudaStream_t st, cudaEvent_t e) -> cudaError_t {
+            return two ? cudaStreamWaitEvent(st, e, 0) : cudaSuccess;
+        };
+        if (two) {
+            GPTQ_CUDA_TRY(record(conc->fork, s));
+            GPTQ_CUDA_TRY(wait(cs, conc->fork));
+            GPTQ_CUDA_TRY(wait(ss, conc->fork));
+        }
+        // the SMs are split between the streams: persistent CTAs of one stream would
+        // otherwise hold SMs that the other's next kernel waits for
+        GemmOpts side_opts, chain_opts;
+        side_opts.max_ctas = two ? std::max(1, device_sm_count() - kChainSMs) : 0;
+        chain_opts.max_ctas = two ? kChainSMs : 0;
+        // Programmatic dependent launch only where the previous item in the stream is one
+        // of these kernels (not an event wait): cs_k / ss_k say whether it is.
+        bool cs_k = !two, ss_k = false;
+        auto waited = [&](cudaStream_t st) {
+            if (st == cs) cs_k = false;
+            if (st == ss) ss_k = false;
+        };
         for (int64_t kb = 0; kb < nblk; ++kb) {
             const int64_t k0 = kb * NB;
             const int n = (int)std::min<int64_t>(NB, d - k0);
             const int64_t m = d - k0 - n, ncols = k0 + n;
+            const int nn = (int)std::min<int64_t>(NB, m);  // width of the next panel
+            const int par = (int)(kb & 1);
+            float* lhi = w.lhi + par * NB * NB;
+            float* llo = w.llo + par * NB * NB;
+            float* phi = w.phi + par * d * NB;
+            float* plo = w.plo + par * d * NB;
             float* LinvK = w.LinvD + kb * NB * NB;
-            GPTQ_LAUNCH(K_POTRF, s, potrf_diag_kernel<<<1, 512, potrf_smem, s>>>(w.A, d, k0, n, LinvK, w.lhi, w.llo,
-                                                                                 w.status));
+            if (two && kb >= 2) {
+                GPTQ_CUDA_TRY(wait(cs, conc->side_done[par]));
+                waited(cs);
+            }
+            if (cs_k) {
+                cudaError_t le = cudaSuccess;
+                GPTQ_LAUNCH(K_POTRF, cs, le = launch_pdl(potrf_diag_kernel, dim3(1), dim3(512), potrf_smem, cs, w.A,
+                                                         d, k0, n, LinvK, lhi, llo, w.status));
+                GPTQ_CUDA_TRY(le);
+            } else {
+                GPTQ_LAUNCH(K_POTRF, cs, potrf_diag_kernel<<<1, 512, potrf_smem, cs>>>(w.A, d, k0, n, LinvK, lhi, llo,
+                                                                                      w.status));
+            }
             GPTQ_LAUNCH_CHECK();
+            cs_k = true;
             float* P = w.A + (k0 + n) * d + k0;
             if (m > 0) {
-                SplitOut l21;  // L21 split for the trailing update and the inverse step
-                l21.hi = w.phi;
-                l21.lo = w.plo;
+                GemmOpts l21 = chain_opts;  // L21 split for the trailing update and the inverse step
+                l21.hi = phi;
+                l21.lo = plo;
                 l21.ld = NB;
                 l21.mode = 1;
-                GPTQ_CUDA_TRY(split_rows(K_SPLIT, P, d, (int)m, n, w.ahi, w.alo, NB, s));
-                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, n, n, 1.0f, w.ahi, w.alo, w.lhi, w.llo, NB, 0.0f, P, d,
-                                         false, w.status, s, l21));
-                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, (int)m, n, -1.0f, w.phi, w.plo, w.phi, w.plo, NB, 1.0f,
-                                         w.A + (k0 + n) * d + k0 + n, d, true, w.status, s));
+                l21.pdl = true;
+                GPTQ_CUDA_TRY(split_rows(K_SPLIT, P, d, (int)m, n, w.ahi, w.alo, NB, cs, true));
+                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, n, n, 1.0f, w.ahi, w.alo, lhi, llo, NB, 0.0f, P, d,
+                                         false, w.status, cs, l21));
+                GPTQ_CUDA_TRY(record(two ? conc->trsm : nullptr, cs));
+                // the next panel's columns; the side stream's SYRK of panel k-1 wrote them too
+                if (two && kb >= 1) {
+                    GPTQ_CUDA_TRY(wait(cs, conc->rest));
+                    waited(cs);
+                }
+                GemmOpts strip = chain_opts;
+                strip.pdl = cs_k;
+                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, nn, n, -1.0f, phi, plo, phi, plo, NB, 1.0f,
+                                         w.A + (k0 + n) * d + k0 + n, d, true, w.status, cs, strip));
+                cs_k = true;
+                GPTQ_CUDA_TRY(wait(ss, two ? conc->trsm : nullptr));
+                waited(ss);
+                if (m > nn) {
+                    const int64_t off = (int64_t)nn * NB;
+                    GemmOpts rest = side_opts;
+                    rest.pdl = ss_k;
+                    GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)(m - nn), (int)(m - nn), n, -1.0f, phi + off, plo + off,
+                                             phi + off, plo + off, NB, 1.0f, w.A + (k0 + n + nn) * (d + 1), d, true,
+                                             w.status, ss, rest));
+                    ss_k = true;
+                }
+                GPTQ_CUDA_TRY(record(two ? conc->rest : nullptr, ss));
+            } else {
+                GPTQ_CUDA_TRY(record(two ? conc->trsm : nullptr, cs));
+                GPTQ_CUDA_TRY(wait(ss, two ? conc->trsm : nullptr));
+                waited(ss);
             }
             float* Xi = w.Binv + k0 * d;
-            SplitOut xt;  // X[k, 0:ncols]^T split for the inverse's trailing update
+            GemmOpts xt = side_opts;  // X[k, 0:ncols]^T split for the inverse's trailing update
             xt.hi = w.xhi;
             xt.lo = w.xlo;
             xt.ld = NB;
             xt.mode = 2;
-            GPTQ_CUDA_TRY(split_cols(K_SPLIT, Xi, d, n, (int)ncols, w.bhi, w.blo, NB, s));
-            GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, n, (int)ncols, n, 1.0f, w.lhi, w.llo, w.bhi, w.blo, NB, 0.0f, Xi, d,
-                                     false, w.status, s, xt));
+            xt.pdl = true;
+            GPTQ_CUDA_TRY(split_cols(K_SPLIT, Xi, d, n, (int)ncols, w.bhi, w.blo, NB, ss, ss_k));
+            GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, n, (int)ncols, n, 1.0f, lhi, llo, w.bhi, w.blo, NB, 0.0f, Xi, d,
+                                     false, w.status, ss, xt));
+            ss_k = true;
             if (m > 0) {
-                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, (int)ncols, n, -1.0f, w.phi, w.plo, w.xhi, w.xlo, NB, 1.0f,
-                                         w.Binv + (k0 + n) * d, d, false, w.status, s));
+                GemmOpts upd = side_opts;
+                upd.pdl = true;
+                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, (int)ncols, n, -1.0f, phi, plo, w.xhi, w.xlo, NB, 1.0f,
+                                         w.Binv + (k0 + n) * d, d, false, w.status, ss, upd));
             }
+            GPTQ_CUDA_TRY(record(two ? conc->side_done[par] : nullptr, ss));
+        }
+        if (two) {
+            GPTQ_CUDA_TRY(record(conc->join_side, ss));
+            GPTQ_CUDA_TRY(record(conc->join_crit, cs));
+            GPTQ_CUDA_TRY(wait(s, conc->join_side));
+            GPTQ_CUDA_TRY(wait(s, conc->join_crit));
         }
     } else {
         // blocked right-looking Cholesky of A (lower), FFMA trailing products
@@ -514,6 +671,26 @@ extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, fl
     return hstatus;
 }
 
+}  // namespace
+}  // namespace gptq
+
+extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, float damp, int act_order, float* U,
+                            int32_t* perm, uint8_t* dead, void* ws, size_t ws_bytes, void* stream) {
+    const int arg = check_args(H, diag_xtx, d, damp, act_order, U, perm, dead, ws, ws_bytes);
+    if (arg != GPTQ_OK) return arg;
+    int dev = 0;
+    GPTQ_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxPrepDevices || d <= NB)
+        return prepare_impl(H, diag_xtx, d, damp, act_order, U, perm, dead, ws, ws_bytes, stream, nullptr);
+    PrepConcurrency& c = g_conc[dev];
+    std::lock_guard<std::mutex> lk(c.mu);
+    if (conc_init(c) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GPTQ_ERR_CUDA;
+    }
+    return prepare_impl(H, diag_xtx, d, damp, act_order, U, perm, dead, ws, ws_bytes, stream, &c);
+}
+
 // ------------------------------------------------------------------------------------
 // gptq_prepare_noalloc: gptq_prepare for callers that cannot allocate device memory.
 //
@@ -522,7 +699,7 @@ extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, fl
 // nothing extra, or a latency-sensitive path that cannot take cudaMalloc's implicit
 // device synchronisation. For them this entry point uses a fixed scratch area compiled
 // into the library as a file-scope __device__ array, sized for d <= kNoAllocMaxD.
-// Every GPU that loads the library holds this array (about 10.5 MiB) until the process
+// Every GPU that loads the library holds this array (about 14 MiB) until the process
 // exits. The entry point itself allocates nothing: no cudaMalloc, cudaFree or allocating
 // library routine.
 // ------------------------------------------------------------------------------------
@@ -574,5 +751,6 @@ extern "C" int gptq_prepare_noalloc(const float* H, const float* diag_xtx, int64
     }
     // every slab gptq_prepare reads is written by it first (its status word is cleared),
     // so the previous call's contents need no clearing here
-    return gptq_prepare(H, diag_xtx, d, damp, act_order, U, perm, dead, scratch, kNoAllocBytes, stream);
+    // one stream: no streams or events are created for this entry point
+    return prepare_impl(H, diag_xtx, d, damp, act_order, U, perm, dead, scratch, kNoAllocBytes, stream, nullptr);
 }

@@ -143,6 +143,10 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // One 128-column block of the loop. TPR threads share a row; thread `sub` owns the
 // 4-column chunks sub, sub+TPR, sub+2*TPR, ... of the block (CPT columns in registers),
 // so the TPR lanes of a row read one contiguous 16*TPR-byte span of U's row per step.
+// Besides its own chunks every lane keeps copies of the chunk being quantised (`cur`)
+// and of the next one (`nxt`), updated with the same operations as the owner's, so the
+// column-to-column dependency never goes through a shuffle: the next chunk is fetched
+// from its owner one chunk ahead.
 template <int TPR, bool SMALL_GROUPS>
 __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
     constexpr int CPT = QB / TPR;   // columns per thread
@@ -151,6 +155,7 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
     extern __shared__ __align__(16) float us[];  // QB x QB block of U, zeros below the diagonal
     __shared__ float invd[QB];
 
+    // prologue (U is not written by any kernel of this call): U[blk, blk], upper part only
     const int bw = a.bw;
     const bool full = (bw == QB) && ((a.cols & 3) == 0);
     if (full) {
@@ -158,13 +163,17 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
 #pragma unroll 8
         for (int v = threadIdx.x; v < QB * QB / 4; v += 128) {
             const int i = v >> 5, c4 = (v & 31) << 2;
-            cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(us + i * QB + c4)), src + i * a.cols + c4);
+            float* dst = us + i * QB + c4;
+            if (c4 + 3 < i)
+                *reinterpret_cast<float4*>(dst) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            else
+                cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(dst)), src + i * a.cols + c4);
         }
         cp_async_wait_all();
         __syncthreads();
-        // zero the block left of the diagonal: warp w takes rows w, w+4, ..., lanes the columns
-        for (int i = threadIdx.x >> 5; i < QB; i += 4)
-            for (int c = threadIdx.x & 31; c < i; c += 32) us[i * QB + c] = 0.0f;
+        // the chunk that straddles the diagonal: zero its part left of it
+        for (int i = threadIdx.x; i < QB; i += 128)
+            for (int c = i & ~3; c < i; ++c) us[i * QB + c] = 0.0f;
     } else {
 #pragma unroll 4
         for (int idx = threadIdx.x; idx < QB * QB; idx += blockDim.x) {
@@ -175,6 +184,8 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
     __syncthreads();
     invd[threadIdx.x] = (threadIdx.x < bw) ? 1.0f / us[threadIdx.x * QB + threadIdx.x] : 0.0f;
     __syncthreads();
+    pdl_wait();
+    pdl_trigger();
 
     const int sub = threadIdx.x % TPR;
     const int64_t row = (int64_t)blockIdx.x * RPC + threadIdx.x / TPR;
@@ -255,9 +266,19 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
     int next_gs = 0;  // next in-block group start (groups smaller than the block)
     const float flo = (float)lo, fhi = (float)hi;
 
-    // one column step: broadcast w_j, quantise, error, update this thread's columns
+    // copies of chunk 0 (owner: lane 0, registers 0..3)
+    float cur[4], nxt[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        cur[e] = __shfl_sync(0xffffffffu, w[e], 0, TPR);
+        nxt[e] = 0.0f;
+    }
+
+    // one column step (chunk cc = m*TPR + o, element e): quantise cur[e], error, update
+    // this thread's columns and both copies
     auto step = [&](int m, int o, int e, int jj) {
-        const float wj = __shfl_sync(0xffffffffu, w[4 * m + e], o, TPR);
+        const int cc = m * TPR + o;
+        const float wj = cur[e];
         const float cf = grid_code_f(wj, g, sym, flo, fhi);
         const float q = grid_dequant_f(cf, g, sym);
         const float err = (wj - q) * invd[jj];
@@ -268,6 +289,15 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
         }
         loss = fmaf(err, err, loss);
         const float* ur = us + jj * QB;
+        const float4 uc = *reinterpret_cast<const float4*>(ur + 4 * cc);
+        if (e < 1) cur[1] = fmaf(-err, uc.y, cur[1]);
+        if (e < 2) cur[2] = fmaf(-err, uc.z, cur[2]);
+        if (e < 3) cur[3] = fmaf(-err, uc.w, cur[3]);
+        const float4 un = *reinterpret_cast<const float4*>(ur + min(4 * cc + 4, QB - 4));
+        nxt[0] = fmaf(-err, un.x, nxt[0]);
+        nxt[1] = fmaf(-err, un.y, nxt[1]);
+        nxt[2] = fmaf(-err, un.z, nxt[2]);
+        nxt[3] = fmaf(-err, un.w, nxt[3]);
 #pragma unroll
         for (int mm = 0; mm < NCH; ++mm) {
             const float4 u4 = *reinterpret_cast<const float4*>(ur + col_of(mm, 0));
@@ -278,33 +308,32 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
         }
     };
 
-    if (SMALL_GROUPS) {
+    // the owner lane o stays a runtime loop: a fully unrolled block (128 steps) overflows
+    // the instruction cache
 #pragma unroll
-        for (int m = 0; m < NCH; ++m) {
-            for (int o = 0; o < TPR; ++o) {
+    for (int m = 0; m < NCH; ++m) {
+#pragma unroll 1
+        for (int o = 0; o < TPR; ++o) {
+            const int cc = m * TPR + o;
+            if (4 * cc >= bw) break;
+            // fetch the next chunk (m, o+1) or (m+1, 0) from its owner, current as of now
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int jj = (m * TPR + o) * 4 + e;
-                    if (jj >= bw) break;
-                    if (jj == next_gs) {
-                        next_gs += a.group;
-                        g = group_grid(jj, min(jj + a.group, bw));
-                    }
-                    step(m, o, e, jj);
-                }
+            for (int e = 0; e < 4; ++e) {
+                const float v = (o + 1 < TPR || m + 1 >= NCH) ? w[4 * m + e] : w[4 * (m + 1 < NCH ? m + 1 : m) + e];
+                nxt[e] = __shfl_sync(0xffffffffu, v, (o + 1) % TPR, TPR);
             }
-        }
-    } else {
 #pragma unroll
-        for (int m = 0; m < NCH; ++m) {
-#pragma unroll
-            for (int o = 0; o < TPR; ++o) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int jj = (m * TPR + o) * 4 + e;
-                    if (jj < bw) step(m, o, e, jj);
+            for (int e = 0; e < 4; ++e) {
+                const int jj = 4 * cc + e;
+                if (jj >= bw) break;
+                if (SMALL_GROUPS && jj == next_gs) {
+                    next_gs += a.group;
+                    g = group_grid(jj, min(jj + a.group, bw));
                 }
+                step(m, o, e, jj);
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) cur[e] = nxt[e];
         }
     }
     (void)next_gs;
@@ -499,13 +528,15 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
     const bool sym = q.sym != 0;
     const int64_t G = q.group ? ceil_div(cols, q.group) : 1;
 
+    // (the memsets first: every later item in the stream is one of this call's kernels, so
+    // the block and trailing kernels may be launched as programmatic dependents)
+    GPTQ_CUDA_TRY(cudaMemsetAsync(w.loss, 0, sizeof(float) * rows, s));
+    GPTQ_CUDA_TRY(cudaMemsetAsync(w.status, 0, sizeof(int), s));
     {
         dim3 grid((unsigned)std::min<int64_t>(ceil_div(cols, 256), 64), (unsigned)rows);
         GPTQ_LAUNCH(K_INIT_WORK, s, init_work_kernel<<<grid, 256, 0, s>>>(W, rows, cols, perm, dead, w.W));
         GPTQ_LAUNCH_CHECK();
     }
-    GPTQ_CUDA_TRY(cudaMemsetAsync(w.loss, 0, sizeof(float) * rows, s));
-    GPTQ_CUDA_TRY(cudaMemsetAsync(w.status, 0, sizeof(int), s));
     // tensor-core trailing update when every row of W and U is 16-byte aligned
     const bool tc = (cols % 4 == 0) && tc_gemm_nt_ok(w.W, cols);
     if (tc) GPTQ_CUDA_TRY(split_cols(K_SPLIT, U, cols, (int)cols, (int)cols, w.uhi, w.ulo, (int)cols, s));
@@ -569,14 +600,17 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         }
         a.j0 = j0;
         a.bw = bw;
-        GPTQ_LAUNCH(K_BLOCK, s, kblock<<<bgrid, 128, smem, s>>>(a));
+        cudaError_t le = cudaSuccess;
+        GPTQ_LAUNCH(K_BLOCK, s, le = launch_pdl(kblock, dim3(bgrid), dim3(128), smem, s, a));
+        GPTQ_CUDA_TRY(le);
         GPTQ_LAUNCH_CHECK();
         const int64_t e = j0 + bw;
         if (e < cols) {
             if (tc) {
                 // W[:, e:] -= Err * U[blk, e:] = Err * (U^T[e:, blk])^T on the tensor cores
-                SplitOut o;
+                GemmOpts o;
                 o.ldb = cols;
+                o.pdl = true;
                 GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_TRAIL, (int)rows, (int)(cols - e), bw, -1.0f, w.ehi, w.elo,
                                          w.uhi + e * cols + j0, w.ulo + e * cols + j0, QB, 1.0f, w.W + e, cols, false,
                                          w.status, s, o));

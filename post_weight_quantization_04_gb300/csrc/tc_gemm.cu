@@ -175,6 +175,8 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int ktiles = (p.K + G_BK - 1) / G_BK;
+    pdl_wait();      // operands and C may be the previous kernel's output
+    pdl_trigger();
 
     if (warp == 0) {
         // ------------------------------- TMA producer -------------------------------
@@ -355,6 +357,8 @@ __device__ __forceinline__ void split1(float a, float& hi, float& lo) {
 
 __global__ void split_rows_kernel(const float* __restrict__ A, int64_t lda, int rows, int K, float* __restrict__ hi,
                                   float* __restrict__ lo, int ldk) {
+    pdl_wait();
+    pdl_trigger();
     const int r = blockIdx.y;
     for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < K; k += gridDim.x * blockDim.x) {
         float h, l;
@@ -364,10 +368,32 @@ __global__ void split_rows_kernel(const float* __restrict__ A, int64_t lda, int 
     }
 }
 
+// the same with one float4 per thread (K, lda, ldk multiples of 4, 16-byte aligned rows)
+__global__ void __launch_bounds__(256) split_rows4_kernel(const float* __restrict__ A, int64_t lda, int rows, int K,
+                                                         float* __restrict__ hi, float* __restrict__ lo, int ldk) {
+    pdl_wait();
+    pdl_trigger();
+    const int k4 = K >> 2;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)rows * k4) return;
+    const int64_t r = idx / k4;
+    const int k = (int)(idx - r * k4) * 4;
+    const float4 v = *reinterpret_cast<const float4*>(A + r * lda + k);
+    float4 h, l;
+    split1(v.x, h.x, l.x);
+    split1(v.y, h.y, l.y);
+    split1(v.z, h.z, l.z);
+    split1(v.w, h.w, l.w);
+    *reinterpret_cast<float4*>(hi + r * ldk + k) = h;
+    *reinterpret_cast<float4*>(lo + r * ldk + k) = l;
+}
+
 // B (K x N block, row stride ld) -> hi/lo (N x ldk), transposed through a 32 x 33 tile
 __global__ void __launch_bounds__(256) split_cols_kernel(const float* __restrict__ B, int64_t ld, int K, int N,
                                                         float* __restrict__ hi, float* __restrict__ lo, int ldk) {
     __shared__ float tile[32][33];
+    pdl_wait();
+    pdl_trigger();
     const int k0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     for (int r = ty; r < 32; r += 8) {
@@ -415,18 +441,38 @@ bool make_map(CUtensorMap* m, const float* base, int rows, int K, int64_t ldk) {
 }  // namespace
 
 cudaError_t split_rows(int id, const float* A, int64_t lda, int rows, int K, float* hi, float* lo, int ldk,
-                       cudaStream_t s) {
+                       cudaStream_t s, bool pdl) {
     if (rows <= 0 || K <= 0) return cudaSuccess;
     dim3 grid((unsigned)std::min((K + 255) / 256, 8), (unsigned)rows);
-    GPTQ_LAUNCH(id, s, split_rows_kernel<<<grid, 256, 0, s>>>(A, lda, rows, K, hi, lo, ldk));
+    const bool vec = (K % 4 == 0) && (lda % 4 == 0) && (ldk % 4 == 0) &&
+                     ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(hi) |
+                       reinterpret_cast<uintptr_t>(lo)) % 16 == 0);
+    cudaError_t e = cudaSuccess;
+    if (vec) {
+        const unsigned blocks = (unsigned)(((int64_t)rows * (K / 4) + 255) / 256);
+        if (pdl)
+            GPTQ_LAUNCH(id, s, e = launch_pdl(split_rows4_kernel, dim3(blocks), dim3(256), 0, s, A, lda, rows, K, hi, lo, ldk));
+        else
+            GPTQ_LAUNCH(id, s, split_rows4_kernel<<<blocks, 256, 0, s>>>(A, lda, rows, K, hi, lo, ldk));
+    } else if (pdl) {
+        GPTQ_LAUNCH(id, s, e = launch_pdl(split_rows_kernel, grid, dim3(256), 0, s, A, lda, rows, K, hi, lo, ldk));
+    } else {
+        GPTQ_LAUNCH(id, s, split_rows_kernel<<<grid, 256, 0, s>>>(A, lda, rows, K, hi, lo, ldk));
+    }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 cudaError_t split_cols(int id, const float* B, int64_t ld, int K, int N, float* hi, float* lo, int ldk,
-                       cudaStream_t s) {
+                       cudaStream_t s, bool pdl) {
     if (K <= 0 || N <= 0) return cudaSuccess;
     dim3 grid((unsigned)((N + 31) / 32), (unsigned)((K + 31) / 32));
-    GPTQ_LAUNCH(id, s, split_cols_kernel<<<grid, 256, 0, s>>>(B, ld, K, N, hi, lo, ldk));
+    cudaError_t e = cudaSuccess;
+    if (pdl)
+        GPTQ_LAUNCH(id, s, e = launch_pdl(split_cols_kernel, grid, dim3(256), 0, s, B, ld, K, N, hi, lo, ldk));
+    else
+        GPTQ_LAUNCH(id, s, split_cols_kernel<<<grid, 256, 0, s>>>(B, ld, K, N, hi, lo, ldk));
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -436,7 +482,7 @@ bool tc_gemm_nt_ok(const float* C, int64_t ldc) {
 
 cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ahi, const float* Alo, const float* Bhi,
                        const float* Blo, int ldk, float beta, float* C, int64_t ldc, bool lower_only, int* status,
-                       cudaStream_t s, SplitOut out) {
+                       cudaStream_t s, GemmOpts out) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     if (out.ldb == 0) out.ldb = ldk;
     CUtensorMap tah, tal, tbh, tbl, tcm;
@@ -466,10 +512,16 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
     p.omode = out.hi ? out.mode : 0;
     if (p.ntiles == 0) return cudaSuccess;
     static const int sms = device_sm_count();
-    const int grid = std::min(p.ntiles, sms);
+    const int grid = std::min(p.ntiles, out.max_ctas > 0 ? std::min(out.max_ctas, sms) : sms);
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_nt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
     if (e != cudaSuccess) return e;
-    GPTQ_LAUNCH(id, s, tc_gemm_nt_kernel<<<grid, G_THREADS, G_SMEM, s>>>(tah, tal, tbh, tbl, tcm, p));
+    if (out.pdl) {
+        GPTQ_LAUNCH(id, s, e = launch_pdl(tc_gemm_nt_kernel, dim3(grid), dim3(G_THREADS), (size_t)G_SMEM, s, tah, tal,
+                                          tbh, tbl, tcm, p));
+        if (e != cudaSuccess) return e;
+    } else {
+        GPTQ_LAUNCH(id, s, tc_gemm_nt_kernel<<<grid, G_THREADS, G_SMEM, s>>>(tah, tal, tbh, tbl, tcm, p));
+    }
     return cudaGetLastError();
 }
 
