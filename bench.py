@@ -34,7 +34,7 @@ L2_BYTES = 129 * 1024 * 1024
 FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x 2 flop x max SM clock
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5)
@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-profile", action="store_true")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_info():
@@ -265,7 +265,6 @@ ROOF = {
 # kernel changed since its capture has no entry here.
 TRAFFIC = {
     (2, "hessian_tc_kernel"): 4.827069e9 + 159.446272e6,
-    (1, "potrf_diag_kernel"): 185.856e3,
     (2, "pack_kernel"): 16.788224e6,
 }
 
@@ -284,55 +283,61 @@ def peak_for(bound, pk):
 
 def oracle_pass(cfg: int, layers_host):
     """One layer pass of the oracle (numpy fp64) over host copies of the inputs; returns
-    (ms for H + prepare, ms for the column loops + packing on the rows given)."""
+    (ms for H over the tokens given, ms for the dead fix + damping + inv + cholesky, ms for
+    the column loops + packing on the rows given)."""
     import numpy as np
     import oracle as O
-    t_hp = t_q = 0.0
-    for X, Ws, q in layers_host:
+    t_h = t_p = t_q = 0.0
+    for X, n_full, Ws, q in layers_host:
         t0 = time.perf_counter()
-        S = O.xtx(X)
-        H = O.hessian_from_sum(S, X.shape[0])
-        U, perm, dead = O.prepare(H, q.damp, q.act_order, np.diag(S))
+        S = O.xtx(X) * (n_full / X.shape[0])  # the sum over the sample, scaled to n tokens
+        H = O.hessian_from_sum(S, n_full)
         t1 = time.perf_counter()
+        U, perm, dead = O.prepare(H, q.damp, q.act_order, np.diag(S))
+        t2 = time.perf_counter()
         for W in Ws:
             O.gptq_quantize(W, U, perm, dead, q.bits, q.group, q.sym)
-        t2 = time.perf_counter()
-        t_hp += (t1 - t0) * 1e3
-        t_q += (t2 - t1) * 1e3
-    return t_hp, t_q
+        t3 = time.perf_counter()
+        t_h += (t1 - t0) * 1e3
+        t_p += (t2 - t1) * 1e3
+        t_q += (t3 - t2) * 1e3
+    return t_h, t_p, t_q
 
 
-def host_layers(cfg: int, layers, row_frac: float = 1.0):
+def host_layers(cfg: int, layers, row_frac: float = 1.0, token_frac: float = 1.0):
     import synth
     out = []
     for L in layers:
-        X = synth.to_numpy_f64(L.X)
+        n = L.X.shape[0]
+        X = synth.to_numpy_f64(L.X[: max(1, int(round(n * token_frac)))])
         Ws = [synth.to_numpy_f64(W[: max(1, int(round(W.shape[0] * row_frac)))]) for W in L.Ws]
-        out.append((X, Ws, L.spec.q))
+        out.append((X, n, Ws, L.spec.q))
     return out
 
 
-def cpu_sample_desc(cfg, row_frac):
-    if row_frac >= 1.0:
+def cpu_sample_desc(cfg, row_frac, token_frac=1.0):
+    if row_frac >= 1.0 and token_frac >= 1.0:
         return (f"the whole workload-{cfg} layer pass in the oracle (numpy fp64: H, inv+cholesky, column loop, "
                 "packing) on the host cores")
-    return (f"workload-{cfg} in the oracle (numpy fp64): H and inv+cholesky in full, the column loop and packing "
-            f"on the first {row_frac:.4g} of each weight's rows (rows are independent given U), loop time scaled "
-            f"by {1 / row_frac:.4g}")
+    return (f"workload-{cfg} in the oracle (numpy fp64): H on the first {token_frac:.4g} of the tokens (time scaled "
+            f"by {1 / token_frac:.4g}), inv+cholesky in full, the column loop and packing on the first "
+            f"{row_frac:.4g} of each weight's rows (rows are independent given U; time scaled by {1 / row_frac:.4g})")
 
 
-def time_oracle(cfg, layers, row_frac, reps=1):
-    hl = host_layers(cfg, layers, row_frac)
+def time_oracle(cfg, layers, row_frac, reps=1, token_frac=1.0):
+    hl = host_layers(cfg, layers, row_frac, token_frac)
     ts = []
     for _ in range(reps):
-        t_hp, t_q = oracle_pass(cfg, hl)
-        ts.append(t_hp + t_q / row_frac)
+        t_h, t_p, t_q = oracle_pass(cfg, hl)
+        ts.append(t_h / token_frac + t_p + t_q / row_frac)
     return ts
 
 
 # oracle row fraction per workload: bounded CPU samples (roughly 3-30 s each on 8-16 cores)
 ORACLE_ROW_FRAC = {0: 1.0, 1: 0.125, 2: 1.0 / 256, 3: 1.0 / 1024, 4: 1.0 / 1024}
 CPU_BASELINE_ROW_FRAC = {0: 1.0, 1: 1.0, 2: 1.0 / 64, 3: 1.0 / 512, 4: 1.0 / 512}
+# token fraction for the oracle's H (X^T X is linear in the tokens)
+TOKEN_FRAC = {0: 1.0, 1: 1.0, 2: 1.0 / 16, 3: 1.0 / 64, 4: 1.0 / 64}
 
 
 # ------------------------------------------------------------------------------ arms
@@ -344,17 +349,35 @@ def run_reference(args, ws, rank):
     cores = len(os.sched_getaffinity(0))
     wl, layers = build_layers(args.config, "cpu")
     frac = ORACLE_ROW_FRAC[args.config]
-    time_oracle(args.config, layers, frac, reps=min(args.warmup, 1))
-    v = statistics.mean(time_oracle(args.config, layers, frac, reps=args.steps))
+    tf = TOKEN_FRAC[args.config]
+    time_oracle(args.config, layers, frac, reps=min(args.warmup, 1), token_frac=tf)
+    v = statistics.mean(time_oracle(args.config, layers, frac, reps=args.steps, token_frac=tf))
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "ms", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": v, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic", "config": {"workload": wl.name, "config_index": args.config},
         "cpu_baseline": {"value": v, "unit": "ms", "cores": cores, "kind": "oracle",
-                         "sample": cpu_sample_desc(args.config, frac)},
+                         "sample": cpu_sample_desc(args.config, frac, tf)},
         "e2e": {"value": v, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def max_over_ranks(ms: float, ws: int, device) -> float:
+    """The slowest rank's step time (every rank gets it)."""
+    if ws <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(ms_max: float, ws: int) -> float:
+    """ws independent replicas each finish one layer pass within ms_max: the job's time per
+    layer pass (weak scaling; lower is better)."""
+    return ms_max / max(1, ws)
 
 
 def run_ours(args, ws, rank, local):
@@ -406,11 +429,7 @@ def run_ours(args, ws, rank, local):
     wall = (time.perf_counter() - t_wall0) * 1e3
     launches = lib.gptq_launch_count() - n0
     ck = clocks.stop()
-    ms = statistics.mean(times)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(times), ws, dev)
 
     # ---- profiled pass: per-stage and per-kernel CUDA events over the same steps ----
     stages, kernels, roof = {}, {}, None
@@ -490,12 +509,13 @@ def run_ours(args, ws, rank, local):
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and ws == 1:
         frac = CPU_BASELINE_ROW_FRAC[args.config]
-        t = time_oracle(args.config, layers, frac, reps=1)
+        tf = TOKEN_FRAC[args.config]
+        t = time_oracle(args.config, layers, frac, reps=1, token_frac=tf)
         cpu = {"value": statistics.mean(t), "unit": "ms", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-               "sample": cpu_sample_desc(args.config, frac)}
+               "sample": cpu_sample_desc(args.config, frac, tf)}
 
     if rank == 0:
-        value = ms / ws   # weak scaling over independent layer replicas: ms per layer pass
+        value = replica_value(ms, ws)
         line = {
             "metric": METRIC, "value": value, "unit": "ms", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",

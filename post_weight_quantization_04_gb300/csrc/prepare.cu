@@ -168,22 +168,23 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
     A[i * d + j] = v;
 }
 
-// Warp-level Cholesky + inverse of a (nb <= 32)-square block held in shared memory (row
-// stride LD). Lane r keeps row r of the block in registers. Step k publishes column k of
-// the partly reduced block as row k of `lt` (32 x LT_LD floats, 16-byte aligned rows): the
-// pivot lt[k][k] and lt[k][i] = L[i][k] * L[k][k] for i > k, which every lane then reads
-// with broadcast vector loads. Afterwards lane c forms column c of X = L^-1 by forward
-// substitution over the same rows of lt. On return the lower triangles of Sb and Xb hold L
-// and L^-1.
+// Warp-level Cholesky + inverse of a (nb <= 32)-square block held in shared memory. Lane
+// r keeps row r of the block (row stride LDS_) in registers. Step k publishes column k of
+// the partly reduced block as row k of `lt` (32 x LT_LD floats, 16-byte aligned rows):
+// the pivot lt[k][k] and lt[k][i] = L[i][k] * L[k][k] for i > k, which every lane then
+// reads with broadcast vector loads. Afterwards lane c forms column c of X = L^-1 by
+// forward substitution over the same rows of lt. On return the lower triangles of Sb and
+// Xb (row stride LDX_) hold L and L^-1, and XT (32 x LT_LD) holds X transposed (zeros
+// above its diagonal and outside nb).
 constexpr int LT_LD = 36;
-template <int LD>
-__device__ __forceinline__ void chol_inv_32(float* Sb, float* Xb, int nb, float* lt, int* status) {
+template <int LDS_, int LDX_>
+__device__ __forceinline__ void chol_inv_32(float* Sb, float* Xb, float* XT, int nb, float* lt, int* status) {
     const int r = threadIdx.x & 31;
     float dinv[32];
     {
         float a[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) a[c] = (r < nb && c <= r) ? Sb[r * LD + c] : 0.0f;
+        for (int c = 0; c < 32; ++c) a[c] = (r < nb && c <= r) ? Sb[r * LDS_ + c] : 0.0f;
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
             if (k >= nb) break;
@@ -210,7 +211,7 @@ __device__ __forceinline__ void chol_inv_32(float* Sb, float* Xb, int nb, float*
         }
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-            if (r < nb && c <= r) Sb[r * LD + c] = a[c];
+            if (r < nb && c <= r) Sb[r * LDS_ + c] = a[c];
     }
     // column r of X: X[k][r] = acc[k] / L[k][k], then acc[i] -= L[i][k] X[k][r] for i > k
     float acc[32];
@@ -232,28 +233,55 @@ __device__ __forceinline__ void chol_inv_32(float* Sb, float* Xb, int nb, float*
         }
     }
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-        if (i < nb && r < nb && i >= r) Xb[i * LD + r] = acc[i];
+    for (int i = 0; i < 32; ++i) {
+        const bool in = i < nb && r < nb && i >= r;
+        if (!in) acc[i] = 0.0f;
+        if (in) Xb[i * LDX_ + r] = acc[i];
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4*>(XT + r * LT_LD + 4 * q) = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2],
+                                                                         acc[4 * q + 3]);
     __syncwarp();  // lt is reused by the next call
 }
 
-// One CTA factors the diagonal block A[k0:k0+n, k0:k0+n] = L L^T in place (lower), and
-// writes L^-1 (lower, NB x NB, zeros above) to Linv. A non-positive or non-finite pivot
-// records GPTQ_ERR_NOT_SPD (and is replaced by 1 so the kernel finishes).
+// (ti, tj) of the t-th 4 x 4 tile of a lower triangle, row by row
+__device__ __forceinline__ void tri_tile(int t, int& ti, int& tj) {
+    int i = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
+    while ((i + 1) * (i + 2) / 2 <= t) ++i;
+    while (i * (i + 1) / 2 > t) --i;
+    ti = i;
+    tj = t - i * (i + 1) / 2;
+}
+
+// One CTA factors the diagonal block A[k0:k0+n, k0:k0+n] = L L^T in place (lower) and
+// forms L^-1 (lower, NB x NB, zeros above): optionally written to Linv, and as its TF32
+// split to Lhi/Llo. A non-positive or non-finite pivot records GPTQ_ERR_NOT_SPD (and is
+// replaced by 1 so the kernel finishes).
 //
-// Blocked by 32 columns inside shared memory: for each 32-column panel, warp 0 factors
-// and inverts the 32 x 32 diagonal block (chol_inv_32), then all threads form the panel
-// below it (L21 = A21 * X11^T) and update the trailing block (A22 -= L21 L21^T). The
-// off-diagonal 32 x 32 blocks of L^-1 follow block row by block row:
-// X_ij = -X_ii * sum_{j<=k<i} L_ik X_kj.
+// Blocked by 32 columns inside shared memory. For each 32-column sub-panel b:
+//   1. warp 0: L_bb and X_bb = L_bb^-1 (chol_inv_32)
+//   2. the panel below it, L21 = A21 X_bb^T (kept also transposed in Lt), and the block
+//      row of the inverse left of the diagonal, X[b, :b] = X_bb B[b, :b]
+//   3. the trailing update A22 -= L21 L21^T and the inverse's right-looking update
+//      B[below, :b+32] -= L21 X[b, :b+32]
+// (B, the right-hand side of L X = I, lives in X's storage until it is overwritten.)
+// All products are 4 x 4 register tiles over shared memory, read with 16-byte loads.
+constexpr int POTRF_LDS = NB + 1;   // row stride of the block (odd: conflict-free columns)
+constexpr int POTRF_LDX = NB + 4;   // row stride of L^-1 and of Lt (16-byte rows)
+constexpr size_t potrf_smem_bytes() {
+    return sizeof(float) * ((size_t)NB * POTRF_LDS + (size_t)NB * POTRF_LDX + 32 * (size_t)POTRF_LDX + 2 * 32 * LT_LD);
+}
 __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, int64_t lda, int64_t k0, int n,
                                                         float* __restrict__ Linv, float* __restrict__ Lhi,
                                                         float* __restrict__ Llo, int* __restrict__ status) {
-    extern __shared__ float sm[];
-    __shared__ __align__(16) float lt[32 * LT_LD];
-    constexpr int LD = NB + 1;
-    float* S = sm;              // NB x LD: the block, then L
-    float* X = sm + NB * LD;    // NB x LD: L^-1
+    extern __shared__ __align__(16) float sm[];
+    constexpr int LD = POTRF_LDS, LDX = POTRF_LDX;
+    float* S = sm;                   // NB x LD: the block, then L
+    float* X = S + NB * LD;          // NB x LDX: B, then L^-1
+    float* Lt = X + NB * LDX;        // 32 x LDX: the current panel of L, transposed
+    float* XT = Lt + 32 * LDX;       // 32 x LT_LD: X_bb transposed
+    float* lt = XT + 32 * LT_LD;     // 32 x LT_LD: chol_inv_32 scratch
     const int tid = threadIdx.x;
     pdl_wait();
     pdl_trigger();
@@ -272,130 +300,163 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, 
             const int idx = tid + 512 * u;
             const int i = idx >> 7, j = idx & (NB - 1);
             S[i * LD + j] = v[u];
-            X[i * LD + j] = 0.0f;
         }
+        for (int idx = tid; idx < NB * LDX / 4; idx += 512)
+            reinterpret_cast<float4*>(X)[idx] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
     __syncthreads();
 
     for (int b = 0; b < n; b += 32) {
         const int nb = min(32, n - b);
-        if (tid < 32) chol_inv_32<LD>(S + b * LD + b, X + b * LD + b, nb, lt, status);
+        if (tid < 32) chol_inv_32<LD, LDX>(S + b * LD + b, X + b * LDX + b, XT, nb, lt, status);
         __syncthreads();
-        const int rb = b + 32, m = n - rb;
-        if (m <= 0) break;
-        // panel: S[r][b+c] = sum_{k<=c} S[r][b+k] * X[b+c][b+k], rows rb..n-1; 4 threads per row
+        const int rb = b + 32, m = max(0, n - rb);
+        const int tm = (m + 3) >> 2;       // 4-row tiles below the sub-panel
+        // ---- 2. panel L21 = A21 X_bb^T, and X[b, :b] = X_bb B[b, :b] ----
         {
-            const int r = rb + (tid >> 2), cq = (tid & 3) * 8;
-            float in[32], out[8];
-            if (r < n) {
+            const int P = tm * 8, Q = 8 * (b >> 2);
+            float acc[4][4];
+            int kind = -1, r0 = 0, c0 = 0;
+            const int t = tid;
+            if (t < P) {
+                kind = 0;
+                r0 = rb + 4 * (t >> 3);
+                c0 = 4 * (t & 7);
 #pragma unroll
-                for (int k = 0; k < 32; ++k) in[k] = S[r * LD + b + k];
+                for (int u = 0; u < 4; ++u)
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const float* xr = X + (b + cq + cc) * LD + b;
-                    float acc = 0.0f;
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) acc = fmaf(in[k], xr[k], acc);
-                    out[cc] = acc;
-                }
-            }
-            __syncthreads();
-            if (r < n) {
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) S[r * LD + b + cq + cc] = out[cc];
-            }
-        }
-        __syncthreads();
-        // trailing: S[r][c] -= sum_k L[r][b+k] L[c][b+k], rb <= c <= r < n, 4 x 4 tiles
-        {
-            const int tdim = (m + 3) >> 2;
-            for (int t = tid; t < tdim * tdim; t += 512) {
-                const int ti = t / tdim, tj = t % tdim;
-                if (tj > ti) continue;
-                const int r0 = rb + 4 * ti, c0 = rb + 4 * tj;
-                float acc[4][4] = {};
-#pragma unroll 8
+                    for (int v = 0; v < 4; ++v) acc[u][v] = 0.0f;
+#pragma unroll 4
                 for (int k = 0; k < 32; ++k) {
-                    float ar[4], bc[4];
+                    const float4 x4 = *reinterpret_cast<const float4*>(XT + k * LT_LD + c0);
+                    float ar[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) ar[u] = (r0 + u < n) ? S[(r0 + u) * LD + b + k] : 0.0f;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        ar[u] = (r0 + u < n) ? S[(r0 + u) * LD + b + k] : 0.0f;
-                        bc[u] = (c0 + u < n) ? S[(c0 + u) * LD + b + k] : 0.0f;
+                        acc[u][0] = fmaf(ar[u], x4.x, acc[u][0]);
+                        acc[u][1] = fmaf(ar[u], x4.y, acc[u][1]);
+                        acc[u][2] = fmaf(ar[u], x4.z, acc[u][2]);
+                        acc[u][3] = fmaf(ar[u], x4.w, acc[u][3]);
+                    }
+                }
+            } else if (t < P + Q) {
+                kind = 1;
+                const int q = t - P;
+                r0 = b + 4 * (q & 7);
+                c0 = 4 * (q >> 3);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) acc[u][v] = 0.0f;
+#pragma unroll 4
+                for (int k = 0; k < 32; ++k) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(XT + k * LT_LD + (r0 - b));
+                    const float4 b4 = *reinterpret_cast<const float4*>(X + (b + k) * LDX + c0);
+                    const float ar[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        acc[u][0] = fmaf(ar[u], b4.x, acc[u][0]);
+                        acc[u][1] = fmaf(ar[u], b4.y, acc[u][1]);
+                        acc[u][2] = fmaf(ar[u], b4.z, acc[u][2]);
+                        acc[u][3] = fmaf(ar[u], b4.w, acc[u][3]);
+                    }
+                }
+            }
+            __syncthreads();  // X[b, :b] is read above before it is overwritten below
+            if (kind == 0) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (r0 + u < n) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) S[(r0 + u) * LD + b + c0 + v] = acc[u][v];
+                    }
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    *reinterpret_cast<float4*>(Lt + (c0 + v) * LDX + r0) =
+                        make_float4(acc[0][v], r0 + 1 < n ? acc[1][v] : 0.0f, r0 + 2 < n ? acc[2][v] : 0.0f,
+                                    r0 + 3 < n ? acc[3][v] : 0.0f);
+            } else if (kind == 1) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (r0 + u < n)
+                        *reinterpret_cast<float4*>(X + (r0 + u) * LDX + c0) =
+                            make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+            }
+        }
+        if (m <= 0) break;
+        __syncthreads();
+        // ---- 3. A22 -= L21 L21^T (lower tiles) and B[below, :b+32] -= L21 X[b, :b+32] ----
+        {
+            const int Ts = tm * (tm + 1) / 2, Tb = tm * ((b + 32) >> 2);
+            for (int t = tid; t < Ts + Tb; t += 512) {
+                float acc[4][4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) acc[u][v] = 0.0f;
+                if (t < Ts) {
+                    int ti, tj;
+                    tri_tile(t, ti, tj);
+                    const int r0 = rb + 4 * ti, c0 = rb + 4 * tj;
+#pragma unroll 4
+                    for (int k = 0; k < 32; ++k) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(Lt + k * LDX + r0);
+                        const float4 b4 = *reinterpret_cast<const float4*>(Lt + k * LDX + c0);
+                        const float ar[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            acc[u][0] = fmaf(ar[u], b4.x, acc[u][0]);
+                            acc[u][1] = fmaf(ar[u], b4.y, acc[u][1]);
+                            acc[u][2] = fmaf(ar[u], b4.z, acc[u][2]);
+                            acc[u][3] = fmaf(ar[u], b4.w, acc[u][3]);
+                        }
                     }
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(ar[u], bc[v], acc[u][v]);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        if (r0 + u < n && c0 + v <= r0 + u) S[(r0 + u) * LD + c0 + v] -= acc[u][v];
-            }
-        }
-        __syncthreads();
-    }
-
-    // Off-diagonal blocks of L^-1 by 2 x 2 block recursion, [[X11, 0], [X21, X22]] with
-    // X21 = -X22 (L21 X11): first inside each 64-row half (32-blocks), then for the whole
-    // 128 block (64-blocks). Products are 4 x 4 register tiles over shared memory; the
-    // intermediate T = L21 X11 is staged in the place X21 will occupy.
-    auto tile4 = [&](const float* Am, const float* Bm, int r0, int c0, int kb, int ke, float (&acc)[4][4]) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int v = 0; v < 4; ++v) acc[u][v] = 0.0f;
+                        for (int v = 0; v < 4; ++v)
+                            if (r0 + u < n && c0 + v <= r0 + u) S[(r0 + u) * LD + c0 + v] -= acc[u][v];
+                } else {
+                    const int q = t - Ts, nbt = (b + 32) >> 2;
+                    const int r0 = rb + 4 * (q / nbt), c0 = 4 * (q % nbt);
 #pragma unroll 4
-        for (int k = kb; k < ke; ++k) {
-            float ar[4], bc[4];
+                    for (int k = 0; k < 32; ++k) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(Lt + k * LDX + r0);
+                        const float4 b4 = *reinterpret_cast<const float4*>(X + (b + k) * LDX + c0);
+                        const float ar[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                ar[u] = Am[(r0 + u) * LD + k];
-                bc[u] = Bm[k * LD + c0 + u];
+                        for (int u = 0; u < 4; ++u) {
+                            acc[u][0] = fmaf(ar[u], b4.x, acc[u][0]);
+                            acc[u][1] = fmaf(ar[u], b4.y, acc[u][1]);
+                            acc[u][2] = fmaf(ar[u], b4.z, acc[u][2]);
+                            acc[u][3] = fmaf(ar[u], b4.w, acc[u][3]);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (r0 + u < n) {
+                            float4* xp = reinterpret_cast<float4*>(X + (r0 + u) * LDX + c0);
+                            float4 xv = *xp;
+                            xv.x -= acc[u][0];
+                            xv.y -= acc[u][1];
+                            xv.z -= acc[u][2];
+                            xv.w -= acc[u][3];
+                            *xp = xv;
+                        }
+                }
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(ar[u], bc[v], acc[u][v]);
-        }
-    };
-    for (int h = 32; h <= 64; h *= 2) {               // block size of the level: 32, then 64
-        const int tiles = (h / 4) * (h / 4);         // 4 x 4 tiles of one h x h block
-        const int nblocks = NB / (2 * h);            // independent 2h x 2h diagonal blocks
-        const bool act = tid < tiles * nblocks;
-        const int blk = act ? tid / tiles : 0, tt = tid % tiles;
-        const int b = blk * 2 * h;                   // top-left of this 2h x 2h block
-        const int r0 = b + h + 4 * (tt / (h / 4)), c0 = b + 4 * (tt % (h / 4));
-        float acc[4][4];
-        // T = L21 X11: rows b+h.., cols b.., k over [b, b+h)
-        if (act) tile4(S, X, r0, c0, b, b + h, acc);
-        __syncthreads();
-        if (act) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int v = 0; v < 4; ++v) X[(r0 + u) * LD + c0 + v] = acc[u][v];
-        }
-        __syncthreads();
-        // X21 = -X22 T: k over [b+h, b+2h)
-        if (act) tile4(X, X, r0, c0, b + h, b + 2 * h, acc);
-        __syncthreads();
-        if (act) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int v = 0; v < 4; ++v) X[(r0 + u) * LD + c0 + v] = -acc[u][v];
         }
         __syncthreads();
     }
+    __syncthreads();
 
 #pragma unroll 4
     for (int idx = tid; idx < NB * NB; idx += 512) {
         const int i = idx >> 7, j = idx & (NB - 1);
         if (i < n && j <= i) A[(k0 + i) * lda + k0 + j] = S[i * LD + j];
-        const float v = (i < n && j <= i) ? X[i * LD + j] : 0.0f;
-        Linv[idx] = v;
+        const float v = (i < n && j <= i) ? X[i * LDX + j] : 0.0f;
+        if (Linv) Linv[idx] = v;
         if (Lhi) {  // TF32 split for the tensor-core products that use L_kk^-1
             const float h = __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
             Lhi[idx] = h;
@@ -492,7 +553,7 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
         GPTQ_LAUNCH_CHECK();
     }
 
-    const size_t potrf_smem = sizeof(float) * 2 * NB * (NB + 1);
+    const size_t potrf_smem = potrf_smem_bytes();
     GPTQ_CUDA_TRY(cudaFuncSetAttribute(potrf_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)potrf_smem));
 
@@ -548,7 +609,6 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
             float* llo = w.llo + par * NB * NB;
             float* phi = w.phi + par * d * NB;
             float* plo = w.plo + par * d * NB;
-            float* LinvK = w.LinvD + kb * NB * NB;
             if (two && kb >= 2) {
                 GPTQ_CUDA_TRY(wait(cs, conc->side_done[par]));
                 waited(cs);
@@ -556,11 +616,11 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
             if (cs_k) {
                 cudaError_t le = cudaSuccess;
                 GPTQ_LAUNCH(K_POTRF, cs, le = launch_pdl(potrf_diag_kernel, dim3(1), dim3(512), potrf_smem, cs, w.A,
-                                                         d, k0, n, LinvK, lhi, llo, w.status));
+                                                         d, k0, n, (float*)nullptr, lhi, llo, w.status));
                 GPTQ_CUDA_TRY(le);
             } else {
-                GPTQ_LAUNCH(K_POTRF, cs, potrf_diag_kernel<<<1, 512, potrf_smem, cs>>>(w.A, d, k0, n, LinvK, lhi, llo,
-                                                                                      w.status));
+                GPTQ_LAUNCH(K_POTRF, cs, potrf_diag_kernel<<<1, 512, potrf_smem, cs>>>(w.A, d, k0, n, nullptr, lhi,
+                                                                                      llo, w.status));
             }
             GPTQ_LAUNCH_CHECK();
             cs_k = true;

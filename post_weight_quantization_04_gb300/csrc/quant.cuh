@@ -9,10 +9,12 @@
 // maxq), maxq = 2^bits - 1, dequantised s * (code - z).
 //
 // Rounding is half-to-even. Scales are stored as fp32 and the grid is the stored scale.
-// Every rounding decision equals the one taken in fp64 on the same fp32 inputs: the fast
-// fp32 estimate is used only when it is at least 1e-3 away from a half-integer (its error
-// is below 1e-4 for |w / s| < 1000, and beyond that the clamp decides); otherwise the
-// quotient is recomputed in fp64 with IEEE division.
+// Every rounding decision is the exact one for the fp32 inputs (the one fp64 takes: the
+// quotient of two fp32 numbers is never within fp64 rounding of a half-point unless it
+// is one). The fp32 estimate r = rint(w * (1/s) (+ z)) is off by at most one, and only
+// next to a half-point; it is corrected by the signs of w - (r - z +- 1/2) s, each
+// formed by one fma (exact product, a single rounding, so the sign is exact), with ties
+// going to the even code. No branch, no fp64.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -40,31 +42,29 @@ __device__ __forceinline__ Grid asym_grid(float mn, float mx, int maxq) {
     return Grid{s, 1.0f / s, (float)z};
 }
 
-// round(w / s (+ z)) with the quotient taken in fp64 (IEEE division); kept out of line so
-// the rare near-half-point case does not weigh on the common path
-__device__ __noinline__ float quotient_rint_f64(float w, float s, float z, int sym) {
-    double td = (double)w / (double)s;
-    if (!sym) td += (double)z;
-    return (float)rint(td);
+// round-half-even of w / s (+ z), exact, as an integer-valued float
+__device__ __forceinline__ float grid_round(float w, const Grid& g, bool sym) {
+    const float t = sym ? w * g.inv_s : fmaf(w, g.inv_s, g.z);
+    const float r = rintf(t);
+    const float m = sym ? r : r - g.z;              // the multiple of s that r stands for
+    const float dh = fmaf(-(m + 0.5f), g.s, w);     // > 0: w / s lies above m + 1/2
+    const float dl = fmaf(-(m - 0.5f), g.s, w);     // < 0: w / s lies below m - 1/2
+    const float half = r * 0.5f;
+    const bool odd = rintf(half) != half;
+    const float up = (dh > 0.0f || (dh == 0.0f && odd)) ? 1.0f : 0.0f;
+    const float dn = (dl < 0.0f || (dl == 0.0f && odd)) ? 1.0f : 0.0f;
+    return r + up - dn;
 }
 
 // Integer code of w on the grid, clamped to [lo, hi].
 __device__ __forceinline__ int grid_code(float w, const Grid& g, bool sym, int lo, int hi) {
-    const float t = sym ? w * g.inv_s : fmaf(w, g.inv_s, g.z);
-    float r = rintf(t);
-    if (fabsf(t - floorf(t) - 0.5f) < 1e-3f) r = quotient_rint_f64(w, g.s, g.z, sym ? 1 : 0);
-    r = fminf(fmaxf(r, (float)lo), (float)hi);
-    return (int)r;
+    return (int)fminf(fmaxf(grid_round(w, g, sym), (float)lo), (float)hi);
 }
 
 // The same decision as grid_code, returned as an integer-valued float (no float<->int
-// conversions on the caller's dependency chain). |t - rint(t)| > 0.499 is the same
-// 1e-3-wide band around the half-points as grid_code's test.
+// conversions on the caller's dependency chain).
 __device__ __forceinline__ float grid_code_f(float w, const Grid& g, bool sym, float lo, float hi) {
-    const float t = sym ? w * g.inv_s : fmaf(w, g.inv_s, g.z);
-    float r = rintf(t);
-    if (fabsf(t - r) > 0.499f) r = quotient_rint_f64(w, g.s, g.z, sym ? 1 : 0);
-    return fminf(fmaxf(r, lo), hi);
+    return fminf(fmaxf(grid_round(w, g, sym), lo), hi);
 }
 
 __device__ __forceinline__ float grid_dequant_f(float code, const Grid& g, bool sym) {

@@ -278,29 +278,34 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
     // this thread's columns and both copies
     auto step = [&](int m, int o, int e, int jj) {
         const int cc = m * TPR + o;
+        // shared-memory operands first, off the dependency chain
+        const float* ur = us + jj * QB;
+        const float id = invd[jj];
+        const float4 uc = *reinterpret_cast<const float4*>(ur + 4 * cc);
+        const float4 un = *reinterpret_cast<const float4*>(ur + min(4 * cc + 4, QB - 4));
+        float4 uo[NCH];
+#pragma unroll
+        for (int mm = 0; mm < NCH; ++mm) uo[mm] = *reinterpret_cast<const float4*>(ur + col_of(mm, 0));
         const float wj = cur[e];
         const float cf = grid_code_f(wj, g, sym, flo, fhi);
         const float q = grid_dequant_f(cf, g, sym);
-        const float err = (wj - q) * invd[jj];
+        const float err = (wj - q) * id;
         if (sub == o) {
             cr[4 * m + e] = (int8_t)(int)cf;
             qr[4 * m + e] = q;
             er[4 * m + e] = err;
         }
         loss = fmaf(err, err, loss);
-        const float* ur = us + jj * QB;
-        const float4 uc = *reinterpret_cast<const float4*>(ur + 4 * cc);
         if (e < 1) cur[1] = fmaf(-err, uc.y, cur[1]);
         if (e < 2) cur[2] = fmaf(-err, uc.z, cur[2]);
         if (e < 3) cur[3] = fmaf(-err, uc.w, cur[3]);
-        const float4 un = *reinterpret_cast<const float4*>(ur + min(4 * cc + 4, QB - 4));
         nxt[0] = fmaf(-err, un.x, nxt[0]);
         nxt[1] = fmaf(-err, un.y, nxt[1]);
         nxt[2] = fmaf(-err, un.z, nxt[2]);
         nxt[3] = fmaf(-err, un.w, nxt[3]);
 #pragma unroll
         for (int mm = 0; mm < NCH; ++mm) {
-            const float4 u4 = *reinterpret_cast<const float4*>(ur + col_of(mm, 0));
+            const float4 u4 = uo[mm];
             w[4 * mm] = fmaf(-err, u4.x, w[4 * mm]);
             w[4 * mm + 1] = fmaf(-err, u4.y, w[4 * mm + 1]);
             w[4 * mm + 2] = fmaf(-err, u4.z, w[4 * mm + 2]);

@@ -179,6 +179,52 @@ def test_rtn_bit_exact(lib, rows, cols, bits, group, sym):
     np.testing.assert_array_equal(npy(out["packed"]).view(np.uint32), ref["packed"])
 
 
+def _tie_segment(rng, n, bits, sym):
+    """n fp32 weights whose grid (from their own min/max) puts many of them exactly on, or
+    one ulp either side of, a rounding half-point of w / s (+ z)."""
+    f = np.float32
+    if sym:
+        qm = 2 ** (bits - 1) - 1
+        mx = f(rng.uniform(0.05, 0.5))
+        s = f(np.float64(mx) / qm)
+        z = 0
+        lo_w, hi_w = -mx, mx
+        ks = np.arange(-qm, qm)
+    else:
+        qm = 2 ** bits - 1
+        mn, mx = f(-rng.uniform(0.05, 0.5)), f(rng.uniform(0.05, 0.5))
+        s = f((np.float64(mx) - np.float64(mn)) / qm)
+        z = int(min(max(np.rint(-np.float64(mn) / np.float64(s)), 0), qm))
+        lo_w, hi_w = mn, mx
+        ks = np.arange(0, qm)
+    vals = [hi_w, lo_w]
+    for k in ks:
+        t = f((k + 0.5 - z) * np.float64(s))
+        for v in (t, np.nextafter(t, f(np.inf)), np.nextafter(t, f(-np.inf))):
+            if lo_w <= v <= hi_w:
+                vals.append(f(v))
+    vals = np.array(vals, dtype=f)
+    out = rng.choice(vals[2:], n)
+    out[:2] = vals[:2]
+    return out
+
+
+@pytest.mark.parametrize("bits,group,sym", [(4, 0, True), (3, 0, False), (4, 32, False), (2, 64, True)])
+def test_rtn_exact_at_half_points(lib, bits, group, sym):
+    """Weights on and one ulp around the half-points of their own grid: the codes must be
+    the exact round-half-even decisions (bit-exact against the fp64 oracle)."""
+    rng = np.random.default_rng(bits * 10 + group)
+    rows, cols = 24, 128
+    step = group if group else cols
+    W = np.concatenate([np.stack([_tie_segment(rng, step, bits, sym) for _ in range(rows)])
+                        for _ in range(cols // step)], axis=1)
+    Wt = torch.tensor(W, device=DEV)
+    out = lib.rtn_quantize(Wt, bits, group, sym)
+    ref = O.rtn_quantize(W.astype(np.float64), bits, group, sym)
+    np.testing.assert_array_equal(npy(out["scales"]), f32(ref["scales"]))
+    np.testing.assert_array_equal(npy(out["codes"]).astype(np.int64), ref["codes"])
+
+
 @pytest.mark.parametrize("bits,sym,cols", [(2, True, 64), (3, True, 96), (3, False, 100), (4, False, 33)])
 def test_pack_bit_exact(lib, bits, sym, cols):
     rng = np.random.default_rng(bits * 100 + cols)
