@@ -115,9 +115,15 @@ class Clocks:
 # --------------------------------------------------------------------------- workload
 
 class Layer:
-    def __init__(self, spec, X, Ws, names):
+    """One layer input X and the weights that read it. The weights live stacked by rows in
+    one (sum of rows, cols) matrix `Wcat` (a fused projection); `Ws` are its row blocks.
+    GPTQ's rows are independent given U, so one gptq_quantize over Wcat equals one call per
+    weight, row for row."""
+
+    def __init__(self, spec, X, Wcat, Ws, names):
         self.spec = spec
         self.X = X
+        self.Wcat = Wcat
         self.Ws = Ws
         self.names = names
 
@@ -134,13 +140,21 @@ def build_layers(cfg: int, device, host: bool = False):
             seed = synth.x_seed(cfg, L.x) + (key[1] if cfg == 4 else 0)
             xcache[key] = synth.make_x(L.x, seed, device=device)
         X = xcache[key]
-        Ws = [synth.make_weight(w.out, w.inp, w.std, synth.weight_seed(cfg, w.name), device=device) for w in L.weights]
-        layers.append(Layer(L, X, Ws, [w.name for w in L.weights]))
+        cols = L.weights[0].inp
+        Wcat = torch.empty(sum(w.out for w in L.weights), cols, dtype=torch.float32, device=device)
+        Ws, r0 = [], 0
+        for w in L.weights:
+            Wcat[r0:r0 + w.out].copy_(synth.make_weight(w.out, w.inp, w.std, synth.weight_seed(cfg, w.name),
+                                                        device=device))
+            Ws.append(Wcat[r0:r0 + w.out])
+            r0 += w.out
+        layers.append(Layer(L, X, Wcat, Ws, [w.name for w in L.weights]))
     return wl, layers
 
 
 class Runner:
-    """Holds preallocated outputs/workspaces so a step only enqueues library calls."""
+    """Holds preallocated outputs/workspaces so a step only enqueues library calls: per
+    layer one Hessian pass, one gptq_prepare and one gptq_quantize over the stacked weights."""
 
     def __init__(self, lib, layers, device):
         import torch
@@ -151,6 +165,17 @@ class Runner:
         self.prep_ws = {}
         self.q_ws = {}
         self.outs = []
+        # layers that read the same X with the same damping and ordering share H, U, perm
+        # and dead: one Hessian pass and one gptq_prepare per group (the bit-width sweep of
+        # a decoder block re-quantises the same inputs)
+        self.groups = []
+        gkey = {}
+        for li, L in enumerate(layers):
+            key = (id(L.X), L.spec.q.damp, L.spec.q.act_order)
+            if key not in gkey:
+                gkey[key] = len(self.groups)
+                self.groups.append([])
+            self.groups[gkey[key]].append(li)
         for L in layers:
             d = L.X.shape[1]
             if d not in self.hess:
@@ -158,33 +183,41 @@ class Runner:
                 self.prep_ws[d] = torch.empty(lib.gptq_prepare_workspace_bytes(d, True), dtype=torch.uint8,
                                               device=device)
             q = L.spec.q
-            outs = []
-            for W in L.Ws:
-                r, c = W.shape
-                nb = lib.gptq_quantize_workspace_bytes(r, c, q.bits, q.group, q.sym)
-                if (r, c) not in self.q_ws or self.q_ws[(r, c)].numel() < nb:
-                    self.q_ws[(r, c)] = torch.empty(nb, dtype=torch.uint8, device=device)
-                G = -(-c // q.group) if q.group else 1
-                outs.append({
-                    "codes": torch.empty(r, c, dtype=torch.int8, device=device),
-                    "scales": torch.empty(r, G, dtype=torch.float32, device=device),
-                    "zeros": torch.empty(r, G, dtype=torch.uint8, device=device),
-                    "g_idx": torch.empty(c, dtype=torch.int32, device=device),
-                    "Wq": torch.empty(r, c, dtype=torch.float32, device=device),
-                    "packed": torch.empty(r, lib.gptq_packed_words_per_row(c, q.bits), dtype=torch.int32,
-                                          device=device),
-                    "row_loss": torch.empty(r, dtype=torch.float32, device=device),
-                })
-            self.outs.append(outs)
+            r, c = L.Wcat.shape
+            nb = lib.gptq_quantize_workspace_bytes(r, c, q.bits, q.group, q.sym)
+            if (r, c) not in self.q_ws or self.q_ws[(r, c)].numel() < nb:
+                self.q_ws[(r, c)] = torch.empty(nb, dtype=torch.uint8, device=device)
+            G = -(-c // q.group) if q.group else 1
+            self.outs.append({
+                "codes": torch.empty(r, c, dtype=torch.int8, device=device),
+                "scales": torch.empty(r, G, dtype=torch.float32, device=device),
+                "zeros": torch.empty(r, G, dtype=torch.uint8, device=device),
+                "g_idx": torch.empty(c, dtype=torch.int32, device=device),
+                "Wq": torch.empty(r, c, dtype=torch.float32, device=device),
+                "packed": torch.empty(r, lib.gptq_packed_words_per_row(c, q.bits), dtype=torch.int32,
+                                      device=device),
+                "row_loss": torch.empty(r, dtype=torch.float32, device=device),
+            })
 
-    def step(self, events=None, Xs=None, Wss=None):
-        """One layer pass over every layer; `events` collects (stage, start, end) CUDA events."""
+    def weight_outputs(self, li):
+        """The outputs of layer li split per weight (row blocks of the stacked outputs)."""
+        o, res, r0 = self.outs[li], [], 0
+        for W in self.layers[li].Ws:
+            r1 = r0 + W.shape[0]
+            res.append({k: (v if k == "g_idx" else v[r0:r1]) for k, v in o.items()})
+            r0 = r1
+        return res
+
+    def step(self, events=None, Xs=None, Wcats=None):
+        """One pass over every layer: per group one Hessian pass and one gptq_prepare, then
+        one gptq_quantize per layer; `events` collects (start, H done, U done, end) CUDA
+        events per group."""
         import torch
         lib = self.lib
-        for li, L in enumerate(self.layers):
-            X = L.X if Xs is None else Xs[li]
-            Ws = L.Ws if Wss is None else Wss[li]
-            q = L.spec.q
+        for g in self.groups:
+            L0 = self.layers[g[0]]
+            X = L0.X if Xs is None else Xs[g[0]]
+            q0 = L0.spec.q
             h = self.hess[X.shape[1]]
             e = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if events is not None else None
             if e:
@@ -194,11 +227,15 @@ class Runner:
             H, diag, _ = h.finalize()
             if e:
                 e[1].record()
-            U, perm, dead = lib.gptq_prepare(H, diag, q.damp, act_order=q.act_order, ws=self.prep_ws[X.shape[1]])
+            U, perm, dead = lib.gptq_prepare(H, diag, q0.damp, act_order=q0.act_order, ws=self.prep_ws[X.shape[1]])
             if e:
                 e[2].record()
-            for W, o in zip(Ws, self.outs[li]):
-                lib.gptq_quantize(W, U, perm, dead, q.bits, q.group, q.sym, ws=self.q_ws[tuple(W.shape)], out=o)
+            for li in g:
+                L = self.layers[li]
+                Wcat = L.Wcat if Wcats is None else Wcats[li]
+                q = L.spec.q
+                lib.gptq_quantize(Wcat, U, perm, dead, q.bits, q.group, q.sym, ws=self.q_ws[tuple(Wcat.shape)],
+                                  out=self.outs[li])
             if e:
                 e[3].record()
                 events.append(e)
@@ -218,13 +255,18 @@ def algorithmic(cfg_layers):
         work[k] = work.get(k, 0.0) + v
 
     NB, QB = 128, 128
+    seen = set()
     for L in cfg_layers:
         n, d = L.X.shape
-        add("hessian_tc_kernel", 2.0 * n * d * (d + 1) / 2)
+        key = (id(L.X), L.spec.q.damp, L.spec.q.act_order)
+        first = key not in seen    # H and U once per shared input (as Runner does)
+        seen.add(key)
+        if first:
+            add("hessian_tc_kernel", 2.0 * n * d * (d + 1) / 2)
         # prepare: per 128-wide panel, potrf (Cholesky n^3/3 + inverse n^3/6 FMA), the panel
         # solve 2 m n^2, the lower SYRK 2 m(m+1)/2 n, the inverse's scale 2 n k n and
         # trailing update 2 m k n (k = columns filled so far)
-        for k0 in range(0, d, NB):
+        for k0 in (range(0, d, NB) if first else ()):
             nb = min(NB, d - k0)
             m = d - k0 - nb
             ncols = k0 + nb
@@ -232,7 +274,7 @@ def algorithmic(cfg_layers):
             add("tc_gemm_nt_kernel[prepare]", 2.0 * m * nb * nb + 2.0 * (m * (m + 1) / 2) * nb
                 + 2.0 * nb * ncols * nb + 2.0 * m * ncols * nb)
             add("split_kernel", 12.0 * (m * nb + nb * ncols))
-        for W in L.Ws:
+        for W in (L.Wcat,):   # one gptq_quantize per layer over the stacked weights
             r, c = W.shape
             add("split_kernel", 12.0 * c * c)
             add("init_work_kernel", 8.0 * r * c)
@@ -288,12 +330,18 @@ def oracle_pass(cfg: int, layers_host):
     import numpy as np
     import oracle as O
     t_h = t_p = t_q = 0.0
+    cache = {}
     for X, n_full, Ws, q in layers_host:
+        key = (id(X), q.damp, q.act_order)   # shared inputs: H and U once, as on the GPU
         t0 = time.perf_counter()
-        S = O.xtx(X) * (n_full / X.shape[0])  # the sum over the sample, scaled to n tokens
-        H = O.hessian_from_sum(S, n_full)
-        t1 = time.perf_counter()
-        U, perm, dead = O.prepare(H, q.damp, q.act_order, np.diag(S))
+        if key not in cache:
+            S = O.xtx(X) * (n_full / X.shape[0])  # the sum over the sample, scaled to n tokens
+            H = O.hessian_from_sum(S, n_full)
+            t1 = time.perf_counter()
+            cache[key] = O.prepare(H, q.damp, q.act_order, np.diag(S))
+        else:
+            t1 = t0
+        U, perm, dead = cache[key]
         t2 = time.perf_counter()
         for W in Ws:
             O.gptq_quantize(W, U, perm, dead, q.bits, q.group, q.sym)
@@ -307,9 +355,12 @@ def oracle_pass(cfg: int, layers_host):
 def host_layers(cfg: int, layers, row_frac: float = 1.0, token_frac: float = 1.0):
     import synth
     out = []
+    xs = {}
     for L in layers:
         n = L.X.shape[0]
-        X = synth.to_numpy_f64(L.X[: max(1, int(round(n * token_frac)))])
+        if id(L.X) not in xs:   # one host copy per distinct input
+            xs[id(L.X)] = synth.to_numpy_f64(L.X[: max(1, int(round(n * token_frac)))])
+        X = xs[id(L.X)]
         Ws = [synth.to_numpy_f64(W[: max(1, int(round(W.shape[0] * row_frac)))]) for W in L.Ws]
         out.append((X, n, Ws, L.spec.q))
     return out
@@ -472,25 +523,30 @@ def run_ours(args, ws, rank, local):
     # ---- e2e: pinned host inputs -> device -> same pass -> quantised artefacts back ----
     e2e = None
     if not args.no_e2e:
-        hX = [L.X.to("cpu").pin_memory() for L in layers]
-        hW = [[W.to("cpu").pin_memory() for W in L.Ws] for L in layers]
-        dX = [torch.empty_like(L.X) for L in layers]
-        dW = [[torch.empty_like(W) for W in L.Ws] for L in layers]
-        h_out = [[{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in o.items()
-                   if k in ("packed", "scales", "zeros", "g_idx")} for o in outs] for outs in runner.outs]
-        bi = sum(x.numel() * x.element_size() for x in hX) + sum(w.numel() * 4 for ws_ in hW for w in ws_)
-        bo = sum(v.numel() * v.element_size() for outs in h_out for o in outs for v in o.values())
+        # one host copy and one device buffer per distinct X (shared inputs are copied once)
+        xs = {}
+        for L in layers:
+            if id(L.X) not in xs:
+                xs[id(L.X)] = (L.X.to("cpu").pin_memory(), torch.empty_like(L.X))
+        hX = [v[0] for v in xs.values()]
+        dXu = [v[1] for v in xs.values()]
+        dX = [xs[id(L.X)][1] for L in layers]
+        hW = [L.Wcat.to("cpu").pin_memory() for L in layers]
+        dW = [torch.empty_like(L.Wcat) for L in layers]
+        h_out = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in o.items()
+                  if k in ("packed", "scales", "zeros", "g_idx")} for o in runner.outs]
+        bi = sum(x.numel() * x.element_size() for x in hX) + sum(w.numel() * 4 for w in hW)
+        bo = sum(v.numel() * v.element_size() for o in h_out for v in o.values())
 
         def e2e_step():
+            for hx, dx in zip(hX, dXu):
+                dx.copy_(hx, non_blocking=True)
             for i in range(len(layers)):
-                dX[i].copy_(hX[i], non_blocking=True)
-                for j in range(len(hW[i])):
-                    dW[i][j].copy_(hW[i][j], non_blocking=True)
-            outs = runner.step(Xs=dX, Wss=dW)
-            for i, o_l in enumerate(outs):
-                for j, o in enumerate(o_l):
-                    for k in h_out[i][j]:
-                        h_out[i][j][k].copy_(o[k], non_blocking=True)
+                dW[i].copy_(hW[i], non_blocking=True)
+            outs = runner.step(Xs=dX, Wcats=dW)
+            for i, o in enumerate(outs):
+                for k in h_out[i]:
+                    h_out[i][k].copy_(o[k], non_blocking=True)
             torch.cuda.current_stream().synchronize()
 
         for _ in range(max(1, args.warmup)):

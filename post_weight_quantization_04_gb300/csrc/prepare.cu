@@ -286,29 +286,50 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, 
     pdl_wait();
     pdl_trigger();
 
+    const bool vec = ((lda & 3) == 0) && ((k0 & 3) == 0) && ((reinterpret_cast<uintptr_t>(A) & 15) == 0);
     {
-        // all 32 loads of a thread in flight at once
-        float v[NB * NB / 512];
+        // all loads of a thread in flight at once; 16-byte loads where the rows allow
+        float4 v[NB * NB / 4 / 512];
 #pragma unroll
-        for (int u = 0; u < NB * NB / 512; ++u) {
+        for (int u = 0; u < NB * NB / 4 / 512; ++u) {
             const int idx = tid + 512 * u;
-            const int i = idx >> 7, j = idx & (NB - 1);
-            v[u] = (i < n && j <= i) ? A[(k0 + i) * lda + k0 + j] : 0.0f;
+            const int i = idx >> 5, j4 = (idx & 31) << 2;
+            const float* src = A + (k0 + i) * lda + k0 + j4;
+            float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (i < n && j4 <= i) {
+                if (vec && j4 + 3 < n) {
+                    x = *reinterpret_cast<const float4*>(src);
+                } else {
+                    x.x = src[0];
+                    if (j4 + 1 < n) x.y = src[1];
+                    if (j4 + 2 < n) x.z = src[2];
+                    if (j4 + 3 < n) x.w = src[3];
+                }
+                if (j4 + 1 > i) x.y = 0.0f;
+                if (j4 + 2 > i) x.z = 0.0f;
+                if (j4 + 3 > i) x.w = 0.0f;
+            }
+            v[u] = x;
         }
 #pragma unroll
-        for (int u = 0; u < NB * NB / 512; ++u) {
+        for (int u = 0; u < NB * NB / 4 / 512; ++u) {
             const int idx = tid + 512 * u;
-            const int i = idx >> 7, j = idx & (NB - 1);
-            S[i * LD + j] = v[u];
+            const int i = idx >> 5, j4 = (idx & 31) << 2;
+            float* d = S + i * LD + j4;
+            d[0] = v[u].x;
+            d[1] = v[u].y;
+            d[2] = v[u].z;
+            d[3] = v[u].w;
         }
         for (int idx = tid; idx < NB * LDX / 4; idx += 512)
             reinterpret_cast<float4*>(X)[idx] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
     __syncthreads();
+    if (tid < 32) chol_inv_32<LD, LDX>(S, X, XT, min(32, n), lt, status);
 
+    // the diagonal block of sub-panel b is factored (warp 0) before the iteration starts:
+    // for b = 0 above, for the next ones at the end of the previous iteration
     for (int b = 0; b < n; b += 32) {
-        const int nb = min(32, n - b);
-        if (tid < 32) chol_inv_32<LD, LDX>(S + b * LD + b, X + b * LDX + b, XT, nb, lt, status);
         __syncthreads();
         const int rb = b + 32, m = max(0, n - rb);
         const int tm = (m + 3) >> 2;       // 4-row tiles below the sub-panel
@@ -387,54 +408,92 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, 
         if (m <= 0) break;
         __syncthreads();
         // ---- 3. A22 -= L21 L21^T (lower tiles) and B[below, :b+32] -= L21 X[b, :b+32] ----
-        {
-            const int Ts = tm * (tm + 1) / 2, Tb = tm * ((b + 32) >> 2);
-            for (int t = tid; t < Ts + Tb; t += 512) {
+        // Warp 0 updates the next diagonal block (4 x 4 tiles) and then factors it, while
+        // the 12 warps outside its SM sub-partition (warp % 4 != 0) do the rest in 8 x 4
+        // tiles (three 16-byte loads per 32 FMAs, so the shared-memory traffic leaves room
+        // for the factorisation); warps 4, 8 and 12 stay idle so the latency-bound
+        // factorisation has its issue slots to itself.
+        if (tid < 32) {
+            const int D = min(tm, 8), Td = D * (D + 1) / 2;
+            for (int t = tid; t < Td; t += 32) {
+                int ti, tj;
+                tri_tile(t, ti, tj);
+                const int r0 = rb + 4 * ti, c0 = rb + 4 * tj;
                 float acc[4][4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
 #pragma unroll
                     for (int v = 0; v < 4; ++v) acc[u][v] = 0.0f;
+#pragma unroll 4
+                for (int k = 0; k < 32; ++k) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(Lt + k * LDX + r0);
+                    const float4 b4 = *reinterpret_cast<const float4*>(Lt + k * LDX + c0);
+                    const float ar[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        acc[u][0] = fmaf(ar[u], b4.x, acc[u][0]);
+                        acc[u][1] = fmaf(ar[u], b4.y, acc[u][1]);
+                        acc[u][2] = fmaf(ar[u], b4.z, acc[u][2]);
+                        acc[u][3] = fmaf(ar[u], b4.w, acc[u][3]);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        if (r0 + u < n && c0 + v <= r0 + u) S[(r0 + u) * LD + c0 + v] -= acc[u][v];
+            }
+            __syncwarp();
+            chol_inv_32<LD, LDX>(S + rb * LD + rb, X + rb * LDX + rb, XT, min(32, m), lt, status);
+        } else if ((tid >> 5) & 3) {
+            const int w = tid >> 5, p = (w - 1 - (w >> 2)) * 32 + (tid & 31);  // 0 .. 383
+            const int t8 = (m + 7) >> 3;                  // 8-row tiles below the sub-panel
+            // SYRK: 8 x 8 blocks below the next diagonal block, each as two 8 x 4 tiles
+            const int Ts = 2 * max(0, t8 * (t8 + 1) / 2 - 10);
+            const int nbt = (b + 32) >> 2, Tb = t8 * nbt;  // inverse update: 8 x 4 tiles
+            for (int t = p; t < Ts + Tb; t += 384) {
+                int r0, c0;
+                const float* bsrc;
                 if (t < Ts) {
                     int ti, tj;
-                    tri_tile(t, ti, tj);
-                    const int r0 = rb + 4 * ti, c0 = rb + 4 * tj;
-#pragma unroll 4
-                    for (int k = 0; k < 32; ++k) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(Lt + k * LDX + r0);
-                        const float4 b4 = *reinterpret_cast<const float4*>(Lt + k * LDX + c0);
-                        const float ar[4] = {a4.x, a4.y, a4.z, a4.w};
+                    tri_tile((t >> 1) + 10, ti, tj);   // triangle rows 0-3 are the diagonal block
+                    r0 = rb + 8 * ti;
+                    c0 = rb + 8 * tj + 4 * (t & 1);
+                    bsrc = Lt + c0;
+                } else {
+                    const int q = t - Ts;
+                    r0 = rb + 8 * (q / nbt);
+                    c0 = 4 * (q % nbt);
+                    bsrc = X + b * LDX + c0;
+                }
+                float acc[8][4];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            acc[u][0] = fmaf(ar[u], b4.x, acc[u][0]);
-                            acc[u][1] = fmaf(ar[u], b4.y, acc[u][1]);
-                            acc[u][2] = fmaf(ar[u], b4.z, acc[u][2]);
-                            acc[u][3] = fmaf(ar[u], b4.w, acc[u][3]);
-                        }
+                for (int u = 0; u < 8; ++u)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) acc[u][v] = 0.0f;
+#pragma unroll 2
+                for (int k = 0; k < 32; ++k) {
+                    const float4 a0 = *reinterpret_cast<const float4*>(Lt + k * LDX + r0);
+                    const float4 a1 = *reinterpret_cast<const float4*>(Lt + k * LDX + r0 + 4);
+                    const float4 b0 = *reinterpret_cast<const float4*>(bsrc + k * LDX);
+                    const float ar[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        acc[u][0] = fmaf(ar[u], b0.x, acc[u][0]);
+                        acc[u][1] = fmaf(ar[u], b0.y, acc[u][1]);
+                        acc[u][2] = fmaf(ar[u], b0.z, acc[u][2]);
+                        acc[u][3] = fmaf(ar[u], b0.w, acc[u][3]);
                     }
+                }
+                if (t < Ts) {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
+                    for (int u = 0; u < 8; ++u)
 #pragma unroll
                         for (int v = 0; v < 4; ++v)
                             if (r0 + u < n && c0 + v <= r0 + u) S[(r0 + u) * LD + c0 + v] -= acc[u][v];
                 } else {
-                    const int q = t - Ts, nbt = (b + 32) >> 2;
-                    const int r0 = rb + 4 * (q / nbt), c0 = 4 * (q % nbt);
-#pragma unroll 4
-                    for (int k = 0; k < 32; ++k) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(Lt + k * LDX + r0);
-                        const float4 b4 = *reinterpret_cast<const float4*>(X + (b + k) * LDX + c0);
-                        const float ar[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            acc[u][0] = fmaf(ar[u], b4.x, acc[u][0]);
-                            acc[u][1] = fmaf(ar[u], b4.y, acc[u][1]);
-                            acc[u][2] = fmaf(ar[u], b4.z, acc[u][2]);
-                            acc[u][3] = fmaf(ar[u], b4.w, acc[u][3]);
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
+                    for (int u = 0; u < 8; ++u)
                         if (r0 + u < n) {
                             float4* xp = reinterpret_cast<float4*>(X + (r0 + u) * LDX + c0);
                             float4 xv = *xp;
@@ -447,20 +506,38 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, 
                 }
             }
         }
-        __syncthreads();
     }
     __syncthreads();
 
-#pragma unroll 4
-    for (int idx = tid; idx < NB * NB; idx += 512) {
-        const int i = idx >> 7, j = idx & (NB - 1);
-        if (i < n && j <= i) A[(k0 + i) * lda + k0 + j] = S[i * LD + j];
-        const float v = (i < n && j <= i) ? X[i * LDX + j] : 0.0f;
-        if (Linv) Linv[idx] = v;
+#pragma unroll 2
+    for (int idx = tid; idx < NB * NB / 4; idx += 512) {
+        const int i = idx >> 5, j4 = (idx & 31) << 2;
+        if (i < n && j4 <= i) {
+            float* dst = A + (k0 + i) * lda + k0 + j4;
+            const float* src = S + i * LD + j4;
+            if (vec && j4 + 3 <= i && j4 + 3 < n) {
+                *reinterpret_cast<float4*>(dst) = make_float4(src[0], src[1], src[2], src[3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (j4 + e <= i && j4 + e < n) dst[e] = src[e];
+            }
+        }
+        float4 v = *reinterpret_cast<const float4*>(X + i * LDX + j4);
+        if (i >= n) v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (j4 + 0 > i || j4 + 0 >= n) v.x = 0.0f;
+        if (j4 + 1 > i || j4 + 1 >= n) v.y = 0.0f;
+        if (j4 + 2 > i || j4 + 2 >= n) v.z = 0.0f;
+        if (j4 + 3 > i || j4 + 3 >= n) v.w = 0.0f;
+        if (Linv) *reinterpret_cast<float4*>(Linv + 4 * idx) = v;
         if (Lhi) {  // TF32 split for the tensor-core products that use L_kk^-1
-            const float h = __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
-            Lhi[idx] = h;
-            Llo[idx] = v - h;
+            float4 h;
+            h.x = __uint_as_float(__float_as_uint(v.x) & 0xFFFFE000u);
+            h.y = __uint_as_float(__float_as_uint(v.y) & 0xFFFFE000u);
+            h.z = __uint_as_float(__float_as_uint(v.z) & 0xFFFFE000u);
+            h.w = __uint_as_float(__float_as_uint(v.w) & 0xFFFFE000u);
+            *reinterpret_cast<float4*>(Lhi + 4 * idx) = h;
+            *reinterpret_cast<float4*>(Llo + 4 * idx) = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
         }
     }
 }

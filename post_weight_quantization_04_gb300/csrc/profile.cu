@@ -45,7 +45,7 @@ const char* kNames[K_COUNT] = {
     "hessian_tc_kernel",   "hessian_simt_kernel", "finalize_kernel",   "prep_diag_kernel",
     "prep_perm_kernel",    "prep_gather_kernel",  "potrf_diag_kernel", "sgemm_kernel[prepare]",
     "eye_kernel",          "prep_scatter_kernel", "init_work_kernel",  "row_params_kernel",
-    "gptq_block_kernel",   "sgemm_kernel[trailing]", "g_idx_kernel",   "copy_loss_kernel",
+    "gptq_block_kernel",   "sgemm_kernel[trailing]", "g_idx_kernel",
     "pack_kernel",         "rtn_kernel",          "split_kernel",      "tc_gemm_nt_kernel[prepare]",
     "tc_gemm_nt_kernel[trailing]",
 };

@@ -382,10 +382,6 @@ __global__ void g_idx_kernel(const int32_t* __restrict__ perm, int64_t cols, int
     g_idx[c] = group ? (int32_t)(k / group) : 0;
 }
 
-__global__ void copy_loss_kernel(const float* __restrict__ src, int64_t rows, float* __restrict__ dst) {
-    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (r < rows) dst[r] = src[r];
-}
 
 // One thread per output word: bits [32w, 32w+32) of the row's LSB-first b-bit stream.
 __global__ void pack_kernel(const int8_t* __restrict__ codes, int64_t rows, int64_t cols, int bits, int offset,
@@ -535,7 +531,9 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
 
     // (the memsets first: every later item in the stream is one of this call's kernels, so
     // the block and trailing kernels may be launched as programmatic dependents)
-    GPTQ_CUDA_TRY(cudaMemsetAsync(w.loss, 0, sizeof(float) * rows, s));
+    // the per-row loss accumulates straight into the caller's row_loss when given
+    float* loss = row_loss ? row_loss : w.loss;
+    GPTQ_CUDA_TRY(cudaMemsetAsync(loss, 0, sizeof(float) * rows, s));
     GPTQ_CUDA_TRY(cudaMemsetAsync(w.status, 0, sizeof(int), s));
     {
         dim3 grid((unsigned)std::min<int64_t>(ceil_div(cols, 256), 64), (unsigned)rows);
@@ -592,7 +590,7 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
     a.scales = scales;
     a.zeros = zeros;
     a.G = G;
-    a.loss = w.loss;
+    a.loss = loss;
     const unsigned bgrid = (unsigned)ceil_div(rows, 128 / tpr);
     for (int64_t j0 = 0; j0 < cols; j0 += QB) {
         const int bw = (int)std::min<int64_t>(QB, cols - j0);
@@ -630,10 +628,6 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
 
     if (g_idx) {
         GPTQ_LAUNCH(K_G_IDX, s, g_idx_kernel<<<(unsigned)ceil_div(cols, 256), 256, 0, s>>>(perm, cols, q.group, g_idx));
-        GPTQ_LAUNCH_CHECK();
-    }
-    if (row_loss) {
-        GPTQ_LAUNCH(K_COPY_LOSS, s, copy_loss_kernel<<<(unsigned)ceil_div(rows, 256), 256, 0, s>>>(w.loss, rows, row_loss));
         GPTQ_LAUNCH_CHECK();
     }
     if (packed) {

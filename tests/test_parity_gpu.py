@@ -300,3 +300,33 @@ def test_correlated_channels_gptq_beats_rtn(lib, bits, group, sym, act):
     e_rtn = O.rel_output_error_from_xtx(S, Wh, npy(rtn["Wq"]))
     assert abs(e_gpu - e_ref) <= 0.02 * e_ref, (e_gpu, e_ref)
     assert e_gpu < 0.9 * e_rtn, (e_gpu, e_rtn)
+
+
+def test_stacked_weights_equal_per_weight_calls(lib):
+    """Rows are independent given U: one gptq_quantize over the weights of a layer stacked
+    by rows gives, row for row, exactly what one call per weight gives. (The benchmark
+    quantises each layer's weights stacked, as one fused projection.)"""
+    import bench
+    wl, layers = bench.build_layers(1, DEV)
+    L = layers[0]
+    q = L.spec.q
+    h = lib.Hessian(L.X.shape[1])
+    h.accumulate(L.X)
+    H, diag, _ = h.finalize()
+    U, perm, dead = lib.gptq_prepare(H, diag, q.damp, act_order=q.act_order)
+    cat = lib.gptq_quantize(L.Wcat, U, perm, dead, q.bits, q.group, q.sym)
+    r0 = 0
+    for W in L.Ws:
+        one = lib.gptq_quantize(W, U, perm, dead, q.bits, q.group, q.sym)
+        r1 = r0 + W.shape[0]
+        for k in ("codes", "scales", "zeros", "Wq", "packed", "row_loss"):
+            assert torch.equal(cat[k][r0:r1], one[k]), k
+        assert torch.equal(cat["g_idx"], one["g_idx"])
+        r0 = r1
+    # the benchmark's runner: one step, outputs split back per weight
+    runner = bench.Runner(lib, layers, torch.device(DEV))
+    runner.step()
+    torch.cuda.synchronize()
+    parts = runner.weight_outputs(0)
+    assert [p["codes"].shape[0] for p in parts] == [W.shape[0] for W in L.Ws]
+    assert all(bool(torch.isfinite(p["Wq"]).all()) for p in parts)
