@@ -14,8 +14,9 @@
 //               instruction, three products per K step, into one of two TMEM
 //               accumulators (128 columns each)
 //   warps 2..5  epilogue: TMEM -> registers, combined with the C tile that the producer
-//               brought into shared memory by TMA, stored back by TMA; overlaps the MMAs
-//               of the next tile in the other accumulator
+//               brought into shared memory by TMA, stored back by TMA in four 32-column
+//               chunks (the next tile's chunk loads as soon as this one's has been read
+//               by its store); overlaps the MMAs of the next tile in the other accumulator
 // Every mbarrier wait is bounded (GPTQ_ERR_TIMEOUT into *status, then unwind).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -71,6 +72,7 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 // barrier over the 128 epilogue threads that also ANDs a predicate across them, so that
@@ -130,8 +132,8 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* cbuf = smem + G_STAGES * G_STAGE;
     uint64_t* bars = reinterpret_cast<uint64_t*>(cbuf + G_CBUF);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sbase = smem_u32(smem), cbase = smem_u32(cbuf), bar0 = smem_u32(bars);
@@ -139,9 +141,11 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
     auto empty_bar = [&](int s) { return bar0 + 8u * (G_STAGES + s); };
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * G_STAGES + b); };
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * G_STAGES + 2 + b); };
-    const uint32_t cfull_bar = bar0 + 8u * (2 * G_STAGES + 4);
-    const uint32_t cempty_bar = bar0 + 8u * (2 * G_STAGES + 5);
-    const uint32_t drain_bar = bar0 + 8u * (2 * G_STAGES + 6);
+    // the C tile moves as four 32-column chunks, each with its own full / empty barrier,
+    // so the next tile's chunk c loads as soon as this tile's chunk c has been stored
+    auto cfull_bar = [&](int c) { return bar0 + 8u * (2 * G_STAGES + 4 + c); };
+    auto cempty_bar = [&](int c) { return bar0 + 8u * (2 * G_STAGES + 8 + c); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * G_STAGES + 12);
     const bool load_c = p.beta != 0.0f;
 
     if (threadIdx.x == 0) {
@@ -153,8 +157,10 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
             mbar_init(tfull_bar(b), 1);
             mbar_init(tempty_bar(b), 4);
         }
-        mbar_init(cfull_bar, 1);
-        mbar_init(cempty_bar, 1);
+        for (int c = 0; c < 4; ++c) {
+            mbar_init(cfull_bar(c), 1);
+            mbar_init(cempty_bar(c), 1);
+        }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -182,8 +188,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
         // ------------------------------- TMA producer -------------------------------
         if (lane == 0) {
             int stage = 0;
-            uint32_t phase = 0, issued = 0, issued_par = 0, cph = 0;
-            bool c_issued = false;
+            uint32_t phase = 0, issued = 0, issued_par = 0, cph = 0, c_issued = 0, c_par = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
                 int tm, tn;
@@ -209,18 +214,26 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                 }
                 if (!ok) break;
                 if (load_c) {
-                    // the C buffer is free once the previous tile's stores have read it
-                    if (!mbar_wait(cempty_bar, cph ^ 1u, abort_flag, p.status)) break;
-                    mbar_expect_tx(cfull_bar, G_CBUF);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) tma_load_2d(cbase + c * G_BOX, &tC, cfull_bar, tn * G_BN + 32 * c, tm * G_BM);
-                    c_issued = true;
+                    // chunk c of the C buffer is free once the previous tile's store of it
+                    // has been read
+                    for (int c = 0; c < 4 && ok; ++c) {
+                        if (!mbar_wait(cempty_bar(c), cph ^ 1u, abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_expect_tx(cfull_bar(c), G_BOX);
+                        tma_load_2d(cbase + c * G_BOX, &tC, cfull_bar(c), tn * G_BN + 32 * c, tm * G_BM);
+                        c_issued |= 1u << c;
+                        c_par = (c_par & ~(1u << c)) | (cph << c);
+                    }
+                    if (!ok) break;
                     cph ^= 1u;
                 }
             }
             for (int s = 0; s < G_STAGES; ++s)
                 if (issued & (1u << s)) drain_wait(full_bar(s), (issued_par >> s) & 1u, p.status);
-            if (c_issued) drain_wait(cfull_bar, cph ^ 1u, p.status);
+            for (int c = 0; c < 4; ++c)
+                if (c_issued & (1u << c)) drain_wait(cfull_bar(c), (c_par >> c) & 1u, p.status);
         }
     } else if (warp == 1) {
         // ------------------------------- MMA issuer ---------------------------------
@@ -274,17 +287,20 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
         const bool storer = (threadIdx.x == 64);
         int abuf = 0;
         uint32_t aphase = 0, cph = 0;
-        for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+        bool alive = true;
+        for (int t = blockIdx.x; t < p.ntiles && alive; t += gridDim.x) {
             int tm, tn;
             tile_of(p, t, tm, tn);
-            bool ok = mbar_wait(tfull_bar(abuf), aphase, abort_flag, p.status);
-            if (ok && load_c) ok = mbar_wait(cfull_bar, cph, abort_flag, p.status);
-            if (!epi_all(ok)) break;
+            if (!epi_all(mbar_wait(tfull_bar(abuf), aphase, abort_flag, p.status))) break;
             tc_fence_after();
             const int row = tm * G_BM + rl;
             const uint32_t ta = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(abuf * G_BN);
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
+                if (load_c && !epi_all(mbar_wait(cfull_bar(c), cph, abort_flag, p.status))) {
+                    alive = false;
+                    break;
+                }
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(ta + 32 * c, v);
                 tmem_ld_wait();
@@ -318,20 +334,28 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                         }
                     }
                 }
+                fence_proxy_async_smem();   // make the chunk visible to TMA
+                epi_barrier();
+                if (storer) {
+                    // store chunk c; once the store of chunk c-1 has read its buffer, the
+                    // producer may load the next tile's chunk c-1 there. (Writes of the next
+                    // tile's chunk c-1 by the other threads come after a later barrier.)
+                    tma_store_2d(&tC, cbase + c * G_BOX, tn * G_BN + 32 * c, tm * G_BM);
+                    bulk_commit();
+                    if (c > 0) {
+                        bulk_wait_read1();
+                        if (load_c) mbar_arrive(cempty_bar(c - 1));
+                    }
+                }
             }
+            if (!alive) break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(abuf));   // the accumulator is free again
-            fence_proxy_async_smem();                        // make the tile visible to TMA
-            epi_barrier();
             if (storer) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tma_store_2d(&tC, cbase + c * G_BOX, tn * G_BN + 32 * c, tm * G_BM);
-                bulk_commit();
                 bulk_wait_read0();
-                if (load_c) mbar_arrive(cempty_bar);
+                if (load_c) mbar_arrive(cempty_bar(3));
             }
-            epi_barrier();                                   // the buffer may be written again
             if (++abuf == 2) {
                 abuf = 0;
                 aphase ^= 1u;
