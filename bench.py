@@ -6,6 +6,7 @@ prepare (dead fix, damping, act_order, U), and the GPTQ column loop + packing fo
 every weight that shares the layer input. Inputs are seeded synthetic layers.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+  python bench.py --op dequant_matmul [--config C] [--tokens T]   (the stored-form consumer)
 
 Prints one JSON line. `value` is milliseconds per layer pass (lower is better),
 device-timed with CUDA events, L2 flushed between steps when the inputs fit in it.
@@ -44,6 +45,8 @@ def parse(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-profile", action="store_true")
+    ap.add_argument("--op", choices=["layer", "dequant_matmul"], default="layer")
+    ap.add_argument("--tokens", type=int, default=8192)
     return ap.parse_args(argv)
 
 
@@ -588,6 +591,65 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_dequant_matmul(args):
+    """Y = X Wq^T from the stored form of the workload's first stacked weight matrix (as
+    gptq_quantize writes it), X = the first `tokens` rows of that layer's input. One JSON
+    line: TFLOP/s against the measured bf16 peak, and the stored-weight bytes read."""
+    import torch
+    import post_weight_quantization_04_gb300 as lib
+    from post_weight_quantization_04_gb300 import build as B
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    B.build()
+    lib.load()
+    dev = torch.device("cuda", 0)
+    pk = peaks()
+    wl, layers = build_layers(args.config, dev)
+    L = layers[0]
+    q = L.spec.q
+    h = lib.Hessian(L.X.shape[1], dev)
+    h.accumulate(L.X)
+    H, diag, _ = h.finalize()
+    U, perm, dead = lib.gptq_prepare(H, diag, q.damp, act_order=q.act_order)
+    st = lib.gptq_quantize(L.Wcat, U, perm, dead, q.bits, q.group, q.sym)
+    X = L.X[: args.tokens].contiguous()
+    T, K = X.shape
+    N = L.Wcat.shape[0]
+    Y = torch.empty(T, N, dtype=torch.float32, device=dev)
+    zeros = st["zeros"]
+
+    def step():
+        lib.gptq_dequant_matmul(X, st["packed"], st["scales"], zeros, st["g_idx"], q.bits, out=Y)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n0 = lib.gptq_launch_count()
+    times = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = statistics.mean(times)
+    flops = 2.0 * T * K * N
+    tf = flops / (ms * 1e-3) / 1e12
+    wbytes = st["packed"].numel() * 4 + st["scales"].numel() * 4 + zeros.numel()
+    print(json.dumps({
+        "metric": "dequant matmul from the stored form (TFLOP/s)", "value": tf, "unit": "TFLOP/s",
+        "higher_is_better": True, "ms_per_step": ms, "steps": args.steps, "n_gpus": 1,
+        "dtype": "bf16 x (b-bit -> bf16) -> f32", "data": "synthetic",
+        "config": {"workload": wl.name, "tokens": T, "in": K, "out": N, "bits": q.bits, "group": q.group,
+                   "act_order": q.act_order, "stored_weight_bytes": wbytes},
+        "gpu_launches": lib.gptq_launch_count() - n0,
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tf / pk["bf16_tflops"], "traffic": None},
+    }), flush=True)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_info()
@@ -599,7 +661,10 @@ def main():
                 return
         else:
             dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    if args.impl == "reference":
+    if args.op == "dequant_matmul":
+        if rank == 0:
+            run_dequant_matmul(args)
+    elif args.impl == "reference":
         run_reference(args, ws, rank)
     else:
         run_ours(args, ws, rank, local)

@@ -11,6 +11,8 @@
  *                             dequantised W, packed codes
  *   rtn_quantize              round-to-nearest on the same grid (the baseline)
  *   gptq_pack                 codes -> LSB-first bitstream of b-bit unsigned codes
+ *   gptq_dequant_matmul       Y = X Wq^T read straight from the packed codes, scales,
+ *                             zeros and g_idx (the consumer of the stored form)
  *
  * Conventions shared by every entry point
  *   - Pointers named as device pointers must be CUDA device (or managed) memory of the
@@ -168,6 +170,30 @@ int rtn_quantize(const float* W, int64_t rows, int64_t cols, const uint8_t* dead
 int64_t gptq_packed_words_per_row(int64_t cols, int bits);
 int gptq_pack(const int8_t* codes, int64_t rows, int64_t cols, int bits, int sym,
               uint32_t* packed, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Consumer of the stored form.  GPTQ guide page, "When it breaks" (with act_order the
+ * groups are scattered over the columns, so a kernel that uses the quantised weights needs
+ * the stored column-to-group index g_idx); AutoGPTQ page, `dequantize_weight`
+ * (scale * (code - zero)).
+ *
+ * Y[t][o] = sum_k X[t][k] * Wq[o][k],  Wq[o][k] = scales[o][g] * (u[o][k] - zeros[o][g]),
+ * g = g_idx[k], u[o][k] = the k-th bits-wide field of row o of `packed` (the layout of
+ * gptq_pack; symmetric codes are stored with zero point 2^(bits-1), so the same formula
+ * gives scale * code).
+ *   X       device, bf16, (T, K) row-major, row stride ldx elements (ldx % 8 == 0, X 16-byte
+ *           aligned), K % 64 == 0
+ *   packed  device, uint32, (N, gptq_packed_words_per_row(K, bits))
+ *   scales  device, fp32, (N, G); zeros device, uint8, (N, G); g_idx device, int32, (K),
+ *           16-byte aligned, values in [0, G) (others record INVALID_ARG and read group 0)
+ *   Y       device, fp32, (T, N) row-major, row stride ldy
+ * The weights are expanded to bf16 on chip (rounding each to 8 significant bits) and
+ * multiplied on the tensor cores with fp32 accumulation. Synchronises the stream and
+ * returns the device status. Errors: INVALID_ARG, UNSUPPORTED (bits not 2-4, K % 64,
+ * alignment), TIMEOUT, CUDA. */
+int gptq_dequant_matmul(const void* X, int64_t T, int64_t K, int64_t ldx, const uint32_t* packed,
+                        const float* scales, const uint8_t* zeros, const int32_t* g_idx, int64_t N,
+                        int64_t G, int bits, float* Y, int64_t ldy, void* stream);
 
 /* Static text for a status code. */
 const char* gptq_status_string(int status);

@@ -52,7 +52,7 @@ __all__ = [
     "gptq_loop", "gptq_quantize", "gptq_layer", "rtn_quantize", "unsigned_codes", "pack_rows",
     "g_idx_for", "rel_output_error", "rel_output_error_from_xtx", "layer_loss",
     "obs_bruteforce_row", "auto_compute_hessian", "auto_gptq_quantize_row", "auto_dequantize_row",
-    "near_half", "perm_equivalent", "TieMismatch",
+    "near_half", "perm_equivalent", "TieMismatch", "unpack_rows", "dequant_stored", "dequant_matmul",
 ]
 
 
@@ -332,6 +332,38 @@ def pack_rows(ucodes, bits: int) -> np.ndarray:
     weights = np.array([1 << k for k in range(32)], dtype=np.int64)
     words = (stream.reshape(o, nwords, 32) * weights).sum(axis=2)
     return words.astype(np.uint32)
+
+
+def unpack_rows(packed, bits: int, d: int) -> np.ndarray:
+    """The d unsigned `bits`-bit codes of each row of a pack_rows bitstream: code c is
+    stream bits [c*bits, (c+1)*bits), stream bit p being bit (p % 32) of word p // 32."""
+    w = np.asarray(packed).astype(np.uint32).astype(np.int64)
+    o = w.shape[0]
+    stream = (w[:, :, None] >> np.arange(32, dtype=np.int64)) & 1
+    stream = stream.reshape(o, -1)[:, : d * bits]
+    u = np.zeros((o, d), dtype=np.int64)
+    for b in range(bits):
+        u |= stream[:, b::bits] << b
+    return u
+
+
+def dequant_stored(packed, scales, zeros, g_idx, bits: int, d: int) -> np.ndarray:
+    """The weights a consumer of the stored form sees: Wq[o][k] = s[o][g] * (u[o][k] -
+    z[o][g]) with g = g_idx[k] ([auto] `dequantize_weight`: scale * (code - zero); [guide]
+    "When it breaks": with act_order a kernel needs the stored column-to-group index).
+    Symmetric codes are stored as u = code + 2^(bits-1) with zero 2^(bits-1), so this is
+    scale * code for them."""
+    u = unpack_rows(packed, bits, d).astype(F64)
+    g = np.asarray(g_idx, dtype=np.int64)
+    s = np.asarray(scales, dtype=F64)[:, g]
+    z = np.asarray(zeros, dtype=F64)[:, g]
+    return s * (u - z)
+
+
+def dequant_matmul(X, packed, scales, zeros, g_idx, bits: int) -> np.ndarray:
+    """Y = X Wq^T in fp64 with Wq from the stored form (dequant_stored)."""
+    X = np.asarray(X, dtype=F64)
+    return X @ dequant_stored(packed, scales, zeros, g_idx, bits, X.shape[1]).T
 
 
 def gptq_quantize(W, U, perm, dead, bits: int, group: int = 0, sym: bool = True,

@@ -31,7 +31,8 @@ EXPORTS = [
     "gptq_hessian_create", "gptq_hessian_reset", "gptq_hessian_accumulate", "gptq_hessian_finalize",
     "gptq_hessian_destroy", "gptq_prepare_workspace_bytes", "gptq_prepare", "gptq_prepare_noalloc",
     "gptq_quantize_workspace_bytes",
-    "gptq_quantize", "rtn_quantize", "gptq_packed_words_per_row", "gptq_pack", "gptq_status_string",
+    "gptq_quantize", "rtn_quantize", "gptq_packed_words_per_row", "gptq_pack", "gptq_dequant_matmul",
+    "gptq_status_string",
     "gptq_launch_count", "gptq_profile_enable", "gptq_profile_read", "gptq_profile_kernel_count",
     "gptq_profile_kernel_name",
 ]
@@ -71,6 +72,7 @@ def _declare(lib: ctypes.CDLL) -> None:
         "rtn_quantize": (_I, [_P, _I64, _I64, _P, QConfig, _P, _P, _P, _P, _P, _P]),
         "gptq_packed_words_per_row": (_I64, [_I64, _I]),
         "gptq_pack": (_I, [_P, _I64, _I64, _I, _I, _P, _P]),
+        "gptq_dequant_matmul": (_I, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _I64, _I64, _I, _P, _I64, _P]),
         "gptq_status_string": (ctypes.c_char_p, [_I]),
         "gptq_launch_count": (ctypes.c_ulonglong, []),
         "gptq_profile_enable": (None, [_I]),
@@ -292,6 +294,25 @@ def gptq_pack(codes: torch.Tensor, bits: int, sym: bool = True, out: Optional[to
     return p
 
 
+def gptq_dequant_matmul(X: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
+                        g_idx: torch.Tensor, bits: int, out: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    """Y = X Wq^T straight from the stored form (packed codes, scales, zeros, g_idx)."""
+    T, K = X.shape
+    N, G = scales.shape
+    _dev(X, torch.bfloat16, "X")
+    _dev(packed, torch.int32, "packed", (N, gptq_packed_words_per_row(K, bits)))
+    _dev(scales, torch.float32, "scales")
+    _dev(zeros, torch.uint8, "zeros", (N, G))
+    _dev(g_idx, torch.int32, "g_idx", (K,))
+    Y = out if out is not None else torch.empty(T, N, dtype=torch.float32, device=X.device)
+    _dev(Y, torch.float32, "Y", (T, N))
+    _check("gptq_dequant_matmul", load().gptq_dequant_matmul(
+        _ptr(X), T, K, K, _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(g_idx), N, G, bits, _ptr(Y), N,
+        _stream(stream)))
+    return Y
+
+
 def gptq_status_string(status: int) -> str:
     return _str(status)
 
@@ -320,5 +341,6 @@ __all__ = [
     "load", "Hessian", "GptqError", "QConfig", "qconfig", "gptq_hessian_create", "gptq_hessian_accumulate",
     "gptq_hessian_finalize", "gptq_prepare", "gptq_prepare_workspace_bytes", "gptq_quantize",
     "gptq_quantize_workspace_bytes", "rtn_quantize", "gptq_pack", "gptq_packed_words_per_row",
-    "gptq_status_string", "gptq_launch_count", "gptq_profile_enable", "gptq_profile_read", "EXPORTS", "LIB_PATH",
+    "gptq_dequant_matmul", "gptq_status_string", "gptq_launch_count", "gptq_profile_enable", "gptq_profile_read",
+    "EXPORTS", "LIB_PATH",
 ]

@@ -30,7 +30,7 @@ namespace gptq {
 enum KernelId {
     K_HESS_TC, K_HESS_SIMT, K_FINALIZE, K_PREP_DIAG, K_PREP_PERM, K_PREP_GATHER, K_POTRF, K_SGEMM_PREP,
     K_EYE, K_SCATTER, K_INIT_WORK, K_ROW_PARAMS, K_BLOCK, K_SGEMM_TRAIL, K_G_IDX, K_PACK, K_RTN,
-    K_SPLIT, K_TC_PREP, K_TC_TRAIL, K_COUNT
+    K_SPLIT, K_TC_PREP, K_TC_TRAIL, K_DEQUANT_MM, K_COUNT
 };
 void prof_begin(int id, cudaStream_t s);
 void prof_end(int id, cudaStream_t s);
@@ -144,6 +144,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             }
         }
     }
+}
+
+// The same wait for a whole warp with one lane polling: the other 31 lanes do not poll the
+// barrier word; once lane 0 has seen the phase complete, each lane's own try_wait succeeds
+// at once and gives it the barrier's acquire ordering. Call from all 32 lanes, and only for
+// a barrier whose next phase cannot complete before this warp itself arrives somewhere.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               int* status) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, status);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (ok) ok = mbar_try_wait(bar, parity);
+    return ok;
 }
 
 __device__ __forceinline__ void fence_barrier_init() {

@@ -1,0 +1,511 @@
+// dequant_matmul.cu — Y = X Wq^T computed straight from GPTQ's stored form: packed
+// b-bit codes, per-group scales and zero points, and the column-to-group index g_idx.
+//
+// Wq[o][k] = s[o][g] * (u[o][k] - z[o][g]) with g = g_idx[k] (GPTQ guide page, "When it
+// breaks": with act_order, a kernel that consumes groups needs the stored column-to-group
+// index; AutoGPTQ page, `dequantize_weight`: scale * (code - zero)). u is the k-th b-bit
+// field of row o's LSB-first bitstream (the packing of `gptq_pack`).
+//
+// Structure (one CTA per SM, persistent over a contiguous range of 128 tokens x 128
+// outputs tiles, output tile major):
+//   warp 0       TMA producer: the 128 x 64 bf16 X box of each K step (128-byte swizzle)
+//   warp 1       single-thread tcgen05.mma issuer, kind::f16 (bf16 x bf16 -> fp32),
+//                M = N = 128, K = 16 per instruction, two TMEM accumulators
+//   warps 2..5   epilogue: TMEM -> registers -> fp32 Y
+//   warps 6..13  dequantisers: unpack the b-bit codes of 128 output rows x 64 columns,
+//                look up s and z through g_idx (per-tile tables in shared memory), and
+//                write the bf16 weights straight into the K-major, 128-byte-swizzled image
+//                the MMA reads
+//   warp 14      loader: the packed words of each K step into a shared ring by cp.async
+//                (so the dequantisers, which must fence their writes for the tensor core,
+//                never have a global load in flight)
+// The weight tile is produced on chip, so W is read from HBM as b bits per weight.
+// Every mbarrier wait is bounded (GPTQ_ERR_TIMEOUT into the status word, then unwind).
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "tc_gemm.cuh"
+
+namespace gptq {
+
+namespace {
+
+constexpr int D_BM = 128, D_BN = 128, D_BK = 64;
+// X boxes come from L2 or HBM and need a deep ring to hide their latency; the weight
+// boxes are produced on chip and need only a short one
+constexpr int D_XS = 3, D_WS = 3, D_PS = 4;
+constexpr int D_BOX = D_BM * D_BK * 2;       // 16 KB: 128 rows x 64 bf16
+constexpr int D_PBOX = D_BN * 32;               // one K step of packed words: 128 rows x <= 32 B
+constexpr int D_RING = (D_XS + D_WS) * D_BOX + D_PS * D_PBOX;  // X ring, weight ring, packed ring
+constexpr int D_DQ_WARPS = 8;
+constexpr int D_LOADER_WARP = 6 + D_DQ_WARPS;
+constexpr int D_THREADS = 32 * (7 + D_DQ_WARPS);
+constexpr int D_SMEM_MAX = 227 * 1024;
+constexpr uint32_t D_TMEM_COLS = 2 * D_BN;
+// kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (1), both K-major, N >> 3, M >> 4
+constexpr uint32_t D_IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(D_BN >> 3) << 17) |
+                             ((uint32_t)(D_BM >> 4) << 24);
+
+struct DParams {
+    int T, N, K;
+    int tiles_n, ntiles;
+    const uint32_t* packed;
+    int64_t words;  // 32-bit words per packed row
+    const float* scales;
+    const uint8_t* zeros;
+    int64_t G;
+    const int32_t* g_idx;
+    float* Y;
+    int64_t ldy;
+    int* status;
+    // shared-memory layout after the stages and barriers: g_idx as int16 (K entries), then
+    // (when tab) the tile's scales (128 x sp floats) and zero points (128 x zp bytes); sp
+    // odd and zp / 4 odd so the 32 rows a warp reads hit 32 different banks
+    int tab, sp, zp;
+    int g_off, s_off, z_off;
+};
+
+__device__ __forceinline__ uint32_t bf16x2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // .x = a (low half), .y = b
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void drain(uint32_t bar, uint32_t parity, int* status) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            set_status(status, GPTQ_ERR_TIMEOUT);
+            return;
+        }
+    }
+}
+
+// TAB: scales and zero points come from the per-tile tables in shared memory (a compile-time
+// choice: with a runtime flag the compiler may issue both sources' loads)
+template <int BITS, bool TAB>
+__global__ void __launch_bounds__(D_THREADS, 1) dequant_matmul_kernel(const __grid_constant__ CUtensorMap tX,
+                                                                     const DParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + D_RING);
+    int16_t* g16 = reinterpret_cast<int16_t*>(smem + p.g_off);
+    float* s_tab = reinterpret_cast<float*>(smem + p.s_off);
+    uint8_t* z_tab = smem + p.z_off;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 30);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 31);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t sbase = smem_u32(smem), bar0 = smem_u32(bars);
+    auto xfull = [&](int s) { return bar0 + 8u * s; };                     // X box landed (TMA)
+    auto xempty = [&](int s) { return bar0 + 8u * (D_XS + s); };           // its MMAs are done
+    auto wfull = [&](int s) { return bar0 + 8u * (2 * D_XS + s); };        // weight box written
+    auto wempty = [&](int s) { return bar0 + 8u * (2 * D_XS + D_WS + s); };
+    auto tfull = [&](int b) { return bar0 + 8u * (2 * D_XS + 2 * D_WS + b); };
+    auto tempty = [&](int b) { return bar0 + 8u * (2 * D_XS + 2 * D_WS + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * D_XS + 2 * D_WS + 4);
+    auto pfull = [&](int s) { return bar0 + 8u * (2 * D_XS + 2 * D_WS + 5 + s); };        // words landed
+    auto pempty = [&](int s) { return bar0 + 8u * (2 * D_XS + 2 * D_WS + 5 + D_PS + s); }; // words read
+    uint8_t* pring = smem + (D_XS + D_WS) * D_BOX;
+    const int ktiles = p.K / D_BK;
+    // each CTA walks a contiguous range of tiles, ordered by output tile first, so the
+    // weight rows (and their scale table) stay the same across consecutive tiles
+    const int t_begin = (int)((int64_t)blockIdx.x * p.ntiles / gridDim.x);
+    const int t_end = (int)((int64_t)(blockIdx.x + 1) * p.ntiles / gridDim.x);
+    const int tiles_m = p.ntiles / p.tiles_n;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < D_XS; ++s) {
+            mbar_init(xfull(s), 1);
+            mbar_init(xempty(s), 1);
+        }
+        for (int s = 0; s < D_WS; ++s) {
+            mbar_init(wfull(s), D_DQ_WARPS);
+            mbar_init(wempty(s), 1);
+        }
+        for (int s = 0; s < D_PS; ++s) {
+            mbar_init(pfull(s), 32);            // one cp.async completion per loader lane
+            mbar_init(pempty(s), D_DQ_WARPS);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull(b), 1);
+            mbar_init(tempty(b), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&tX);
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), D_TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------- TMA producer (X) ---------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_par = 0;
+            bool ok = true;
+            for (int t = t_begin; t < t_end && ok; ++t) {
+                const int tm = t % tiles_m;
+                for (int kt = 0; kt < ktiles; ++kt) {
+                    if (!mbar_wait(xempty(stage), phase ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(xfull(stage), D_BOX);
+                    tma_load_2d(sbase + stage * D_BOX, &tX, xfull(stage), kt * D_BK, tm * D_BM);
+                    issued |= 1u << stage;
+                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == D_XS) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (int s = 0; s < D_XS; ++s)
+                if (issued & (1u << s)) drain(xfull(s), (issued_par >> s) & 1u, p.status);
+        }
+    } else if (warp == 1) {
+        // ------------------------------- MMA issuer ---------------------------------
+        if (lane == 0) {
+            int xs = 0, ws = 0, abuf = 0;
+            uint32_t xph = 0, wph = 0, aphase = 0;
+            bool ok = true;
+            for (int t = t_begin; t < t_end && ok; ++t) {
+                if (!mbar_wait(tempty(abuf), aphase ^ 1u, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t dt = tmem_base + (uint32_t)(abuf * D_BN);
+                for (int kt = 0; kt < ktiles; ++kt) {
+                    if (!mbar_wait(xfull(xs), xph, abort_flag, p.status) ||
+                        !mbar_wait(wfull(ws), wph, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = sbase + xs * D_BOX, sb = sbase + (D_XS + ws) * D_BOX;
+#pragma unroll
+                    for (int kk = 0; kk < D_BK / 16; ++kk) {
+                        // 16 bf16 = 32 bytes along K inside the 128-byte swizzle row
+                        const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(sb + kk * 32, 16, 1024, kSwizzle128B);
+                        umma_f16(dt, ad, bd, D_IDESC, (kt > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(xempty(xs));
+                    umma_commit(wempty(ws));
+                    if (++xs == D_XS) {
+                        xs = 0;
+                        xph ^= 1u;
+                    }
+                    if (++ws == D_WS) {
+                        ws = 0;
+                        wph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull(abuf));
+                if (++abuf == 2) {
+                    abuf = 0;
+                    aphase ^= 1u;
+                }
+            }
+            umma_commit(drain_bar);
+            drain(drain_bar, 0, p.status);
+        }
+    } else if (warp < 6) {
+        // ------------------------------- epilogue (4 warps) -------------------------
+        const int q = warp & 3;
+        int abuf = 0;
+        uint32_t aphase = 0;
+        const bool vec = ((p.ldy & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.Y) & 15) == 0);
+        for (int t = t_begin; t < t_end; ++t) {
+            const int tm = t % tiles_m, tn = t / tiles_m;
+            if (!mbar_wait_warp(tfull(abuf), aphase, abort_flag, p.status)) break;
+            tc_fence_after();
+            const int row = tm * D_BM + 32 * q + lane;
+            const uint32_t ta = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(abuf * D_BN);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(ta + 32 * c, v);
+                tmem_ld_wait();
+                const int col = tn * D_BN + 32 * c;
+                if (row < p.T) {
+                    float* y = p.Y + (int64_t)row * p.ldy + col;
+                    if (vec && col + 32 <= p.N) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            reinterpret_cast<float4*>(y)[j] =
+                                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col + j < p.N) y[j] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty(abuf));
+            if (++abuf == 2) {
+                abuf = 0;
+                aphase ^= 1u;
+            }
+        }
+    } else if (warp == D_LOADER_WARP) {
+        // ------------------------------- packed-word loader -------------------------
+        // Copies each K step's packed words (128 rows x 8*BITS bytes) into the packed ring
+        // with cp.async, completion counted on pfull. The expanding warps then hold no
+        // global load in flight when they fence their shared-memory writes for the
+        // tensor core.
+        int ps = 0;
+        uint32_t pph = 0;
+        bool ok = true;
+        for (int t = t_begin; t < t_end && ok; ++t) {
+            const int tn = t / tiles_m;
+            for (int kt = 0; kt < ktiles; ++kt) {
+                if (!mbar_wait_warp(pempty(ps), pph ^ 1u, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int r = lane + 32 * it;
+                    const int o = tn * D_BN + r;
+                    if (o < p.N) {
+                        const uint32_t dst = smem_u32(pring + ps * D_PBOX + r * 32);
+                        const uint32_t* src = p.packed + (int64_t)o * p.words + 2 * BITS * kt;
+                        if (BITS == 3) {
+                            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+                            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst + 8), "l"(src + 2) : "memory");
+                            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst + 16), "l"(src + 4) : "memory");
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < BITS / 2; ++q)
+                                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16 * q),
+                                             "l"(src + 4 * q)
+                                             : "memory");
+                        }
+                    }
+                }
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(pfull(ps)) : "memory");
+                if (++ps == D_PS) {
+                    ps = 0;
+                    pph ^= 1u;
+                }
+            }
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    } else {
+        // ------------------------------- dequantisers (8 warps) ---------------------
+        // A K step's weight box is 128 rows x 8 chunks of 8 columns. Thread i expands chunk
+        // j = i % 8 of rows r = i / 8 + 32 it (it = 0..3); each chunk is one 16-byte unit of
+        // the swizzled shared-memory image, and its codes are 8*BITS bits of the row's words
+        // in the packed ring.
+        const int i = threadIdx.x - 6 * 32;
+        const int j = i & 7, rb = i >> 3;
+        constexpr int NDQ = 32 * D_DQ_WARPS;
+        auto dq_sync = [] { asm volatile("bar.sync 2, %0;" ::"n"(32 * D_DQ_WARPS) : "memory"); };
+        // g_idx into shared memory once (validated: out-of-range groups read group 0)
+        for (int k = i; k < p.K; k += NDQ) {
+            int g = p.g_idx[k];
+            if (g < 0 || g >= p.G) {
+                set_status(p.status, GPTQ_ERR_INVALID_ARG);
+                g = 0;
+            }
+            g16[k] = (int16_t)g;
+        }
+        dq_sync();
+        // bits of chunk j inside the step's 2*BITS words: [8*BITS*j, 8*BITS*(j+1))
+        constexpr int CB = 8 * BITS;
+        const int w0 = (CB * j) >> 5, sh = (CB * j) & 31;
+        const bool two = (BITS == 3) && (sh + CB > 32);   // the chunk straddles two words
+        int ws = 0, ps = 0, tab_tn = -1;
+        uint32_t wph = 0, pph = 0;
+        bool ok = true;
+        for (int t = t_begin; t < t_end && ok; ++t) {
+            const int tn = t / tiles_m;
+            const float* srow[4];
+            const uint8_t* zrow[4];
+            bool live[4];
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int o = tn * D_BN + rb + 32 * it;
+                live[it] = o < p.N;
+                const int64_t oo = live[it] ? o : 0;
+                srow[it] = p.scales + oo * p.G;
+                zrow[it] = p.zeros + oo * p.G;
+            }
+            if (TAB && tn != tab_tn) {
+                // this tile's scales and zero points, read once, coalesced
+                tab_tn = tn;
+                dq_sync();  // every thread is done with the previous tile's table
+                const int64_t n = (int64_t)D_BN * p.G;
+                for (int64_t idx = i; idx < n; idx += NDQ) {
+                    const int rr = (int)(idx / p.G), g = (int)(idx - (int64_t)rr * p.G);
+                    const int oo = tn * D_BN + rr;
+                    const bool lv = oo < p.N;
+                    s_tab[rr * p.sp + g] = lv ? p.scales[(int64_t)oo * p.G + g] : 0.0f;
+                    z_tab[rr * p.zp + g] = lv ? p.zeros[(int64_t)oo * p.G + g] : (uint8_t)0;
+                }
+                dq_sync();
+            }
+            for (int kt = 0; kt < ktiles; ++kt) {
+                if (!mbar_wait_warp(pfull(ps), pph, abort_flag, p.status) ||
+                    !mbar_wait_warp(wempty(ws), wph ^ 1u, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                // the chunk's 8 codes of each row, least significant first
+                uint32_t v[4];
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const uint32_t* wr = reinterpret_cast<const uint32_t*>(pring + ps * D_PBOX + (rb + 32 * it) * 32);
+                    const uint32_t lo = wr[w0], hi = two ? wr[w0 + 1] : 0u;
+                    v[it] = live[it] ? (two ? __funnelshift_r(lo, hi, sh) : (lo >> sh)) : 0u;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pempty(ps));   // the words are in registers
+                if (++ps == D_PS) {
+                    ps = 0;
+                    pph ^= 1u;
+                }
+                const int k0 = kt * D_BK + 8 * j;
+                const uint4 g8 = *reinterpret_cast<const uint4*>(g16 + k0);   // the chunk's 8 groups
+                const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
+                int gc[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) gc[e] = (int)(int16_t)((gw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+                bool one_group = true;
+#pragma unroll
+                for (int e = 1; e < 8; ++e) one_group = one_group && gc[e] == gc[0];
+                uint8_t* sbox = smem + (D_XS + ws) * D_BOX;
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int r = rb + 32 * it;
+                    float s = 0.0f, zb = 8388608.0f;
+                    auto look = [&](int g) {
+                        if (TAB) {
+                            s = s_tab[r * p.sp + g];
+                            zb = 8388608.0f + (float)z_tab[r * p.zp + g];
+                        } else {
+                            s = live[it] ? srow[it][g] : 0.0f;
+                            zb = 8388608.0f + (live[it] ? (float)zrow[it][g] : 0.0f);
+                        }
+                    };
+                    if (one_group) look(gc[0]);
+                    float wq[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        if (!one_group) look(gc[e]);
+                        const uint32_t u = (v[it] >> (BITS * e)) & ((1u << BITS) - 1u);
+                        // 2^23 + u as a float, minus 2^23 + z: u - z exactly, no conversion
+                        wq[e] = s * (__uint_as_float(0x4B000000u | u) - zb);
+                    }
+                    // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)
+                    *reinterpret_cast<uint4*>(sbox + r * 128 + ((j ^ (r & 7)) << 4)) =
+                        make_uint4(bf16x2(wq[0], wq[1]), bf16x2(wq[2], wq[3]), bf16x2(wq[4], wq[5]),
+                                   bf16x2(wq[6], wq[7]));
+                }
+                fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(wfull(ws));
+                if (++ws == D_WS) {
+                    ws = 0;
+                    wph ^= 1u;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, D_TMEM_COLS);
+    }
+}
+
+}  // namespace
+}  // namespace gptq
+
+using namespace gptq;
+
+extern "C" int gptq_dequant_matmul(const void* X, int64_t T, int64_t K, int64_t ldx, const uint32_t* packed,
+                                   const float* scales, const uint8_t* zeros, const int32_t* g_idx, int64_t N,
+                                   int64_t G, int bits, float* Y, int64_t ldy, void* stream) {
+    if (T < 0 || K < 0 || N < 0) return GPTQ_ERR_INVALID_ARG;
+    if (bits < 2 || bits > 4) return GPTQ_ERR_UNSUPPORTED;
+    if (T == 0 || N == 0) return GPTQ_OK;
+    if (!X || !packed || !scales || !zeros || !g_idx || !Y || G < 1 || ldx < K || ldy < N)
+        return GPTQ_ERR_INVALID_ARG;
+    if (K % D_BK != 0 || K == 0 || ldx % 8 != 0 || (reinterpret_cast<uintptr_t>(X) & 15) ||
+        (reinterpret_cast<uintptr_t>(g_idx) & 15) || T > (1ll << 31) - 1 || N > (1ll << 31) - 1)
+        return GPTQ_ERR_UNSUPPORTED;
+    auto enc = tma_encoder();
+    if (!enc) return GPTQ_ERR_CUDA;
+    CUtensorMap tx;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)T};
+    cuuint64_t strides[1] = {(cuuint64_t)ldx * 2};
+    cuuint32_t box[2] = {(cuuint32_t)D_BK, (cuuint32_t)D_BM};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return GPTQ_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DParams p;
+    p.T = (int)T;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.tiles_n = (int)ceil_div(N, D_BN);
+    p.ntiles = (int)(ceil_div(T, D_BM) * p.tiles_n);
+    p.packed = packed;
+    p.words = gptq_packed_words_per_row(K, bits);
+    p.scales = scales;
+    p.zeros = zeros;
+    p.G = G;
+    p.g_idx = g_idx;
+    p.Y = Y;
+    p.ldy = ldy;
+    // shared memory: stages + barriers, g_idx (int16), and the per-tile scale / zero tables
+    // when they fit (otherwise the expansion reads scales and zeros from global memory)
+    if (G > 32767 || K > 32768) return GPTQ_ERR_UNSUPPORTED;
+    auto up16 = [](int64_t x) { return (x + 15) & ~int64_t(15); };
+    p.g_off = D_RING + 256;
+    p.sp = (int)(G | 1);
+    int zq = (int)((G + 3) / 4);
+    if ((zq & 1) == 0) ++zq;
+    p.zp = 4 * zq;
+    p.s_off = (int)up16(p.g_off + 2 * K);
+    p.z_off = (int)up16(p.s_off + 4ll * D_BN * p.sp);
+    const int64_t with_tab = p.z_off + (int64_t)D_BN * p.zp + 1024;
+    p.tab = with_tab <= D_SMEM_MAX ? 1 : 0;
+    const int smem = (int)(p.tab ? with_tab : up16(p.g_off + 2 * K) + 1024);
+    if (smem > D_SMEM_MAX) return GPTQ_ERR_UNSUPPORTED;
+    int* status = nullptr;
+    GPTQ_CUDA_TRY(cudaMallocAsync(reinterpret_cast<void**>(&status), sizeof(int), s));
+    GPTQ_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
+    p.status = status;
+    const int grid = std::min(p.ntiles, device_sm_count());
+    auto kern = p.tab ? (bits == 2 ? dequant_matmul_kernel<2, true> : bits == 3 ? dequant_matmul_kernel<3, true>
+                                                                    : dequant_matmul_kernel<4, true>)
+                      : (bits == 2 ? dequant_matmul_kernel<2, false> : bits == 3 ? dequant_matmul_kernel<3, false>
+                                                                      : dequant_matmul_kernel<4, false>);
+    GPTQ_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    GPTQ_LAUNCH(K_DEQUANT_MM, s, kern<<<grid, D_THREADS, smem, s>>>(tx, p));
+    GPTQ_LAUNCH_CHECK();
+    int hstatus = 0;
+    GPTQ_CUDA_TRY(cudaMemcpyAsync(&hstatus, status, sizeof(int), cudaMemcpyDeviceToHost, s));
+    GPTQ_CUDA_TRY(cudaFreeAsync(status, s));
+    GPTQ_CUDA_TRY(cudaStreamSynchronize(s));
+    return hstatus;
+}

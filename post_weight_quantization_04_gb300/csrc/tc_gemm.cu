@@ -436,19 +436,7 @@ __global__ void __launch_bounds__(256) split_cols_kernel(const float* __restrict
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
+PFN_cuTensorMapEncodeTiled_v12000 encoder() { return tma_encoder(); }
 
 bool make_map(CUtensorMap* m, const float* base, int rows, int K, int64_t ldk) {
     auto enc = encoder();
@@ -463,6 +451,20 @@ bool make_map(CUtensorMap* m, const float* base, int rows, int K, int64_t ldk) {
 }
 
 }  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tma_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
 
 cudaError_t split_rows(int id, const float* A, int64_t lda, int rows, int K, float* hi, float* lo, int ldk,
                        cudaStream_t s, bool pdl) {

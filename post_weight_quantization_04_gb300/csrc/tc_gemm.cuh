@@ -1,10 +1,15 @@
 // tc_gemm.cuh — fp32-accurate NT GEMM on the tensor cores (3xTF32), and the operand splits.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace gptq {
+
+// cuTensorMapEncodeTiled from the driver (looked up once), or null if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tma_encoder();
 
 // A (rows x K, row stride lda) -> hi, lo (rows x ldk, dense), hi = A with the low 13
 // mantissa bits cleared (exactly representable in TF32), lo = A - hi (exact in fp32).

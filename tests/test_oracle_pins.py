@@ -344,3 +344,54 @@ def test_perm_equivalent():
     keys = np.array([5.0, 3.0, 3.0000001, 1.0])
     assert O.perm_equivalent([0, 2, 1, 3], [0, 1, 2, 3], keys, 1e-6)
     assert not O.perm_equivalent([0, 3, 1, 2], [0, 1, 2, 3], keys, 1e-6)
+
+
+# ------------------------------------------------------------ the stored form and its consumer
+
+def test_unpack_by_hand():
+    # 4-bit: word 0x76543210 holds codes 0..7 least significant nibble first
+    np.testing.assert_array_equal(O.unpack_rows(np.array([[0x76543210]], dtype=np.uint32), 4, 8),
+                                  [[0, 1, 2, 3, 4, 5, 6, 7]])
+    # 3-bit: codes 5, 6, 7, ... ; code 10 straddles words 0 and 1 (stream bits 30..32)
+    u = np.array([[5, 6, 7, 1, 0, 2, 3, 4, 5, 6, 7, 1]])
+    stream = [(int(u[0, c]) >> b) & 1 for c in range(12) for b in range(3)]
+    words = [sum(bit << p for p, bit in enumerate(stream[32 * w:32 * w + 32])) for w in range(2)]
+    np.testing.assert_array_equal(O.unpack_rows(np.array([words], dtype=np.uint32), 3, 12), u)
+
+
+@pytest.mark.parametrize("bits,d", [(2, 64), (3, 100), (4, 33), (3, 96)])
+def test_unpack_inverts_pack(bits, d):
+    rng = np.random.default_rng(bits * 1000 + d)
+    u = rng.integers(0, 2 ** bits, size=(7, d))
+    np.testing.assert_array_equal(O.unpack_rows(O.pack_rows(u, bits), bits, d), u)
+
+
+@pytest.mark.parametrize("bits,group,sym,act", [(4, 128, True, False), (3, 32, False, True), (2, 0, True, True),
+                                                (4, 64, False, False)])
+def test_stored_form_dequantises_to_the_loop_weights(bits, group, sym, act):
+    """The packed codes, scales, zeros and g_idx the layer returns, read back through
+    g_idx, give exactly the dequantised weights of the column loop (in the original
+    column order)."""
+    rng = np.random.default_rng(bits + group)
+    X = rng.standard_normal((400, 256)) * np.exp(rng.standard_normal(256))
+    W = 0.05 * rng.standard_normal((24, 256))
+    out = O.gptq_layer(W, X, bits, group, sym, 0.01, act)
+    G = out["scales"].shape[1]
+    zeros = out["zeros"] if not sym else np.full((24, G), 2 ** (bits - 1))
+    Wq = O.dequant_stored(out["packed"], out["scales"], zeros, out["g_idx"], bits, 256)
+    np.testing.assert_array_equal(Wq, out["Wq"])
+
+
+def test_dequant_matmul_brute_force():
+    rng = np.random.default_rng(5)
+    T, d, o, bits, G = 3, 12, 4, 3, 3
+    u = rng.integers(0, 8, size=(o, d))
+    s = rng.uniform(0.5, 2.0, size=(o, G))
+    z = rng.integers(0, 8, size=(o, G))
+    g = rng.integers(0, G, size=d)
+    X = rng.standard_normal((T, d))
+    Y = O.dequant_matmul(X, O.pack_rows(u, bits), s, z, g, bits)
+    for t in range(T):
+        for r in range(o):
+            want = sum(X[t, k] * s[r, g[k]] * (u[r, k] - z[r, g[k]]) for k in range(d))
+            assert abs(Y[t, r] - want) <= 1e-12 * (1 + abs(want))

@@ -133,6 +133,9 @@ QCASES = [
     (33, 200, 4, 64, False, True),
     (130, 640, 3, 128, True, True),
     (40, 384, 2, 128, False, False),
+    # asymmetric 2- and 3-bit with act_order (the paper's default grid, narrow widths)
+    (72, 256, 2, 128, False, True),
+    (50, 384, 3, 32, False, True),
 ]
 
 
