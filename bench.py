@@ -7,6 +7,7 @@ every weight that shares the layer input. Inputs are seeded synthetic layers.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
   python bench.py --op dequant_matmul [--config C] [--tokens T]   (the stored-form consumer)
+  python bench.py --op layerwise [--mlp mlp4096|toy]             (apply_layerwise on a synthetic MLP)
 
 Prints one JSON line. `value` is milliseconds per layer pass (lower is better),
 device-timed with CUDA events, L2 flushed between steps when the inputs fit in it.
@@ -45,7 +46,8 @@ def parse(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-profile", action="store_true")
-    ap.add_argument("--op", choices=["layer", "dequant_matmul"], default="layer")
+    ap.add_argument("--op", choices=["layer", "dequant_matmul", "layerwise"], default="layer")
+    ap.add_argument("--mlp", default="mlp4096")
     ap.add_argument("--tokens", type=int, default=8192)
     return ap.parse_args(argv)
 
@@ -650,6 +652,50 @@ def run_dequant_matmul(args):
     }), flush=True)
 
 
+def run_layerwise(args):
+    """The layer-wise pipeline on a synthetic MLP: per layer H from the previous quantised
+    layers' bf16 outputs, prepare, quantize, and the forward pass on the stored form. One
+    JSON line: ms per whole-network pass (device time, CUDA events)."""
+    import torch
+    import post_weight_quantization_04_gb300 as lib
+    from post_weight_quantization_04_gb300 import build as B
+    import synth
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    B.build()
+    lib.load()
+    dev = torch.device("cuda", 0)
+    spec = synth.mlp_workload(args.mlp)
+    X = synth.make_x(spec.x, 1234, device=dev)
+    Ws = synth.make_mlp_weights(spec, 1334, device=dev)
+
+    def step():
+        return lib.gptq_layerwise(X, Ws, spec.bits, spec.group, spec.sym, spec.damp, spec.act_order)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n0 = lib.gptq_launch_count()
+    times = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = statistics.mean(times)
+    print(json.dumps({
+        "metric": "layer-wise MLP quantization (ms per network pass)", "value": ms, "unit": "ms",
+        "higher_is_better": False, "steps": args.steps, "n_gpus": 1, "data": "synthetic",
+        "dtype": "bf16 activations, f32 quantisation", "config": {"workload": spec.name, "dims": list(spec.dims),
+                                                                   "tokens": spec.x.n, "bits": spec.bits,
+                                                                   "group": spec.group},
+        "gpu_launches": (lib.gptq_launch_count() - n0) // max(1, args.steps) * args.steps,
+    }), flush=True)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_info()
@@ -664,6 +710,9 @@ def main():
     if args.op == "dequant_matmul":
         if rank == 0:
             run_dequant_matmul(args)
+    elif args.op == "layerwise":
+        if rank == 0:
+            run_layerwise(args)
     elif args.impl == "reference":
         run_reference(args, ws, rank)
     else:

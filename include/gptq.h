@@ -186,14 +186,17 @@ int gptq_pack(const int8_t* codes, int64_t rows, int64_t cols, int bits, int sym
  *   packed  device, uint32, (N, gptq_packed_words_per_row(K, bits))
  *   scales  device, fp32, (N, G); zeros device, uint8, (N, G); g_idx device, int32, (K),
  *           16-byte aligned, values in [0, G) (others record INVALID_ARG and read group 0)
- *   Y       device, fp32, (T, N) row-major, row stride ldy
+ *   flags   GPTQ_DQ_RELU: Y = max(., 0) (the hidden layers of an MLP forward);
+ *           GPTQ_DQ_BF16_OUT: Y is bf16 (rounded to nearest even), else fp32
+ *   Y       device, (T, N) row-major, row stride ldy elements
  * The weights are expanded to bf16 on chip (rounding each to 8 significant bits) and
  * multiplied on the tensor cores with fp32 accumulation. Synchronises the stream and
  * returns the device status. Errors: INVALID_ARG, UNSUPPORTED (bits not 2-4, K % 64,
- * alignment), TIMEOUT, CUDA. */
+ * alignment, K or G too large for the shared-memory plan), TIMEOUT, CUDA. */
+enum { GPTQ_DQ_RELU = 1, GPTQ_DQ_BF16_OUT = 2 };
 int gptq_dequant_matmul(const void* X, int64_t T, int64_t K, int64_t ldx, const uint32_t* packed,
                         const float* scales, const uint8_t* zeros, const int32_t* g_idx, int64_t N,
-                        int64_t G, int bits, float* Y, int64_t ldy, void* stream);
+                        int64_t G, int bits, int flags, void* Y, int64_t ldy, void* stream);
 
 /* Static text for a status code. */
 const char* gptq_status_string(int status);

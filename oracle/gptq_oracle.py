@@ -53,6 +53,7 @@ __all__ = [
     "g_idx_for", "rel_output_error", "rel_output_error_from_xtx", "layer_loss",
     "obs_bruteforce_row", "auto_compute_hessian", "auto_gptq_quantize_row", "auto_dequantize_row",
     "near_half", "perm_equivalent", "TieMismatch", "unpack_rows", "dequant_stored", "dequant_matmul",
+    "round_bf16", "mlp_forward", "apply_layerwise",
 ]
 
 
@@ -401,6 +402,50 @@ def gptq_layer(W, X, bits: int = 4, group: int = 0, sym: bool = True, damp: floa
     out = gptq_quantize(W, U, perm, dead, bits, group, sym, scale_dtype)
     out.update({"U": U, "dead": dead, "H": H})
     return out
+
+
+def round_bf16(a) -> np.ndarray:
+    """Round to the nearest bfloat16 (ties to even), returned as fp64: the activations a
+    bf16 forward pass hands to the next layer."""
+    x = np.asarray(a, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(F64)
+
+
+def mlp_forward(X, Ws, act_round=None):
+    """The MLP of the guide page's simulations: hidden layers relu(h W^T), the last layer
+    linear (no biases: the pages give none). `act_round` rounds every layer output."""
+    h = np.asarray(X, dtype=F64)
+    for i, W in enumerate(Ws):
+        h = h @ np.asarray(W, dtype=F64).T
+        if i < len(Ws) - 1:
+            h = np.maximum(h, 0.0)
+        if act_round is not None:
+            h = act_round(h)
+    return h
+
+
+def apply_layerwise(X, Ws, fn, skip_last: bool = False, act_round=None):
+    """[guide] `apply_layerwise`: run fn(W, layer_input) -> quantised W on every layer in
+    order, each calibrated on the inputs it will actually see — the outputs of the layers
+    before it, already quantised. Returns the quantised weights, the calibration input of
+    every layer and the final output."""
+    h = np.asarray(X, dtype=F64)
+    if act_round is not None:
+        h = act_round(h)
+    Qs, hs = [], []
+    for i, W in enumerate(Ws):
+        hs.append(h)
+        Q = np.asarray(W, dtype=F64) if (skip_last and i == len(Ws) - 1) else fn(W, h)
+        Qs.append(Q)
+        h = h @ Q.T
+        if i < len(Ws) - 1:
+            h = np.maximum(h, 0.0)
+        if act_round is not None:
+            h = act_round(h)
+    return Qs, hs, h
 
 
 def rtn_quantize(W, bits: int, group: int = 0, sym: bool = True, dead=None,

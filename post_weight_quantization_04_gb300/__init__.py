@@ -72,7 +72,7 @@ def _declare(lib: ctypes.CDLL) -> None:
         "rtn_quantize": (_I, [_P, _I64, _I64, _P, QConfig, _P, _P, _P, _P, _P, _P]),
         "gptq_packed_words_per_row": (_I64, [_I64, _I]),
         "gptq_pack": (_I, [_P, _I64, _I64, _I, _I, _P, _P]),
-        "gptq_dequant_matmul": (_I, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _I64, _I64, _I, _P, _I64, _P]),
+        "gptq_dequant_matmul": (_I, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _I64, _I64, _I, _I, _P, _I64, _P]),
         "gptq_status_string": (ctypes.c_char_p, [_I]),
         "gptq_launch_count": (ctypes.c_ulonglong, []),
         "gptq_profile_enable": (None, [_I]),
@@ -294,10 +294,14 @@ def gptq_pack(codes: torch.Tensor, bits: int, sym: bool = True, out: Optional[to
     return p
 
 
+DQ_RELU, DQ_BF16_OUT = 1, 2
+
+
 def gptq_dequant_matmul(X: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
-                        g_idx: torch.Tensor, bits: int, out: Optional[torch.Tensor] = None,
-                        stream=None) -> torch.Tensor:
-    """Y = X Wq^T straight from the stored form (packed codes, scales, zeros, g_idx)."""
+                        g_idx: torch.Tensor, bits: int, out: Optional[torch.Tensor] = None, relu: bool = False,
+                        out_dtype=torch.float32, stream=None) -> torch.Tensor:
+    """Y = X Wq^T (optionally max(., 0)) straight from the stored form (packed codes,
+    scales, zeros, g_idx); Y fp32 or bf16."""
     T, K = X.shape
     N, G = scales.shape
     _dev(X, torch.bfloat16, "X")
@@ -305,12 +309,40 @@ def gptq_dequant_matmul(X: torch.Tensor, packed: torch.Tensor, scales: torch.Ten
     _dev(scales, torch.float32, "scales")
     _dev(zeros, torch.uint8, "zeros", (N, G))
     _dev(g_idx, torch.int32, "g_idx", (K,))
-    Y = out if out is not None else torch.empty(T, N, dtype=torch.float32, device=X.device)
-    _dev(Y, torch.float32, "Y", (T, N))
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out_dtype must be float32 or bfloat16")
+    Y = out if out is not None else torch.empty(T, N, dtype=out_dtype, device=X.device)
+    _dev(Y, out_dtype, "Y", (T, N))
+    flags = (DQ_RELU if relu else 0) | (DQ_BF16_OUT if out_dtype == torch.bfloat16 else 0)
     _check("gptq_dequant_matmul", load().gptq_dequant_matmul(
-        _ptr(X), T, K, K, _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(g_idx), N, G, bits, _ptr(Y), N,
+        _ptr(X), T, K, K, _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(g_idx), N, G, bits, flags, _ptr(Y), N,
         _stream(stream)))
     return Y
+
+
+def gptq_layerwise(X: torch.Tensor, Ws, bits: int = 4, group: int = 0, sym: bool = True, damp: float = 0.01,
+                   act_order: bool = False, stream=None):
+    """GPTQ guide page's `apply_layerwise` on the GPU: every layer is calibrated on the
+    inputs it will actually see — the bf16 outputs of the layers before it, already
+    quantised — and the forward pass runs on the stored form (gptq_dequant_matmul; relu on
+    the hidden layers, bf16 activations, the last layer's output fp32). Returns one dict
+    per layer (its calibration input, H, U, perm, dead and the gptq_quantize outputs) and
+    the network's output. Host orchestration only: every step runs in the library."""
+    h = X
+    layers = []
+    for i, W in enumerate(Ws):
+        last = i == len(Ws) - 1
+        acc = Hessian(h.shape[1], h.device)
+        acc.accumulate(h, stream=stream)
+        H, diag, _ = acc.finalize(stream=stream)
+        acc.close()
+        U, perm, dead = gptq_prepare(H, diag, damp, act_order=act_order, stream=stream)
+        st = gptq_quantize(W, U, perm, dead, bits, group, sym, stream=stream)
+        out = gptq_dequant_matmul(h, st["packed"], st["scales"], st["zeros"], st["g_idx"], bits, relu=not last,
+                                  out_dtype=torch.float32 if last else torch.bfloat16, stream=stream)
+        layers.append({"input": h, "H": H, "U": U, "perm": perm, "dead": dead, **st})
+        h = out
+    return layers, h
 
 
 def gptq_status_string(status: int) -> str:
@@ -341,6 +373,6 @@ __all__ = [
     "load", "Hessian", "GptqError", "QConfig", "qconfig", "gptq_hessian_create", "gptq_hessian_accumulate",
     "gptq_hessian_finalize", "gptq_prepare", "gptq_prepare_workspace_bytes", "gptq_quantize",
     "gptq_quantize_workspace_bytes", "rtn_quantize", "gptq_pack", "gptq_packed_words_per_row",
-    "gptq_dequant_matmul", "gptq_status_string", "gptq_launch_count", "gptq_profile_enable", "gptq_profile_read",
+    "gptq_dequant_matmul", "gptq_layerwise", "gptq_status_string", "gptq_launch_count", "gptq_profile_enable", "gptq_profile_read",
     "EXPORTS", "LIB_PATH",
 ]

@@ -57,8 +57,9 @@ struct DParams {
     const uint8_t* zeros;
     int64_t G;
     const int32_t* g_idx;
-    float* Y;
+    void* Y;          // fp32, or bf16 with GPTQ_DQ_BF16_OUT
     int64_t ldy;
+    int relu, bf16_out;
     int* status;
     // shared-memory layout after the stages and barriers: g_idx as int16 (K entries), then
     // (when tab) the tile's scales (128 x sp floats) and zero points (128 x zp bytes); sp
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(D_THREADS, 1) dequant_matmul_kernel(const __gr
         const int q = warp & 3;
         int abuf = 0;
         uint32_t aphase = 0;
-        const bool vec = ((p.ldy & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.Y) & 15) == 0);
+        const bool vec = ((p.ldy & 7) == 0) && ((reinterpret_cast<uintptr_t>(p.Y) & 15) == 0);
         for (int t = t_begin; t < t_end; ++t) {
             const int tm = t % tiles_m, tn = t / tiles_m;
             if (!mbar_wait_warp(tfull(abuf), aphase, abort_flag, p.status)) break;
@@ -236,18 +237,32 @@ __global__ void __launch_bounds__(D_THREADS, 1) dequant_matmul_kernel(const __gr
                 tmem_ld_32x32b_x32(ta + 32 * c, v);
                 tmem_ld_wait();
                 const int col = tn * D_BN + 32 * c;
-                if (row < p.T) {
-                    float* y = p.Y + (int64_t)row * p.ldy + col;
+                float f[32];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) f[jj] = p.relu ? fmaxf(__uint_as_float(v[jj]), 0.0f) : __uint_as_float(v[jj]);
+                if (row < p.T && p.bf16_out) {
+                    __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.Y) + (int64_t)row * p.ldy + col;
                     if (vec && col + 32 <= p.N) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            reinterpret_cast<float4*>(y)[j] =
-                                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                        for (int jj = 0; jj < 4; ++jj)
+                            reinterpret_cast<uint4*>(y)[jj] =
+                                make_uint4(bf16x2(f[8 * jj], f[8 * jj + 1]), bf16x2(f[8 * jj + 2], f[8 * jj + 3]),
+                                           bf16x2(f[8 * jj + 4], f[8 * jj + 5]), bf16x2(f[8 * jj + 6], f[8 * jj + 7]));
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col + j < p.N) y[j] = __uint_as_float(v[j]);
+                        for (int jj = 0; jj < 32; ++jj)
+                            if (col + jj < p.N) y[jj] = __float2bfloat16_rn(f[jj]);
+                    }
+                } else if (row < p.T) {
+                    float* y = reinterpret_cast<float*>(p.Y) + (int64_t)row * p.ldy + col;
+                    if (vec && col + 32 <= p.N) {
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj)
+                            reinterpret_cast<float4*>(y)[jj] = make_float4(f[4 * jj], f[4 * jj + 1], f[4 * jj + 2], f[4 * jj + 3]);
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj)
+                            if (col + jj < p.N) y[jj] = f[jj];
                     }
                 }
             }
@@ -441,11 +456,12 @@ using namespace gptq;
 
 extern "C" int gptq_dequant_matmul(const void* X, int64_t T, int64_t K, int64_t ldx, const uint32_t* packed,
                                    const float* scales, const uint8_t* zeros, const int32_t* g_idx, int64_t N,
-                                   int64_t G, int bits, float* Y, int64_t ldy, void* stream) {
+                                   int64_t G, int bits, int flags, void* Y, int64_t ldy, void* stream) {
     if (T < 0 || K < 0 || N < 0) return GPTQ_ERR_INVALID_ARG;
     if (bits < 2 || bits > 4) return GPTQ_ERR_UNSUPPORTED;
     if (T == 0 || N == 0) return GPTQ_OK;
-    if (!X || !packed || !scales || !zeros || !g_idx || !Y || G < 1 || ldx < K || ldy < N)
+    if (!X || !packed || !scales || !zeros || !g_idx || !Y || G < 1 || ldx < K || ldy < N ||
+        (flags & ~(GPTQ_DQ_RELU | GPTQ_DQ_BF16_OUT)))
         return GPTQ_ERR_INVALID_ARG;
     if (K % D_BK != 0 || K == 0 || ldx % 8 != 0 || (reinterpret_cast<uintptr_t>(X) & 15) ||
         (reinterpret_cast<uintptr_t>(g_idx) & 15) || T > (1ll << 31) - 1 || N > (1ll << 31) - 1)
@@ -476,6 +492,8 @@ extern "C" int gptq_dequant_matmul(const void* X, int64_t T, int64_t K, int64_t 
     p.g_idx = g_idx;
     p.Y = Y;
     p.ldy = ldy;
+    p.relu = (flags & GPTQ_DQ_RELU) ? 1 : 0;
+    p.bf16_out = (flags & GPTQ_DQ_BF16_OUT) ? 1 : 0;
     // shared memory: stages + barriers, g_idx (int16), and the per-tile scale / zero tables
     // when they fit (otherwise the expansion reads scales and zeros from global memory)
     if (G > 32767 || K > 32768) return GPTQ_ERR_UNSUPPORTED;

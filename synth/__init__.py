@@ -260,3 +260,40 @@ __all__ = [
     "make_x_rows", "iter_segments", "channel_scales", "dead_channels", "seeds", "weight_seed",
     "x_seed", "to_numpy_f64",
 ]
+
+
+# ------------------------------------------------------------ layer-wise MLP workloads
+
+@dataclasses.dataclass(frozen=True)
+class MLPSpec:
+    """A synthetic MLP for the layer-wise pipeline: inputs X (n, dims[0]) and weights
+    W_i (dims[i+1], dims[i]) ~ N(0, 1/dims[i]); hidden layers relu, last layer linear."""
+    name: str
+    dims: Sequence[int]
+    x: XSpec
+    bits: int
+    group: int
+    sym: bool
+    act_order: bool = False
+    damp: float = 0.01
+
+
+def mlp_workload(name: str) -> MLPSpec:
+    """'toy': the guide page's simulation scale (three 256-wide hidden layers, 512
+    calibration inputs; the 12-feature input widened to 128 so every width is a multiple
+    of 64), 3-bit symmetric per-row. 'mlp4096': three 4096-wide layers on 8192 tokens,
+    4-bit symmetric, group 128."""
+    if name == "toy":
+        return MLPSpec("toy-128-256-256-256-x512-3b-sym-row", (128, 256, 256, 256),
+                       XSpec(n=512, d=128, kind="correlated", dtype="bf16", segment=512), 3, 0, True)
+    if name == "mlp4096":
+        return MLPSpec("mlp-4096x3-x8192-4b-sym-g128", (4096, 4096, 4096, 4096),
+                       XSpec(n=8192, d=4096, kind="scaled", dtype="bf16", n_outliers=16, outlier_factor=50.0,
+                             segment=2048), 4, 128, True)
+    raise ValueError(name)
+
+
+def make_mlp_weights(spec: MLPSpec, seed: int, device="cpu"):
+    return [make_weight(spec.dims[i + 1], spec.dims[i], 1.0 / math.sqrt(spec.dims[i]), seed + 17 * i, device)
+            for i in range(len(spec.dims) - 1)]
+
