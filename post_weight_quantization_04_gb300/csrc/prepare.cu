@@ -709,7 +709,9 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
                 l21.ld = NB;
                 l21.mode = 1;
                 l21.pdl = true;
-                GPTQ_CUDA_TRY(split_rows(K_SPLIT, P, d, (int)m, n, w.ahi, w.alo, NB, cs, true));
+                // the panel's split: for panel 0 here; for the others it was written by the
+                // previous panel's SYRK of these columns (its rows below the diagonal block)
+                if (kb == 0) GPTQ_CUDA_TRY(split_rows(K_SPLIT, P, d, (int)m, n, w.ahi, w.alo, NB, cs, true));
                 GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, n, n, 1.0f, w.ahi, w.alo, lhi, llo, NB, 0.0f, P, d,
                                          false, w.status, cs, l21));
                 GPTQ_CUDA_TRY(record(two ? conc->trsm : nullptr, cs));
@@ -720,6 +722,11 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
                 }
                 GemmOpts strip = chain_opts;
                 strip.pdl = cs_k;
+                strip.hi = w.ahi;   // rows below the next diagonal block = the next panel, split
+                strip.lo = w.alo;
+                strip.ld = NB;
+                strip.mode = 1;
+                strip.row0 = nn;
                 GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, nn, n, -1.0f, phi, plo, phi, plo, NB, 1.0f,
                                          w.A + (k0 + n) * d + k0 + n, d, true, w.status, cs, strip));
                 cs_k = true;

@@ -52,6 +52,8 @@ struct GParams {
     float* olo;
     int64_t old_;
     int omode;
+    int orow0;
+    int ovec;   // row-major split rows are 16-byte aligned
 };
 
 __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -319,15 +321,26 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                         o.w = fmaf(p.beta, cv.w, o.w);
                     }
                     *ptr = o;
-                    if (p.omode && row < p.M) {
+                    const int gc0 = tn * G_BN + 32 * c + 4 * j;
+                    if (p.omode == 1 && row < p.M && row >= p.orow0 && gc0 + 3 < p.N && p.ovec) {
+                        // row-major split, four columns at once (16-byte stores)
+                        float4 h4;
+                        h4.x = __uint_as_float(__float_as_uint(o.x) & 0xFFFFE000u);
+                        h4.y = __uint_as_float(__float_as_uint(o.y) & 0xFFFFE000u);
+                        h4.z = __uint_as_float(__float_as_uint(o.z) & 0xFFFFE000u);
+                        h4.w = __uint_as_float(__float_as_uint(o.w) & 0xFFFFE000u);
+                        const int64_t at = (int64_t)(row - p.orow0) * p.old_ + gc0;
+                        *reinterpret_cast<float4*>(p.ohi + at) = h4;
+                        *reinterpret_cast<float4*>(p.olo + at) = make_float4(o.x - h4.x, o.y - h4.y, o.z - h4.z, o.w - h4.w);
+                    } else if (p.omode && row < p.M && row >= p.orow0) {
                         const float o4[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int gc = tn * G_BN + 32 * c + 4 * j + e;
                             if (gc < p.N) {
                                 const float h = __uint_as_float(__float_as_uint(o4[e]) & 0xFFFFE000u);
-                                const int64_t at = (p.omode == 1) ? (int64_t)row * p.old_ + gc
-                                                                  : (int64_t)gc * p.old_ + row;
+                                const int64_t orow = row - p.orow0;
+                                const int64_t at = (p.omode == 1) ? orow * p.old_ + gc : (int64_t)gc * p.old_ + orow;
                                 p.ohi[at] = h;
                                 p.olo[at] = o4[e] - h;
                             }
@@ -536,6 +549,9 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
     p.olo = out.lo;
     p.old_ = out.ld;
     p.omode = out.hi ? out.mode : 0;
+    p.orow0 = (int)out.row0;
+    p.ovec = (out.hi && (out.ld % 4 == 0) &&
+              ((reinterpret_cast<uintptr_t>(out.hi) | reinterpret_cast<uintptr_t>(out.lo)) % 16 == 0)) ? 1 : 0;
     if (p.ntiles == 0) return cudaSuccess;
     static const int sms = device_sm_count();
     const int grid = std::min(p.ntiles, out.max_ctas > 0 ? std::min(out.max_ctas, sms) : sms);
