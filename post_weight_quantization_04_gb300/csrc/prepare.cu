@@ -89,7 +89,7 @@ PrepWs carve(void* base, int64_t d) {
 }
 
 // dead[j] = (H[j][j] == 0); the dead diagonal becomes 1; mean of the fixed diagonal in
-// fp64; damped diagonal and its inverse square root.
+// fp64; damped diagonal (rounded to fp32) and its inverse square root in fp32.
 __global__ void __launch_bounds__(1024) prep_diag_kernel(const float* __restrict__ H, int64_t d, float damp,
                                                         uint8_t* __restrict__ dead, float* __restrict__ ddiag,
                                                         float* __restrict__ rr) {
@@ -113,9 +113,9 @@ __global__ void __launch_bounds__(1024) prep_diag_kernel(const float* __restrict
     const double add = (double)damp * (part[0] / (double)d);
     for (int64_t j = threadIdx.x; j < d; j += blockDim.x) {
         const float h = H[j * d + j];
-        const double hd = (h == 0.0f ? 1.0 : (double)h) + add;
-        ddiag[j] = (float)hd;
-        rr[j] = (float)(1.0 / sqrt(hd));
+        const float hd = (float)((h == 0.0f ? 1.0 : (double)h) + add);
+        ddiag[j] = hd;
+        rr[j] = 1.0f / sqrtf(hd);   // fp32 (correctly rounded sqrt and divide)
     }
 }
 
@@ -639,8 +639,10 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
     const bool tc = (d % 4 == 0) && tc_gemm_nt_ok(w.A, d);
 
     const int64_t nblk = ceil_div(d, NB);
-    GPTQ_LAUNCH(K_EYE, s, eye_kernel<<<(unsigned)ceil_div(d * d, 256), 256, 0, s>>>(w.Binv, d));
-    GPTQ_LAUNCH_CHECK();
+    if (!tc || !conc) {
+        GPTQ_LAUNCH(K_EYE, s, eye_kernel<<<(unsigned)ceil_div(d * d, 256), 256, 0, s>>>(w.Binv, d));
+        GPTQ_LAUNCH_CHECK();
+    }
     if (tc) {
         // Blocked right-looking Cholesky of A (lower) with the block-row inverse step of
         // L^-1 interleaved, in two streams. The critical chain (stream `cs`) is
@@ -663,6 +665,9 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
             GPTQ_CUDA_TRY(record(conc->fork, s));
             GPTQ_CUDA_TRY(wait(cs, conc->fork));
             GPTQ_CUDA_TRY(wait(ss, conc->fork));
+            // B = I (the right-hand side of L X = I) is first read by the side stream
+            GPTQ_LAUNCH(K_EYE, ss, eye_kernel<<<(unsigned)ceil_div(d * d, 256), 256, 0, ss>>>(w.Binv, d));
+            GPTQ_LAUNCH_CHECK();
         }
         // the SMs are split between the streams: persistent CTAs of one stream would
         // otherwise hold SMs that the other's next kernel waits for

@@ -14,6 +14,13 @@
 //                          from the updated weights; Err[:, blk] kept for the update below
 //     trailing update      W[:, j0+128:] -= Err * U[blk, j0+128:]   (fp32 GEMM)
 //
+// On the tensor-core path the trailing update is applied in two levels: blocks are grouped
+// four at a time into super-blocks; after a block only the rest of its super-block is
+// updated, and at the end of a super-block the columns past it are updated with the
+// errors of all four blocks in one K = 512 product. The sum is the same (each column
+// still receives every earlier block's correction before its own block runs); the large
+// trailing matrix is read and written a quarter as often.
+//
 // The working copy of W lives in the caller's workspace, permuted into loop order with
 // dead columns zeroed (guide page, "Source code": W[:, dead] = 0, W = W[:, perm]).
 // Outputs go straight to the original column order.
@@ -29,13 +36,14 @@ namespace gptq {
 namespace {
 
 constexpr int QB = 128;  // column block width
+constexpr int SB = 4;    // blocks per super-block of the deferred trailing update
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct QuantWs {
     float* W;       // rows x cols working copy (loop order)
     float* Err;     // rows x QB
-    float* ehi;     // rows x QB: TF32 split of Err
+    float* ehi;     // rows x SB*QB: TF32 split of Err for the blocks of one super-block
     float* elo;
     float* uhi;     // cols x cols: TF32 split of U^T
     float* ulo;
@@ -57,8 +65,8 @@ QuantWs carve(void* base, int64_t rows, int64_t cols) {
     };
     w.W = reinterpret_cast<float*>(take(sizeof(float) * rows * cols));
     w.Err = reinterpret_cast<float*>(take(sizeof(float) * rows * QB));
-    w.ehi = reinterpret_cast<float*>(take(sizeof(float) * rows * QB));
-    w.elo = reinterpret_cast<float*>(take(sizeof(float) * rows * QB));
+    w.ehi = reinterpret_cast<float*>(take(sizeof(float) * rows * SB * QB));
+    w.elo = reinterpret_cast<float*>(take(sizeof(float) * rows * SB * QB));
     w.uhi = reinterpret_cast<float*>(take(sizeof(float) * cols * cols));
     w.ulo = reinterpret_cast<float*>(take(sizeof(float) * cols * cols));
     w.cur_s = reinterpret_cast<float*>(take(sizeof(float) * rows));
@@ -72,12 +80,39 @@ QuantWs carve(void* base, int64_t rows, int64_t cols) {
 bool group_ok(int group) { return group == 0 || (group > 0 && (group % QB == 0 || QB % group == 0)); }
 
 // Wk[r][k] = dead[perm[k]] ? 0 : W[r][perm[k]]
-__global__ void init_work_kernel(const float* __restrict__ W, int64_t rows, int64_t cols, const int32_t* __restrict__ perm,
-                                 const uint8_t* __restrict__ dead, float* __restrict__ Wk) {
-    const int64_t r = blockIdx.y;
-    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < cols; k += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t c = perm ? perm[k] : k;
-        Wk[r * cols + k] = (dead && dead[c]) ? 0.0f : W[r * cols + c];
+// Four consecutive loop columns per thread (one 16-byte store when cols % 4 == 0), IW_ROWS
+// rows per CTA so the permutation and dead flags are read once for several rows.
+constexpr int IW_ROWS = 4;
+__global__ void __launch_bounds__(256) init_work_kernel(const float* __restrict__ W, int64_t rows, int64_t cols,
+                                                        const int32_t* __restrict__ perm,
+                                                        const uint8_t* __restrict__ dead, float* __restrict__ Wk) {
+    const int64_t k0 = 4 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x);
+    if (k0 >= cols) return;
+    const int nk = cols - k0 < 4 ? (int)(cols - k0) : 4;
+    int64_t c[4];
+    bool z[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int64_t k = k0 + (e < nk ? e : 0);
+        c[e] = perm ? (int64_t)perm[k] : k;
+        z[e] = dead && dead[c[e]];
+    }
+    const bool vec = (cols & 3) == 0;
+    const int64_t r0 = (int64_t)blockIdx.y * IW_ROWS;
+#pragma unroll
+    for (int u = 0; u < IW_ROWS; ++u) {
+        const int64_t r = r0 + u;
+        if (r >= rows) break;
+        const float* src = W + r * cols;
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = z[e] ? 0.0f : src[c[e]];
+        float* dst = Wk + r * cols + k0;
+        if (vec) {
+            *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+            for (int e = 0; e < nk; ++e) dst[e] = v[e];
+        }
     }
 }
 
@@ -122,8 +157,9 @@ struct BlockArgs {
     const float* cur_s;
     const float* cur_z;
     float* Err;
-    float* ehi;  // optional TF32 split of Err (rows x QB)
+    float* ehi;  // optional TF32 split of Err (rows x QB, row stride eld)
     float* elo;
+    int64_t eld;
     int8_t* codes;
     float* Wq;
     const int32_t* perm;
@@ -359,8 +395,8 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
             l.y = er[4 * m + 1] - h.y;
             l.z = er[4 * m + 2] - h.z;
             l.w = er[4 * m + 3] - h.w;
-            *reinterpret_cast<float4*>(a.ehi + row * QB + c0) = h;
-            *reinterpret_cast<float4*>(a.elo + row * QB + c0) = l;
+            *reinterpret_cast<float4*>(a.ehi + row * a.eld + c0) = h;
+            *reinterpret_cast<float4*>(a.elo + row * a.eld + c0) = l;
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -536,7 +572,7 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
     GPTQ_CUDA_TRY(cudaMemsetAsync(loss, 0, sizeof(float) * rows, s));
     GPTQ_CUDA_TRY(cudaMemsetAsync(w.status, 0, sizeof(int), s));
     {
-        dim3 grid((unsigned)std::min<int64_t>(ceil_div(cols, 256), 64), (unsigned)rows);
+        dim3 grid((unsigned)ceil_div(cols, 4 * 256), (unsigned)ceil_div(rows, IW_ROWS));
         GPTQ_LAUNCH(K_INIT_WORK, s, init_work_kernel<<<grid, 256, 0, s>>>(W, rows, cols, perm, dead, w.W));
         GPTQ_LAUNCH_CHECK();
     }
@@ -582,8 +618,7 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
     a.cur_s = w.cur_s;
     a.cur_z = w.cur_z;
     a.Err = w.Err;
-    a.ehi = tc ? w.ehi : nullptr;
-    a.elo = tc ? w.elo : nullptr;
+    a.eld = SB * QB;
     a.codes = codes;
     a.Wq = Wq;
     a.perm = perm;
@@ -603,6 +638,10 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         }
         a.j0 = j0;
         a.bw = bw;
+        // this block's errors go to its slot of the super-block's split
+        const int64_t sb0 = j0 / (SB * QB) * (SB * QB), sb_end = std::min<int64_t>(cols, sb0 + SB * QB);
+        a.ehi = tc ? w.ehi + (j0 - sb0) : nullptr;
+        a.elo = tc ? w.elo + (j0 - sb0) : nullptr;
         cudaError_t le = cudaSuccess;
         GPTQ_LAUNCH(K_BLOCK, s, le = launch_pdl(kblock, dim3(bgrid), dim3(128), smem, s, a));
         GPTQ_CUDA_TRY(le);
@@ -610,13 +649,23 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         const int64_t e = j0 + bw;
         if (e < cols) {
             if (tc) {
-                // W[:, e:] -= Err * U[blk, e:] = Err * (U^T[e:, blk])^T on the tensor cores
+                // W[:, e:] -= Err * U[blk, e:] = Err * (U^T[e:, blk])^T on the tensor cores,
+                // deferred for the columns past the super-block: inside it only the block's
+                // own super-block columns are updated (K = 128); at its end the columns past
+                // it take the errors of all its blocks at once (K = SB * 128), so the large
+                // trailing matrix is read and written once per SB blocks.
                 GemmOpts o;
                 o.ldb = cols;
                 o.pdl = true;
-                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_TRAIL, (int)rows, (int)(cols - e), bw, -1.0f, w.ehi, w.elo,
-                                         w.uhi + e * cols + j0, w.ulo + e * cols + j0, QB, 1.0f, w.W + e, cols, false,
-                                         w.status, s, o));
+                if (e < sb_end) {
+                    GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_TRAIL, (int)rows, (int)(sb_end - e), bw, -1.0f, w.ehi + (j0 - sb0),
+                                             w.elo + (j0 - sb0), w.uhi + e * cols + j0, w.ulo + e * cols + j0, SB * QB,
+                                             1.0f, w.W + e, cols, false, w.status, s, o));
+                } else {
+                    GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_TRAIL, (int)rows, (int)(cols - e), (int)(e - sb0), -1.0f, w.ehi,
+                                             w.elo, w.uhi + e * cols + sb0, w.ulo + e * cols + sb0, SB * QB, 1.0f,
+                                             w.W + e, cols, false, w.status, s, o));
+                }
             } else {
                 GPTQ_CUDA_TRY(sgemm(K_SGEMM_TRAIL, false, (int)rows, (int)(cols - e), bw, -1.0f, w.Err, QB,
                                     U + j0 * cols + e, cols, 1.0f, w.W + e, cols, false, s));
