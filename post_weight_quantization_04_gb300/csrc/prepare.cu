@@ -18,8 +18,10 @@
 //   A     d*d fp32   reversed, equilibrated Hp -> L (lower triangle)
 //   Binv  d*d fp32   identity -> L^-1 (lower triangle)
 //   LinvD nblk*NB*NB fp32  inverses of L's diagonal blocks
-//   TF32 hi/lo splits of the GEMM operands (d x NB; the solved panel and L_kk^-1 twice,
-//   for even and odd panels, so the next panel can start while the last is still read)
+//   TF32 hi/lo splits of the GEMM operands: the panel before its solve and B_k (d x NB);
+//   L_kk^-1 twice (even / odd panels); the solved panels L21 of a super-panel (d x SPW,
+//   twice: even / odd super-panels) and its block rows of L^-1 (d x SPW), so the next
+//   panel can start while the side stream still reads the last ones
 //   ddiag d fp32, rr d fp32 (1/sqrt(ddiag)), status int
 #include <math.h>
 
@@ -35,6 +37,11 @@ namespace gptq {
 namespace {
 
 constexpr int NB = 128;  // panel width of the blocked factorisation
+// Panels per super-panel: from kDeferMinD on, the side stream's large rank updates are
+// deferred to the end of each super-panel of kSP panels and applied with K = kSP * NB.
+constexpr int kSP = 4;
+constexpr int64_t kDeferMinD = 2048;
+constexpr int64_t prep_spw(int64_t d) { return (d >= kDeferMinD ? kSP : 1) * (int64_t)NB; }
 
 struct PrepWs {
     float* A;
@@ -44,9 +51,9 @@ struct PrepWs {
     float* alo;
     float* bhi;   //   the block row of the inverse (transposed),
     float* blo;
-    float* phi;   //   L21 (the solved panel), two buffers (even / odd panels),
-    float* plo;
-    float* xhi;   //   the new block row of L^-1 (transposed),
+    float* phi;   //   L21 of the panels of a super-panel (d x SPW), two buffers
+    float* plo;   //   (even / odd super-panels),
+    float* xhi;   //   the super-panel's block rows of L^-1, transposed (d x SPW),
     float* xlo;
     float* lhi;   // NB x NB: L_kk^-1, two buffers (even / odd panels)
     float* llo;
@@ -63,7 +70,8 @@ constexpr int kPrepSlabs = 16;
 constexpr size_t prep_slab(int64_t d, int i) {
     return i < 2 ? sizeof(float) * d * d
          : i == 2 ? sizeof(float) * ((d + NB - 1) / NB) * NB * NB
-         : (i == 7 || i == 8) ? sizeof(float) * 2 * d * NB
+         : (i == 7 || i == 8) ? sizeof(float) * 2 * d * prep_spw(d)
+         : (i == 9 || i == 10) ? sizeof(float) * d * prep_spw(d)
          : i < 11 ? sizeof(float) * d * NB
          : i < 13 ? sizeof(float) * 2 * NB * NB
          : i < 15 ? sizeof(float) * d
@@ -581,8 +589,8 @@ struct PrepConcurrency {
     std::mutex mu;
     bool ready = false;
     cudaStream_t crit = nullptr, side = nullptr;
-    cudaEvent_t fork = nullptr, trsm = nullptr, rest = nullptr, side_done[2] = {nullptr, nullptr},
-                join_side = nullptr, join_crit = nullptr;
+    cudaEvent_t fork = nullptr, trsm = nullptr, rest = nullptr, rest_far = nullptr, side_done[2] = {nullptr, nullptr},
+                far_done[2] = {nullptr, nullptr}, join_side = nullptr, join_crit = nullptr;
 };
 PrepConcurrency g_conc[kMaxPrepDevices];
 
@@ -592,7 +600,8 @@ cudaError_t conc_init(PrepConcurrency& c) {
     cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.crit, cudaStreamNonBlocking, greatest);
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.side, cudaStreamNonBlocking, least);
-    cudaEvent_t* evs[] = {&c.fork, &c.trsm, &c.rest, &c.side_done[0], &c.side_done[1], &c.join_side, &c.join_crit};
+    cudaEvent_t* evs[] = {&c.fork,          &c.trsm,        &c.rest,        &c.rest_far,  &c.side_done[0],
+                          &c.side_done[1], &c.far_done[0], &c.far_done[1], &c.join_side, &c.join_crit};
     for (cudaEvent_t* ev : evs)
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e == cudaSuccess) c.ready = true;
@@ -681,18 +690,41 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
             if (st == cs) cs_k = false;
             if (st == ss) ss_k = false;
         };
+        // Super-panels. L21 of each panel is split into column block j (= its index in the
+        // super-panel) of the super-panel's buffer phi/plo (row stride SPW; buffer row
+        // r = global row - (sp0 + NB), so panel j's L21 starts at row NB * j), and each
+        // block row X_k of L^-1 into column block j of xhi/xlo (transposed, row stride SPW).
+        // Inside a super-panel the side stream updates only the super-panel's own columns
+        // (of A and of B = L^-1's right-hand side); at its end it updates everything past
+        // it with the errors of all its panels at once (K = SPW). With SPW = NB this is the
+        // plain one-panel-at-a-time schedule.
+        const int64_t SPW = prep_spw(d);
+        const int SP = (int)(SPW / NB);
         for (int64_t kb = 0; kb < nblk; ++kb) {
             const int64_t k0 = kb * NB;
             const int n = (int)std::min<int64_t>(NB, d - k0);
             const int64_t m = d - k0 - n, ncols = k0 + n;
             const int nn = (int)std::min<int64_t>(NB, m);  // width of the next panel
             const int par = (int)(kb & 1);
+            const int64_t sp = kb / SP, j = kb % SP;
+            const int64_t sp0 = sp * SPW, sp_end = std::min<int64_t>(d, sp0 + SPW);
+            const bool sp_last = (k0 + n == sp_end);   // last panel of its super-panel
+            const int spar = (int)(sp & 1);
             float* lhi = w.lhi + par * NB * NB;
             float* llo = w.llo + par * NB * NB;
-            float* phi = w.phi + par * d * NB;
-            float* plo = w.plo + par * d * NB;
-            if (two && kb >= 2) {
+            float* shi = w.phi + spar * d * SPW;   // this super-panel's L21 splits
+            float* slo = w.plo + spar * d * SPW;
+            float* Lhi = shi + (NB * j) * SPW + NB * j;   // this panel's L21 split (m x n)
+            float* Llo = slo + (NB * j) * SPW + NB * j;
+            // rows at or below sp_end of all the super-panel's L21 (the deferred updates' operand)
+            float* Ehi = shi + (SPW - NB) * SPW;
+            float* Elo = slo + (SPW - NB) * SPW;
+            if (two && kb >= 2) {   // L_kk^-1 buffer par: read by the side stream's panel kb-2
                 GPTQ_CUDA_TRY(wait(cs, conc->side_done[par]));
+                waited(cs);
+            }
+            if (two && j == 0 && sp >= 2) {   // super-panel buffer spar: read up to the end of sp-2
+                GPTQ_CUDA_TRY(wait(cs, conc->far_done[spar]));
                 waited(cs);
             }
             if (cs_k) {
@@ -708,10 +740,10 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
             cs_k = true;
             float* P = w.A + (k0 + n) * d + k0;
             if (m > 0) {
-                GemmOpts l21 = chain_opts;  // L21 split for the trailing update and the inverse step
-                l21.hi = phi;
-                l21.lo = plo;
-                l21.ld = NB;
+                GemmOpts l21 = chain_opts;  // L21 split for the trailing updates and the inverse step
+                l21.hi = Lhi;
+                l21.lo = Llo;
+                l21.ld = SPW;
                 l21.mode = 1;
                 l21.pdl = true;
                 // the panel's split: for panel 0 here; for the others it was written by the
@@ -720,9 +752,12 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
                 GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, n, n, 1.0f, w.ahi, w.alo, lhi, llo, NB, 0.0f, P, d,
                                          false, w.status, cs, l21));
                 GPTQ_CUDA_TRY(record(two ? conc->trsm : nullptr, cs));
-                // the next panel's columns; the side stream's SYRK of panel k-1 wrote them too
-                if (two && kb >= 1) {
-                    GPTQ_CUDA_TRY(wait(cs, conc->rest));
+                // the next panel's columns; the side stream's updates wrote them too: inside
+                // a super-panel the previous panel's update of the super-panel's columns (or
+                // the first part of the previous super-panel's deferred update), for the first
+                // panel of the next super-panel the second part of that deferred update
+                if (two && kb >= 1 && (!sp_last || sp >= 1)) {
+                    GPTQ_CUDA_TRY(wait(cs, sp_last ? conc->rest_far : conc->rest));
                     waited(cs);
                 }
                 GemmOpts strip = chain_opts;
@@ -732,44 +767,75 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
                 strip.ld = NB;
                 strip.mode = 1;
                 strip.row0 = nn;
-                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, nn, n, -1.0f, phi, plo, phi, plo, NB, 1.0f,
+                // inside the super-panel: this panel's L21 (K = n); at its end the next panel
+                // starts a new super-panel and takes all of this one's panels (K = SPW)
+                const int ks = sp_last ? (int)SPW : n;
+                const float* sh = sp_last ? Ehi : Lhi;
+                const float* sl = sp_last ? Elo : Llo;
+                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, nn, ks, -1.0f, sh, sl, sh, sl, (int)SPW, 1.0f,
                                          w.A + (k0 + n) * d + k0 + n, d, true, w.status, cs, strip));
                 cs_k = true;
-                GPTQ_CUDA_TRY(wait(ss, two ? conc->trsm : nullptr));
-                waited(ss);
-                if (m > nn) {
-                    const int64_t off = (int64_t)nn * NB;
-                    GemmOpts rest = side_opts;
-                    rest.pdl = ss_k;
-                    GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)(m - nn), (int)(m - nn), n, -1.0f, phi + off, plo + off,
-                                             phi + off, plo + off, NB, 1.0f, w.A + (k0 + n + nn) * (d + 1), d, true,
-                                             w.status, ss, rest));
-                    ss_k = true;
-                }
-                GPTQ_CUDA_TRY(record(two ? conc->rest : nullptr, ss));
             } else {
                 GPTQ_CUDA_TRY(record(two ? conc->trsm : nullptr, cs));
-                GPTQ_CUDA_TRY(wait(ss, two ? conc->trsm : nullptr));
-                waited(ss);
             }
+            GPTQ_CUDA_TRY(wait(ss, two ? conc->trsm : nullptr));
+            waited(ss);
+            auto side_gemm = [&](int M, int N, int K, const float* ah, const float* al, const float* bh,
+                                 const float* bl, float* C, bool lower) -> cudaError_t {
+                if (M <= 0 || N <= 0) return cudaSuccess;
+                GemmOpts o = side_opts;
+                o.pdl = ss_k;
+                const cudaError_t e = tc_gemm_nt(K_TC_PREP, M, N, K, -1.0f, ah, al, bh, bl, (int)SPW, 1.0f, C, d,
+                                                 lower, w.status, ss, o);
+                if (e == cudaSuccess) ss_k = true;
+                return e;
+            };
+            if (m > 0 && !sp_last) {
+                // A[c0:, c0:sp_end] -= L21[nn:] L21[nn : sp_end-k0-n]^T (the super-panel's own
+                // columns past the next panel)
+                const int64_t c0 = k0 + n + nn;
+                GPTQ_CUDA_TRY(side_gemm((int)(d - c0), (int)(sp_end - c0), n, Lhi + nn * SPW, Llo + nn * SPW,
+                                        Lhi + nn * SPW, Llo + nn * SPW, w.A + c0 * (d + 1), true));
+            }
+            if (m > 0 && sp_last) {
+                // deferred: first the next super-panel's columns past its first panel (the
+                // chain needs them next), then everything past the next super-panel
+                const int64_t c0 = sp_end + nn, c1 = std::min<int64_t>(d, sp_end + SPW);
+                GPTQ_CUDA_TRY(side_gemm((int)(d - c0), (int)(c1 - c0), (int)SPW, Ehi + nn * SPW, Elo + nn * SPW,
+                                        Ehi + nn * SPW, Elo + nn * SPW, w.A + c0 * (d + 1), true));
+                GPTQ_CUDA_TRY(record(two ? conc->rest : nullptr, ss));
+                const int64_t rb = c1 - sp_end;   // rows of E from c1 on
+                GPTQ_CUDA_TRY(side_gemm((int)(d - c1), (int)(d - c1), (int)SPW, Ehi + rb * SPW, Elo + rb * SPW,
+                                        Ehi + rb * SPW, Elo + rb * SPW, w.A + c1 * (d + 1), true));
+                GPTQ_CUDA_TRY(record(two ? conc->rest_far : nullptr, ss));
+            } else {
+                GPTQ_CUDA_TRY(record(two ? conc->rest : nullptr, ss));
+            }
+            // X_k = L_kk^-1 B_k over the super-panel's columns (B_k is zero from ncols on)
+            const int64_t xn = sp_end;
             float* Xi = w.Binv + k0 * d;
-            GemmOpts xt = side_opts;  // X[k, 0:ncols]^T split for the inverse's trailing update
-            xt.hi = w.xhi;
-            xt.lo = w.xlo;
-            xt.ld = NB;
+            GemmOpts xt = side_opts;  // X_k^T split for the inverse's trailing updates
+            xt.hi = w.xhi + NB * j;
+            xt.lo = w.xlo + NB * j;
+            xt.ld = SPW;
             xt.mode = 2;
             xt.pdl = true;
-            GPTQ_CUDA_TRY(split_cols(K_SPLIT, Xi, d, n, (int)ncols, w.bhi, w.blo, NB, ss, ss_k));
-            GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, n, (int)ncols, n, 1.0f, lhi, llo, w.bhi, w.blo, NB, 0.0f, Xi, d,
-                                     false, w.status, ss, xt));
+            GPTQ_CUDA_TRY(split_cols(K_SPLIT, Xi, d, n, (int)xn, w.bhi, w.blo, NB, ss, ss_k));
+            GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, n, (int)xn, n, 1.0f, lhi, llo, w.bhi, w.blo, NB, 0.0f, Xi, d, false,
+                                     w.status, ss, xt));
             ss_k = true;
-            if (m > 0) {
-                GemmOpts upd = side_opts;
-                upd.pdl = true;
-                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, (int)ncols, n, -1.0f, phi, plo, w.xhi, w.xlo, NB, 1.0f,
-                                         w.Binv + (k0 + n) * d, d, false, w.status, ss, upd));
+            if (m > 0 && !sp_last) {
+                // B[k0+n : sp_end, 0:ncols] -= L21[0 : sp_end-k0-n] X_k
+                GPTQ_CUDA_TRY(side_gemm((int)(sp_end - k0 - n), (int)ncols, n, Lhi, Llo, w.xhi + NB * j,
+                                        w.xlo + NB * j, w.Binv + (k0 + n) * d, false));
+            }
+            if (m > 0 && sp_last) {
+                // deferred: B[sp_end:, 0:sp_end] -= L[sp_end:, sp0:sp_end] X[sp0:sp_end, 0:sp_end]
+                GPTQ_CUDA_TRY(side_gemm((int)(d - sp_end), (int)sp_end, (int)SPW, Ehi, Elo, w.xhi, w.xlo,
+                                        w.Binv + sp_end * d, false));
             }
             GPTQ_CUDA_TRY(record(two ? conc->side_done[par] : nullptr, ss));
+            if (sp_last) GPTQ_CUDA_TRY(record(two ? conc->far_done[spar] : nullptr, ss));
         }
         if (two) {
             GPTQ_CUDA_TRY(record(conc->join_side, ss));

@@ -101,7 +101,7 @@ def _h_for(d, seed, dead_frac=0.02, n=None):
 
 
 @pytest.mark.parametrize("d,act_order", [(256, False), (768, False), (300, True), (1000, True), (129, False),
-                                         (2048, True)])
+                                         (2048, True), (2100, False), (2176, True)])
 def test_prepare_matches_oracle(lib, d, act_order):
     H32, diag32, _ = _h_for(d, 100 + d)
     U, perm, dead = lib.gptq_prepare(torch.tensor(H32, device=DEV), torch.tensor(diag32, device=DEV), 0.01,
@@ -136,6 +136,8 @@ QCASES = [
     # asymmetric 2- and 3-bit with act_order (the paper's default grid, narrow widths)
     (72, 256, 2, 128, False, True),
     (50, 384, 3, 32, False, True),
+    # several super-blocks of the deferred trailing update, ragged last block
+    (64, 1100, 4, 128, False, True),
 ]
 
 
