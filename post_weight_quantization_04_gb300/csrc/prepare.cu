@@ -15,7 +15,8 @@
 // fp32 factorisation; damping (0.01 * mean diag) bounds the condition number.
 //
 // Workspace layout (256-byte aligned slabs):
-//   A     d*d fp32   reversed, equilibrated Hp -> L (lower triangle)
+//   A     d*d fp32   reversed, equilibrated Hp -> L below the diagonal blocks (of those
+//                    only the inverses are formed, in LinvD or the TF32 splits)
 //   Binv  d*d fp32   identity -> L^-1 (lower triangle)
 //   LinvD nblk*NB*NB fp32  inverses of L's diagonal blocks
 //   TF32 hi/lo splits of the GEMM operands: the panel before its solve and B_k (d x NB);
@@ -181,12 +182,12 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
 // the partly reduced block as row k of `lt` (32 x LT_LD floats, 16-byte aligned rows):
 // the pivot lt[k][k] and lt[k][i] = L[i][k] * L[k][k] for i > k, which every lane then
 // reads with broadcast vector loads. Afterwards lane c forms column c of X = L^-1 by
-// forward substitution over the same rows of lt. On return the lower triangles of Sb and
-// Xb (row stride LDX_) hold L and L^-1, and XT (32 x LT_LD) holds X transposed (zeros
-// above its diagonal and outside nb).
+// forward substitution over the same rows of lt. On return the lower triangle of Xb (row
+// stride LDX_) holds L^-1 and XT (32 x LT_LD) holds X transposed (zeros above its diagonal
+// and outside nb); L itself is not stored (its users need only L^-1).
 constexpr int LT_LD = 36;
 template <int LDS_, int LDX_>
-__device__ __forceinline__ void chol_inv_32(float* Sb, float* Xb, float* XT, int nb, float* lt, int* status) {
+__device__ __forceinline__ void chol_inv_32(const float* Sb, float* Xb, float* XT, int nb, float* lt, int* status) {
     const int r = threadIdx.x & 31;
     float dinv[32];
     {
@@ -204,7 +205,6 @@ __device__ __forceinline__ void chol_inv_32(float* Sb, float* Xb, float* XT, int
                 piv = 1.0f;
             }
             const float inv = rsqrtf(piv);  // 1 / L[k][k] (hardware approximation, ~2 ulp)
-            const float lkk = piv * inv;
             dinv[k] = inv;
             const float t = a[k] * (inv * inv);  // L[r][k] / L[k][k]
 #pragma unroll
@@ -215,11 +215,7 @@ __device__ __forceinline__ void chol_inv_32(float* Sb, float* Xb, float* XT, int
                 if (4 * q + 2 > k) a[4 * q + 2] = fmaf(-t, v.z, a[4 * q + 2]);
                 if (4 * q + 3 > k) a[4 * q + 3] = fmaf(-t, v.w, a[4 * q + 3]);
             }
-            a[k] = (r == k) ? lkk : a[k] * inv;
         }
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-            if (r < nb && c <= r) Sb[r * LDS_ + c] = a[c];
     }
     // column r of X: X[k][r] = acc[k] / L[k][k], then acc[i] -= L[i][k] X[k][r] for i > k
     float acc[32];
@@ -262,9 +258,9 @@ __device__ __forceinline__ void tri_tile(int t, int& ti, int& tj) {
     tj = t - i * (i + 1) / 2;
 }
 
-// One CTA factors the diagonal block A[k0:k0+n, k0:k0+n] = L L^T in place (lower) and
-// forms L^-1 (lower, NB x NB, zeros above): optionally written to Linv, and as its TF32
-// split to Lhi/Llo. A non-positive or non-finite pivot records GPTQ_ERR_NOT_SPD (and is
+// One CTA factors the diagonal block A[k0:k0+n, k0:k0+n] = L L^T and forms L^-1 (lower,
+// NB x NB, zeros above): optionally written to Linv, and as its TF32 split to Lhi/Llo.
+// A is only read: the callers need L^-1 alone. A non-positive or non-finite pivot records GPTQ_ERR_NOT_SPD (and is
 // replaced by 1 so the kernel finishes).
 //
 // Blocked by 32 columns inside shared memory. For each 32-column sub-panel b:
@@ -280,7 +276,7 @@ constexpr int POTRF_LDX = NB + 4;   // row stride of L^-1 and of Lt (16-byte row
 constexpr size_t potrf_smem_bytes() {
     return sizeof(float) * ((size_t)NB * POTRF_LDS + (size_t)NB * POTRF_LDX + 32 * (size_t)POTRF_LDX + 2 * 32 * LT_LD);
 }
-__global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, int64_t lda, int64_t k0, int n,
+__global__ void __launch_bounds__(512) potrf_diag_kernel(const float* __restrict__ A, int64_t lda, int64_t k0, int n,
                                                         float* __restrict__ Linv, float* __restrict__ Lhi,
                                                         float* __restrict__ Llo, int* __restrict__ status) {
     extern __shared__ __align__(16) float sm[];
@@ -520,17 +516,6 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(float* __restrict__ A, 
 #pragma unroll 2
     for (int idx = tid; idx < NB * NB / 4; idx += 512) {
         const int i = idx >> 5, j4 = (idx & 31) << 2;
-        if (i < n && j4 <= i) {
-            float* dst = A + (k0 + i) * lda + k0 + j4;
-            const float* src = S + i * LD + j4;
-            if (vec && j4 + 3 <= i && j4 + 3 < n) {
-                *reinterpret_cast<float4*>(dst) = make_float4(src[0], src[1], src[2], src[3]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (j4 + e <= i && j4 + e < n) dst[e] = src[e];
-            }
-        }
         float4 v = *reinterpret_cast<const float4*>(X + i * LDX + j4);
         if (i >= n) v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         if (j4 + 0 > i || j4 + 0 >= n) v.x = 0.0f;
