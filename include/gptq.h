@@ -53,11 +53,16 @@ typedef enum gptq_dtype { GPTQ_F32 = 0, GPTQ_BF16 = 1 } gptq_dtype;
  * weights), otherwise the group size in columns (a divisor of 128 or a multiple of 128),
  * each group's scale taken at its start from the already-updated weights; sym = 1 for
  * the symmetric grid clip(round(w/s), -qmax, qmax), qmax = 2^(bits-1) - 1, sym = 0 for the
- * min/max + zero-point grid clamp(round(w/s + z), 0, 2^bits - 1). */
+ * min/max + zero-point grid clamp(round(w/s + z), 0, 2^bits - 1) (GPTQ in plain code page,
+ * "quantize_weight": s = (max - min) / (2^bits - 1), z = round(-min / s) clamped).
+ * zero_in_range = 1 selects the variant of that grid whose range is first widened to
+ * contain 0 (min <- min(min, 0), max <- max(max, 0)), so 0 is always a grid point; the
+ * pages take the raw min/max (zero_in_range = 0). Ignored by the symmetric grid. */
 typedef struct gptq_qconfig {
     int32_t bits;
     int32_t group;
     int32_t sym;
+    int32_t zero_in_range;
 } gptq_qconfig;
 
 /* ------------------------------------------------------------------------------------

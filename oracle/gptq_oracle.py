@@ -172,12 +172,20 @@ def sym_params(block, qmax: int, scale_dtype=np.float32):
     return scale, np.zeros(block.shape[0], dtype=np.int64)
 
 
-def asym_params(block, maxq: int, scale_dtype=np.float32):
+def asym_params(block, maxq: int, scale_dtype=np.float32, zero_in_range: bool = False):
     """Per-row min/max scale and zero point: scale = (max - min) / maxq (1.0 if max == min),
-    zero = clamp(round(-min / scale), 0, maxq)."""
+    zero = clamp(round(-min / scale), 0, maxq).
+
+    zero_in_range: the variant whose range is first widened to contain 0,
+    min <- min(min, 0), max <- max(max, 0), so that 0 is a grid point (z lands in
+    [0, maxq] unclamped and dequantises to exactly 0). Not on the pages, which take the
+    raw min/max; this is the plain reading of "the range includes 0"."""
     block = np.asarray(block, dtype=F64)
     mn = block.min(axis=1)
     mx = block.max(axis=1)
+    if zero_in_range:
+        mn = np.minimum(mn, 0.0)
+        mx = np.maximum(mx, 0.0)
     scale = np.where(mx > mn, (mx - mn) / maxq, 1.0)
     scale = _stored(scale, scale_dtype)
     zero = np.clip(np.round(-mn / scale), 0, maxq).astype(np.int64)
@@ -236,7 +244,8 @@ def _force(own, forced, t, lo, hi, tol, what, j, log):
 
 
 def gptq_loop(W, U, bits: int, group: int = 0, sym: bool = True, scale_dtype=np.float32,
-              forced_codes=None, forced_zeros=None, tie_tol: float = 1e-4) -> Dict[str, np.ndarray]:
+              forced_codes=None, forced_zeros=None, tie_tol: float = 1e-4,
+              zero_in_range: bool = False) -> Dict[str, np.ndarray]:
     """GPTQ's fixed-order column loop on an already dead-zeroed, already permuted W.
 
     For j = 0 .. d-1 ([loop] algorithm; [guide] "Source code", `gptq` loop):
@@ -258,7 +267,8 @@ def gptq_loop(W, U, bits: int, group: int = 0, sym: bool = True, scale_dtype=np.
     G = -(-d // group) if group else 1
     qm = qmax_sym(bits) if sym else maxq_asym(bits)
     lo, hi = (-qm, qm) if sym else (0, qm)
-    params = (lambda b: sym_params(b, qm, scale_dtype)) if sym else (lambda b: asym_params(b, qm, scale_dtype))
+    params = ((lambda b: sym_params(b, qm, scale_dtype)) if sym
+              else (lambda b: asym_params(b, qm, scale_dtype, zero_in_range)))
 
     codes = np.zeros((o, d), dtype=np.int64)
     Q = np.zeros((o, d), dtype=F64)
@@ -369,7 +379,7 @@ def dequant_matmul(X, packed, scales, zeros, g_idx, bits: int) -> np.ndarray:
 
 def gptq_quantize(W, U, perm, dead, bits: int, group: int = 0, sym: bool = True,
                   scale_dtype=np.float32, forced_codes=None, forced_zeros=None,
-                  tie_tol: float = 1e-4) -> Dict[str, np.ndarray]:
+                  tie_tol: float = 1e-4, zero_in_range: bool = False) -> Dict[str, np.ndarray]:
     """One layer's quantisation given (U, perm, dead), outputs in the original column order.
 
     Follows [guide]'s `gptq` after its `_hessian_inverse_chol` call: W[:, dead] = 0,
@@ -381,7 +391,7 @@ def gptq_quantize(W, U, perm, dead, bits: int, group: int = 0, sym: bool = True,
     W[:, np.asarray(dead, dtype=bool)] = 0.0
     perm = np.arange(d) if perm is None else np.asarray(perm)
     fc = None if forced_codes is None else np.asarray(forced_codes)[:, perm]
-    r = gptq_loop(W[:, perm], U, bits, group, sym, scale_dtype, fc, forced_zeros, tie_tol)
+    r = gptq_loop(W[:, perm], U, bits, group, sym, scale_dtype, fc, forced_zeros, tie_tol, zero_in_range)
     inv = np.argsort(perm)
     u = unsigned_codes(r["codes"][:, inv], bits, sym)
     return {
@@ -449,7 +459,7 @@ def apply_layerwise(X, Ws, fn, skip_last: bool = False, act_round=None):
 
 
 def rtn_quantize(W, bits: int, group: int = 0, sym: bool = True, dead=None,
-                 scale_dtype=np.float32) -> Dict[str, np.ndarray]:
+                 scale_dtype=np.float32, zero_in_range: bool = False) -> Dict[str, np.ndarray]:
     """Round-to-nearest baseline: every weight rounded on its own onto the same grid
     ([loop] intro; [guide] "The idea"): scales from W itself (per row, or per contiguous
     group), no error feedback. Dead columns are zeroed first when `dead` is given."""
@@ -466,7 +476,8 @@ def rtn_quantize(W, bits: int, group: int = 0, sym: bool = True, dead=None,
     zeros = np.zeros((o, G), dtype=np.int64)
     for gi in range(G):
         sl = slice(gi * step, min(d, (gi + 1) * step))
-        s, z = sym_params(W[:, sl], qm, scale_dtype) if sym else asym_params(W[:, sl], qm, scale_dtype)
+        s, z = (sym_params(W[:, sl], qm, scale_dtype) if sym
+                else asym_params(W[:, sl], qm, scale_dtype, zero_in_range))
         c = quant_codes(W[:, sl], s[:, None], z[:, None], bits, sym)
         codes[:, sl] = c
         Wq[:, sl] = dequant(c, s[:, None], z[:, None], sym)
@@ -507,7 +518,8 @@ def layer_loss(Q, W0, H) -> np.ndarray:
 # Brute-force OBS  ([guide] "How it works": OBS step 1-4, then "Remove j and repeat")
 # ----------------------------------------------------------------------------------------
 
-def obs_bruteforce_row(w, H, bits: int, group: int = 0, sym: bool = True, scale_dtype=np.float32):
+def obs_bruteforce_row(w, H, bits: int, group: int = 0, sym: bool = True, scale_dtype=np.float32,
+                       zero_in_range: bool = False):
     """One row through explicit OBS: no Cholesky factor, only H^-1 and elimination.
 
     For j in order: e = w_j - quant(w_j); delta = -(e / Hinv[j, j]) * Hinv[j, F] over the
@@ -520,7 +532,8 @@ def obs_bruteforce_row(w, H, bits: int, group: int = 0, sym: bool = True, scale_
     Hinv = np.linalg.inv(np.asarray(H, F64))
     F = list(range(d))
     qm = qmax_sym(bits) if sym else maxq_asym(bits)
-    params = (lambda b: sym_params(b, qm, scale_dtype)) if sym else (lambda b: asym_params(b, qm, scale_dtype))
+    params = ((lambda b: sym_params(b, qm, scale_dtype)) if sym
+              else (lambda b: asym_params(b, qm, scale_dtype, zero_in_range)))
     scale, zero = params(w[None, :])
     q = np.zeros(d)
     incr = np.zeros(d)

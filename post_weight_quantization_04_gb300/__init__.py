@@ -45,7 +45,8 @@ class GptqError(RuntimeError):
 
 
 class QConfig(ctypes.Structure):
-    _fields_ = [("bits", ctypes.c_int32), ("group", ctypes.c_int32), ("sym", ctypes.c_int32)]
+    _fields_ = [("bits", ctypes.c_int32), ("group", ctypes.c_int32), ("sym", ctypes.c_int32),
+                ("zero_in_range", ctypes.c_int32)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -130,8 +131,8 @@ def _dev(t: torch.Tensor, dtype, name: str, shape=None) -> None:
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
-def qconfig(bits: int, group: int = 0, sym: bool = True) -> QConfig:
-    return QConfig(int(bits), int(group), 1 if sym else 0)
+def qconfig(bits: int, group: int = 0, sym: bool = True, zero_in_range: bool = False) -> QConfig:
+    return QConfig(int(bits), int(group), 1 if sym else 0, 1 if zero_in_range else 0)
 
 
 def gptq_packed_words_per_row(cols: int, bits: int) -> int:
@@ -245,8 +246,9 @@ def _outputs(rows, cols, bits, group, dev):
 def gptq_quantize(W: torch.Tensor, U: torch.Tensor, perm: Optional[torch.Tensor] = None,
                   dead: Optional[torch.Tensor] = None, bits: int = 4, group: int = 0, sym: bool = True,
                   ws: Optional[torch.Tensor] = None, out: Optional[Dict[str, torch.Tensor]] = None,
-                  stream=None) -> Dict[str, torch.Tensor]:
-    """GPTQ's column loop on W (rows, cols) given U (loop order), perm and dead."""
+                  stream=None, zero_in_range: bool = False) -> Dict[str, torch.Tensor]:
+    """GPTQ's column loop on W (rows, cols) given U (loop order), perm and dead.
+    zero_in_range: asymmetric grid over the min/max range widened to contain 0."""
     rows, cols = W.shape
     _dev(W, torch.float32, "W")
     _dev(U, torch.float32, "U", (cols, cols))
@@ -264,7 +266,7 @@ def gptq_quantize(W: torch.Tensor, U: torch.Tensor, perm: Optional[torch.Tensor]
     if ws is None:
         ws = torch.empty(nb, dtype=torch.uint8, device=dev)
     _check("gptq_quantize", load().gptq_quantize(
-        _ptr(W), rows, cols, _ptr(U), _ptr(perm), _ptr(dead), qconfig(bits, group, sym),
+        _ptr(W), rows, cols, _ptr(U), _ptr(perm), _ptr(dead), qconfig(bits, group, sym, zero_in_range),
         _ptr(o["codes"]), _ptr(o["scales"]), _ptr(o["zeros"]), _ptr(o["g_idx"]), _ptr(o.get("Wq")),
         _ptr(o.get("packed")), _ptr(o["row_loss"]), _ptr(ws), ws.numel(), _stream(stream)))
     return o
@@ -272,14 +274,14 @@ def gptq_quantize(W: torch.Tensor, U: torch.Tensor, perm: Optional[torch.Tensor]
 
 def rtn_quantize(W: torch.Tensor, bits: int = 4, group: int = 0, sym: bool = True,
                  dead: Optional[torch.Tensor] = None, out: Optional[Dict[str, torch.Tensor]] = None,
-                 stream=None) -> Dict[str, torch.Tensor]:
+                 stream=None, zero_in_range: bool = False) -> Dict[str, torch.Tensor]:
     rows, cols = W.shape
     _dev(W, torch.float32, "W")
     if dead is not None:
         _dev(dead, torch.uint8, "dead", (cols,))
     o = out if out is not None else _outputs(rows, cols, bits, group, W.device)
     _check("rtn_quantize", load().rtn_quantize(
-        _ptr(W), rows, cols, _ptr(dead), qconfig(bits, group, sym), _ptr(o["codes"]), _ptr(o["scales"]),
+        _ptr(W), rows, cols, _ptr(dead), qconfig(bits, group, sym, zero_in_range), _ptr(o["codes"]), _ptr(o["scales"]),
         _ptr(o["zeros"]), _ptr(o.get("Wq")), _ptr(o.get("packed")), _stream(stream)))
     return o
 

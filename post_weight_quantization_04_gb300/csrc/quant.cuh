@@ -34,7 +34,12 @@ __device__ __forceinline__ Grid sym_grid(float absmax, int qmax) {
     return Grid{s, 1.0f / s, 0.0f};
 }
 
-__device__ __forceinline__ Grid asym_grid(float mn, float mx, int maxq) {
+// zr: the range is widened to contain 0 first (the grid then has 0 as a point)
+__device__ __forceinline__ Grid asym_grid(float mn, float mx, int maxq, bool zr) {
+    if (zr) {
+        mn = fminf(mn, 0.0f);
+        mx = fmaxf(mx, 0.0f);
+    }
     const double sd = (mx > mn) ? ((double)mx - (double)mn) / (double)maxq : 1.0;
     const float s = __double2float_rn(sd);
     double z = rint(-(double)mn / (double)s);

@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(256) init_work_kernel(const float* __restrict_
 
 // One warp per row: grid of Wk[r][c0:c1] -> cur_s/cur_z and the (scales, zeros) outputs.
 __global__ void row_params_kernel(const float* __restrict__ Wk, int64_t rows, int64_t cols, int64_t c0, int64_t c1,
-                                  int bits, int sym, float* __restrict__ cur_s, float* __restrict__ cur_z,
+                                  int bits, int sym, int zr, float* __restrict__ cur_s, float* __restrict__ cur_z,
                                   float* __restrict__ scales, uint8_t* __restrict__ zeros, int64_t G, int64_t gi) {
     const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -138,7 +138,7 @@ __global__ void row_params_kernel(const float* __restrict__ Wk, int64_t rows, in
     } else {
         mx = warp_max(mx);
         mn = warp_min(mn);
-        g = asym_grid(mn, mx, (1 << bits) - 1);
+        g = asym_grid(mn, mx, (1 << bits) - 1, zr != 0);
     }
     if (lane == 0) {
         cur_s[r] = g.s;
@@ -154,6 +154,7 @@ struct BlockArgs {
     int bw;
     const float* U;
     int bits, sym, group;  // group in (0, 128] dividing 128: in-block params; else cur_s/cur_z
+    int zr;                // asymmetric grid over a range widened to contain 0
     const float* cur_s;
     const float* cur_z;
     float* Err;
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off, TPR));
             mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off, TPR));
         }
-        const Grid gg = sym ? sym_grid(am, qmax) : asym_grid(mn, mx, qmax);
+        const Grid gg = sym ? sym_grid(am, qmax) : asym_grid(mn, mx, qmax, a.zr != 0);
         if (active && sub == 0) {
             const int64_t gi = (a.j0 + jj) / a.group;
             a.scales[row * a.G + gi] = gg.s;
@@ -440,7 +441,7 @@ __global__ void pack_kernel(const int8_t* __restrict__ codes, int64_t rows, int6
 
 // Round-to-nearest: one warp per (row, group) (group > 0) or one CTA per row (group == 0).
 __global__ void rtn_group_kernel(const float* __restrict__ W, int64_t rows, int64_t cols, const uint8_t* __restrict__ dead,
-                                 int bits, int sym, int group, int64_t G, int8_t* __restrict__ codes,
+                                 int bits, int sym, int zr, int group, int64_t G, int8_t* __restrict__ codes,
                                  float* __restrict__ scales, uint8_t* __restrict__ zeros, float* __restrict__ Wq) {
     const int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -456,7 +457,7 @@ __global__ void rtn_group_kernel(const float* __restrict__ W, int64_t rows, int6
         am = fmaxf(am, fabsf(v));
     }
     const int qmax = sym ? (1 << (bits - 1)) - 1 : (1 << bits) - 1;
-    const Grid g = sym ? sym_grid(warp_max(am), qmax) : asym_grid(warp_min(mn), warp_max(mx), qmax);
+    const Grid g = sym ? sym_grid(warp_max(am), qmax) : asym_grid(warp_min(mn), warp_max(mx), qmax, zr != 0);
     if (lane == 0) {
         scales[r * G + gi] = g.s;
         zeros[r * G + gi] = sym ? (uint8_t)(1 << (bits - 1)) : (uint8_t)g.z;
@@ -471,7 +472,7 @@ __global__ void rtn_group_kernel(const float* __restrict__ W, int64_t rows, int6
 }
 
 __global__ void __launch_bounds__(256) rtn_row_kernel(const float* __restrict__ W, int64_t rows, int64_t cols,
-                                                     const uint8_t* __restrict__ dead, int bits, int sym,
+                                                     const uint8_t* __restrict__ dead, int bits, int sym, int zr,
                                                      int8_t* __restrict__ codes, float* __restrict__ scales,
                                                      uint8_t* __restrict__ zeros, float* __restrict__ Wq) {
     const int64_t r = blockIdx.x;
@@ -503,7 +504,7 @@ __global__ void __launch_bounds__(256) rtn_row_kernel(const float* __restrict__ 
         am = fmaxf(am, red[2][i]);
     }
     const int qmax = sym ? (1 << (bits - 1)) - 1 : (1 << bits) - 1;
-    const Grid g = sym ? sym_grid(am, qmax) : asym_grid(mn, mx, qmax);
+    const Grid g = sym ? sym_grid(am, qmax) : asym_grid(mn, mx, qmax, zr != 0);
     if (threadIdx.x == 0) {
         scales[r] = g.s;
         zeros[r] = sym ? (uint8_t)(1 << (bits - 1)) : (uint8_t)g.z;
@@ -581,7 +582,7 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
     if (tc) GPTQ_CUDA_TRY(split_cols(K_SPLIT, U, cols, (int)cols, (int)cols, w.uhi, w.ulo, (int)cols, s));
     const unsigned pgrid = (unsigned)ceil_div(rows, 8);
     if (q.group == 0) {
-        GPTQ_LAUNCH(K_ROW_PARAMS, s, row_params_kernel<<<pgrid, 256, 0, s>>>(w.W, rows, cols, 0, cols, q.bits, q.sym,
+        GPTQ_LAUNCH(K_ROW_PARAMS, s, row_params_kernel<<<pgrid, 256, 0, s>>>(w.W, rows, cols, 0, cols, q.bits, q.sym, q.zero_in_range,
                                                                              w.cur_s, w.cur_z, scales, zeros, G, 0));
         GPTQ_LAUNCH_CHECK();
     }
@@ -614,6 +615,7 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
     a.U = U;
     a.bits = q.bits;
     a.sym = q.sym;
+    a.zr = q.zero_in_range;
     a.group = q.group;
     a.cur_s = w.cur_s;
     a.cur_z = w.cur_z;
@@ -633,6 +635,7 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
             GPTQ_LAUNCH(K_ROW_PARAMS, s,
                         row_params_kernel<<<pgrid, 256, 0, s>>>(w.W, rows, cols, j0,
                                                                 std::min<int64_t>(cols, j0 + q.group), q.bits, q.sym,
+                                                                q.zero_in_range,
                                                                 w.cur_s, w.cur_z, scales, zeros, G, j0 / q.group));
             GPTQ_LAUNCH_CHECK();
         }
@@ -697,12 +700,12 @@ extern "C" int rtn_quantize(const float* W, int64_t rows, int64_t cols, const ui
     if (!W || !codes || !scales || !zeros || rows > 65535) return GPTQ_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (q.group == 0) {
-        GPTQ_LAUNCH(K_RTN, s, rtn_row_kernel<<<(unsigned)rows, 256, 0, s>>>(W, rows, cols, dead, q.bits, q.sym, codes, scales, zeros, Wq));
+        GPTQ_LAUNCH(K_RTN, s, rtn_row_kernel<<<(unsigned)rows, 256, 0, s>>>(W, rows, cols, dead, q.bits, q.sym, q.zero_in_range, codes, scales, zeros, Wq));
     } else {
         const int64_t G = ceil_div(cols, q.group);
         const int64_t tasks = rows * G;
         GPTQ_LAUNCH(K_RTN, s,
-                    rtn_group_kernel<<<(unsigned)ceil_div(tasks, 8), 256, 0, s>>>(W, rows, cols, dead, q.bits, q.sym,
+                    rtn_group_kernel<<<(unsigned)ceil_div(tasks, 8), 256, 0, s>>>(W, rows, cols, dead, q.bits, q.sym, q.zero_in_range,
                                                                                   q.group, G, codes, scales, zeros, Wq));
     }
     GPTQ_LAUNCH_CHECK();

@@ -120,6 +120,45 @@ def test_asym_quantizer_by_hand():
     assert s3[0] == 1.0 and z3[0] == 0
 
 
+def test_asym_zero_in_range_by_hand():
+    """The variant whose range is widened to contain 0 (values worked by hand)."""
+    # all-positive block, 2 bits: range [0, 1] -> scale 1/3, zero 0 (the raw range [0.5, 1]
+    # would give scale 1/6 and no grid point at 0)
+    s, z = O.asym_params(np.array([[0.5, 1.0]]), 3, scale_dtype=None, zero_in_range=True)
+    assert np.isclose(s[0], 1.0 / 3.0, rtol=1e-15) and z[0] == 0
+    c = O.quant_codes(np.array([[0.5, 1.0, 0.0]]), s[:, None], z[:, None], 2, False)
+    np.testing.assert_array_equal(c, [[2, 3, 0]])            # 0.5 * 3 = 1.5 -> 2 (half to even)
+    # all-negative block, 3 bits: range [-1.4, 0] -> scale 0.2, zero round(7) = 7 = maxq
+    s, z = O.asym_params(np.array([[-1.4, -0.2]]), 7, scale_dtype=None, zero_in_range=True)
+    assert np.isclose(s[0], 0.2, rtol=1e-15) and z[0] == 7
+    c = O.quant_codes(np.array([[-1.4, -0.2, 0.0]]), s[:, None], z[:, None], 3, False)
+    np.testing.assert_array_equal(c, [[0, 6, 7]])
+    np.testing.assert_allclose(O.dequant(c, s[:, None], z[:, None], False), [[-1.4, -0.2, 0.0]], atol=1e-15)
+    # a block that already straddles 0 is unchanged by the widening
+    b = _rng(5).standard_normal((6, 16))
+    b[:, 0], b[:, 1] = -1.0, 1.0
+    for bits in (2, 3, 4):
+        s1, z1 = O.asym_params(b, 2 ** bits - 1)
+        s2, z2 = O.asym_params(b, 2 ** bits - 1, zero_in_range=True)
+        np.testing.assert_array_equal(s1, s2)
+        np.testing.assert_array_equal(z1, z2)
+
+
+def test_asym_zero_in_range_zero_is_exact():
+    """With the widened range every block has 0 on its grid: w = 0 quantises to code z,
+    which dequantises to exactly 0, and z lies in [0, maxq] without clamping."""
+    rng = _rng(6)
+    for bits in (2, 3, 4):
+        maxq = 2 ** bits - 1
+        b = rng.standard_normal((200, 8)) * 0.1 + rng.choice([-0.3, 0.0, 0.3], size=(200, 1))
+        s, z = O.asym_params(b, maxq, zero_in_range=True)
+        mn, mx = np.minimum(b.min(1), 0), np.maximum(b.max(1), 0)
+        assert np.all((-mn / s >= -0.5) & (-mn / s <= maxq + 0.5))   # no clamping needed
+        c = O.quant_codes(np.zeros((200, 1)), s[:, None], z[:, None], bits, False)
+        np.testing.assert_array_equal(c[:, 0], z)
+        assert np.all(O.dequant(c, s[:, None], z[:, None], False) == 0.0)
+
+
 def test_stored_scale_is_float32_grid():
     w = _rng(3).standard_normal((5, 9))
     s, _ = O.sym_params(w, 7)
@@ -164,9 +203,11 @@ def test_act_order_perm_stable_descending():
 
 # ------------------------------------------------------------------- the GPTQ loop
 
-@pytest.mark.parametrize("d,group,sym,bits", [(4, 0, True, 3), (6, 0, True, 2), (8, 0, True, 4),
-                                              (8, 4, True, 3), (8, 4, False, 4), (6, 3, False, 2)])
-def test_cholesky_loop_equals_bruteforce_obs(d, group, sym, bits):
+@pytest.mark.parametrize("d,group,sym,bits,zr", [(4, 0, True, 3, False), (6, 0, True, 2, False),
+                                                 (8, 0, True, 4, False), (8, 4, True, 3, False),
+                                                 (8, 4, False, 4, False), (6, 3, False, 2, False),
+                                                 (8, 4, False, 3, True), (6, 0, False, 2, True)])
+def test_cholesky_loop_equals_bruteforce_obs(d, group, sym, bits, zr):
     """P-1/P-2: the Cholesky-form loop equals explicit OBS with Gaussian elimination,
     and each step raises the loss by err_j^2 / 2 = e^2 / (2 Hinv_F[j, j])."""
     rng = _rng(10 + d + group)
@@ -174,14 +215,16 @@ def test_cholesky_loop_equals_bruteforce_obs(d, group, sym, bits):
     W = rng.standard_normal((5, d)) * 0.3
     H = _damped(O.hessian(X))
     U = O.upper_cholesky_of_inverse(H)
-    r = O.gptq_loop(W, U, bits, group, sym)
+    if zr:
+        W = W + 0.4   # mostly one-signed rows, where the widened range differs
+    r = O.gptq_loop(W, U, bits, group, sym, zero_in_range=zr)
     for i in range(W.shape[0]):
-        q, incr = O.obs_bruteforce_row(W[i], H, bits, group, sym)
+        q, incr = O.obs_bruteforce_row(W[i], H, bits, group, sym, zero_in_range=zr)
         np.testing.assert_allclose(r["Q"][i], q, rtol=0, atol=1e-12)
     # error increments: OBS's e^2 / (2 Hinv_F[j, j]) summed over the steps equals the
     # loop's sum of err_j^2 / 2, row by row
     for i in range(W.shape[0]):
-        _, incr = O.obs_bruteforce_row(W[i], H, bits, group, sym)
+        _, incr = O.obs_bruteforce_row(W[i], H, bits, group, sym, zero_in_range=zr)
         np.testing.assert_allclose(incr, 0.5 * r["err"][i] ** 2, rtol=1e-9, atol=1e-15)
         np.testing.assert_allclose(incr.sum(), 0.5 * r["err_sq"][i], rtol=1e-10, atol=1e-15)
 

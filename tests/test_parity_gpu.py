@@ -184,6 +184,56 @@ def test_rtn_bit_exact(lib, rows, cols, bits, group, sym):
     np.testing.assert_array_equal(npy(out["packed"]).view(np.uint32), ref["packed"])
 
 
+# asymmetric grid over the range widened to contain 0: rows shifted so most groups are
+# one-signed (where the widening changes the grid)
+ZCASES = [(64, 256, 4, 128, False), (50, 384, 3, 32, True), (40, 300, 2, 0, True), (33, 640, 3, 128, True)]
+
+
+@pytest.mark.parametrize("rows,cols,bits,group,act", ZCASES)
+def test_quantize_zero_in_range_given_oracle_u(lib, rows, cols, bits, group, act):
+    # no dead inputs here: a zeroed dead column puts 0 into its group's range by itself
+    H32, diag32, _ = _h_for(cols, 500 + cols + rows, dead_frac=0.0)
+    Uref, perm, dead = O.prepare(H32.astype(np.float64), 0.01, act, diag32.astype(np.float64))
+    U32 = f32(Uref)
+    W = synth.make_weight(rows, cols, 0.02, 600 + rows, device=DEV)
+    W += torch.linspace(-0.1, 0.1, rows, device=DEV)[:, None]
+    Wh = synth.to_numpy_f64(W)
+    out = lib.gptq_quantize(W, torch.tensor(U32, device=DEV), torch.tensor(perm.astype(np.int32), device=DEV),
+                            torch.tensor(dead.astype(np.uint8), device=DEV), bits, group, False, zero_in_range=True)
+    codes = npy(out["codes"]).astype(np.int64)
+    zeros = npy(out["zeros"]).astype(np.int64)
+    ref = O.gptq_quantize(Wh, U32.astype(np.float64), perm, dead, bits, group, False, forced_codes=codes,
+                          forced_zeros=zeros, zero_in_range=True)
+    nmis = len([t for t in ref["ties"] if t[2] == "code"])
+    assert nmis <= 1e-4 * codes.size + 0.5, ref["ties"]
+    np.testing.assert_array_equal(codes, ref["codes"])
+    np.testing.assert_allclose(npy(out["scales"]), ref["scales"], rtol=2e-5, atol=0)
+    np.testing.assert_array_equal(zeros, ref["zeros"])
+    np.testing.assert_allclose(npy(out["Wq"]), ref["Wq"], rtol=2e-5, atol=1e-7)
+    np.testing.assert_array_equal(npy(out["g_idx"]), ref["g_idx"])
+    np.testing.assert_array_equal(npy(out["packed"]).view(np.uint32), ref["packed"])
+    # the widened grid differs from the raw one on these rows (one-signed groups get
+    # another scale), and 0 is a grid point of every group: code z dequantises to 0
+    raw = O.gptq_quantize(Wh, U32.astype(np.float64), perm, dead, bits, group, False)
+    assert np.mean(raw["scales"] != ref["scales"]) > 0.2
+
+
+@pytest.mark.parametrize("rows,cols,bits,group", [(64, 256, 4, 128), (37, 300, 3, 64), (16, 1000, 2, 128),
+                                                  (9, 77, 3, 0)])
+def test_rtn_zero_in_range_bit_exact(lib, rows, cols, bits, group):
+    W = synth.make_weight(rows, cols, 0.05, 700 + cols, device=DEV)
+    W += torch.linspace(-0.2, 0.2, rows, device=DEV)[:, None]
+    dead = torch.zeros(cols, dtype=torch.uint8, device=DEV)
+    dead[::17] = 1
+    out = lib.rtn_quantize(W, bits, group, False, dead=dead, zero_in_range=True)
+    ref = O.rtn_quantize(synth.to_numpy_f64(W), bits, group, False, dead=npy(dead).astype(bool), zero_in_range=True)
+    np.testing.assert_array_equal(npy(out["codes"]).astype(np.int64), ref["codes"])
+    np.testing.assert_array_equal(npy(out["scales"]), f32(ref["scales"]))
+    np.testing.assert_array_equal(npy(out["zeros"]).astype(np.int64), ref["zeros"])
+    np.testing.assert_array_equal(npy(out["Wq"]), f32(ref["Wq"]))
+    np.testing.assert_array_equal(npy(out["packed"]).view(np.uint32), ref["packed"])
+
+
 def _tie_segment(rng, n, bits, sym):
     """n fp32 weights whose grid (from their own min/max) puts many of them exactly on, or
     one ulp either side of, a rounding half-point of w / s (+ z)."""
