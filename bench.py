@@ -307,10 +307,13 @@ ROOF = {
     "init_work_kernel": ("hbm", "GB/s"),
 }
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
-# --set full capture per kernel class and workload (summaries under profiles/); a
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures
+# (summaries under profiles/): one --set full launch per kernel class, or, for a class
+# launched with many shapes per step, the average over one whole step's launches; a
 # kernel changed since its capture has no entry here.
 TRAFFIC = {
+    (1, "tc_gemm_nt_kernel[prepare]"): 768337.92,
+    (1, "tc_gemm_nt_kernel[trailing]"): 10274048.0,
     (2, "hessian_tc_kernel"): 4.827069e9 + 159.446272e6,
     (2, "pack_kernel"): 16.788224e6,
 }
