@@ -190,6 +190,7 @@ template <int LDS_, int LDX_>
 __device__ __forceinline__ void chol_inv_32(const float* Sb, float* Xb, float* XT, int nb, float* lt, int* status) {
     const int r = threadIdx.x & 31;
     float dinv[32];
+    bool bad = false;
     {
         float a[32];
 #pragma unroll
@@ -199,11 +200,8 @@ __device__ __forceinline__ void chol_inv_32(const float* Sb, float* Xb, float* X
             if (k >= nb) break;
             lt[k * LT_LD + r] = a[k];
             __syncwarp();
-            float piv = lt[k * LT_LD + k];
-            if (!(piv > 0.0f) || !isfinite(piv)) {
-                if (r == 0) set_status(status, GPTQ_ERR_NOT_SPD);
-                piv = 1.0f;
-            }
+            const float piv = lt[k * LT_LD + k];
+            bad |= !(piv > 0.0f && piv < INFINITY);   // checked once, after the loop
             const float inv = rsqrtf(piv);  // 1 / L[k][k] (hardware approximation, ~2 ulp)
             dinv[k] = inv;
             const float t = a[k] * (inv * inv);  // L[r][k] / L[k][k]
@@ -217,6 +215,10 @@ __device__ __forceinline__ void chol_inv_32(const float* Sb, float* Xb, float* X
             }
         }
     }
+    // a pivot that is not positive and finite: the block is not positive definite; the
+    // factorisation goes on with the non-finite values it produces (nothing downstream
+    // loops on data) and the call reports the status
+    if (bad && r == 0) set_status(status, GPTQ_ERR_NOT_SPD);
     // column r of X: X[k][r] = acc[k] / L[k][k], then acc[i] -= L[i][k] X[k][r] for i > k
     float acc[32];
 #pragma unroll
@@ -249,6 +251,10 @@ __device__ __forceinline__ void chol_inv_32(const float* Sb, float* Xb, float* X
     __syncwarp();  // lt is reused by the next call
 }
 
+// named barrier 1: warps 1-3 hand the updated next diagonal block to warp 0
+__device__ __forceinline__ void bar_arrive_diag() { asm volatile("bar.arrive 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void bar_sync_diag() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 // (ti, tj) of the t-th 4 x 4 tile of a lower triangle, row by row
 __device__ __forceinline__ void tri_tile(int t, int& ti, int& tj) {
     int i = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
@@ -260,17 +266,18 @@ __device__ __forceinline__ void tri_tile(int t, int& ti, int& tj) {
 
 // One CTA factors the diagonal block A[k0:k0+n, k0:k0+n] = L L^T and forms L^-1 (lower,
 // NB x NB, zeros above): optionally written to Linv, and as its TF32 split to Lhi/Llo.
-// A is only read: the callers need L^-1 alone. A non-positive or non-finite pivot records GPTQ_ERR_NOT_SPD (and is
-// replaced by 1 so the kernel finishes).
+// A is only read: the callers need L^-1 alone. A non-positive or non-finite pivot records
+// GPTQ_ERR_NOT_SPD (the kernel still finishes; its outputs are then not finite).
 //
 // Blocked by 32 columns inside shared memory. For each 32-column sub-panel b:
 //   1. warp 0: L_bb and X_bb = L_bb^-1 (chol_inv_32)
 //   2. the panel below it, L21 = A21 X_bb^T (kept also transposed in Lt), and the block
 //      row of the inverse left of the diagonal, X[b, :b] = X_bb B[b, :b]
-//   3. the trailing update A22 -= L21 L21^T and the inverse's right-looking update
+//   3. the trailing update A22 -= L21 L21^T (its next diagonal block first, by warps 1-3,
+//      then factored by warp 0) and the inverse's right-looking update
 //      B[below, :b+32] -= L21 X[b, :b+32]
 // (B, the right-hand side of L X = I, lives in X's storage until it is overwritten.)
-// All products are 4 x 4 register tiles over shared memory, read with 16-byte loads.
+// All products are register tiles over shared memory, read with 16-byte loads.
 constexpr int POTRF_LDS = NB + 1;   // row stride of the block (odd: conflict-free columns)
 constexpr int POTRF_LDX = NB + 4;   // row stride of L^-1 and of Lt (16-byte rows)
 constexpr size_t potrf_smem_bytes() {
@@ -281,7 +288,7 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(const float* __restrict
                                                         float* __restrict__ Llo, int* __restrict__ status) {
     extern __shared__ __align__(16) float sm[];
     constexpr int LD = POTRF_LDS, LDX = POTRF_LDX;
-    float* S = sm;                   // NB x LD: the block, then L
+    float* S = sm;                   // NB x LD: the block (lower triangle), updated in place
     float* X = S + NB * LD;          // NB x LDX: B, then L^-1
     float* Lt = X + NB * LDX;        // 32 x LDX: the current panel of L, transposed
     float* XT = Lt + 32 * LDX;       // 32 x LT_LD: X_bb transposed
@@ -290,40 +297,21 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(const float* __restrict
     pdl_wait();
     pdl_trigger();
 
-    const bool vec = ((lda & 3) == 0) && ((k0 & 3) == 0) && ((reinterpret_cast<uintptr_t>(A) & 15) == 0);
     {
-        // all loads of a thread in flight at once; 16-byte loads where the rows allow
-        float4 v[NB * NB / 4 / 512];
+        // the lower triangle, one element per thread and step with consecutive columns
+        // across a warp: 128-byte global reads, conflict-free shared stores; all loads of
+        // a thread in flight at once
+        float v[NB * NB / 512];
 #pragma unroll
-        for (int u = 0; u < NB * NB / 4 / 512; ++u) {
+        for (int u = 0; u < NB * NB / 512; ++u) {
             const int idx = tid + 512 * u;
-            const int i = idx >> 5, j4 = (idx & 31) << 2;
-            const float* src = A + (k0 + i) * lda + k0 + j4;
-            float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            if (i < n && j4 <= i) {
-                if (vec && j4 + 3 < n) {
-                    x = *reinterpret_cast<const float4*>(src);
-                } else {
-                    x.x = src[0];
-                    if (j4 + 1 < n) x.y = src[1];
-                    if (j4 + 2 < n) x.z = src[2];
-                    if (j4 + 3 < n) x.w = src[3];
-                }
-                if (j4 + 1 > i) x.y = 0.0f;
-                if (j4 + 2 > i) x.z = 0.0f;
-                if (j4 + 3 > i) x.w = 0.0f;
-            }
-            v[u] = x;
+            const int i = idx >> 7, j = idx & (NB - 1);
+            v[u] = (i < n && j <= i) ? A[(k0 + i) * lda + k0 + j] : 0.0f;
         }
 #pragma unroll
-        for (int u = 0; u < NB * NB / 4 / 512; ++u) {
+        for (int u = 0; u < NB * NB / 512; ++u) {
             const int idx = tid + 512 * u;
-            const int i = idx >> 5, j4 = (idx & 31) << 2;
-            float* d = S + i * LD + j4;
-            d[0] = v[u].x;
-            d[1] = v[u].y;
-            d[2] = v[u].z;
-            d[3] = v[u].w;
+            S[(idx >> 7) * LD + (idx & (NB - 1))] = v[u];
         }
         for (int idx = tid; idx < NB * LDX / 4; idx += 512)
             reinterpret_cast<float4*>(X)[idx] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -337,28 +325,29 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(const float* __restrict
         __syncthreads();
         const int rb = b + 32, m = max(0, n - rb);
         const int tm = (m + 3) >> 2;       // 4-row tiles below the sub-panel
-        // ---- 2. panel L21 = A21 X_bb^T, and X[b, :b] = X_bb B[b, :b] ----
+        // ---- 2. panel L21 = A21 X_bb^T (2 x 4 tiles: up to 384 threads, each a short
+        //      chain on the critical path), and X[b, :b] = X_bb B[b, :b] (4 x 4 tiles) ----
         {
-            const int P = tm * 8, Q = 8 * (b >> 2);
+            const int P = 8 * ((m + 1) >> 1), Q = 8 * (b >> 2);
             float acc[4][4];
             int kind = -1, r0 = 0, c0 = 0;
             const int t = tid;
             if (t < P) {
                 kind = 0;
-                r0 = rb + 4 * (t >> 3);
+                r0 = rb + 2 * (t >> 3);
                 c0 = 4 * (t & 7);
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                for (int u = 0; u < 2; ++u)
 #pragma unroll
                     for (int v = 0; v < 4; ++v) acc[u][v] = 0.0f;
 #pragma unroll 4
                 for (int k = 0; k < 32; ++k) {
                     const float4 x4 = *reinterpret_cast<const float4*>(XT + k * LT_LD + c0);
-                    float ar[4];
+                    float ar[2];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) ar[u] = (r0 + u < n) ? S[(r0 + u) * LD + b + k] : 0.0f;
+                    for (int u = 0; u < 2; ++u) ar[u] = (r0 + u < n) ? S[(r0 + u) * LD + b + k] : 0.0f;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
+                    for (int u = 0; u < 2; ++u) {
                         acc[u][0] = fmaf(ar[u], x4.x, acc[u][0]);
                         acc[u][1] = fmaf(ar[u], x4.y, acc[u][1]);
                         acc[u][2] = fmaf(ar[u], x4.z, acc[u][2]);
@@ -390,17 +379,11 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(const float* __restrict
             }
             __syncthreads();  // X[b, :b] is read above before it is overwritten below
             if (kind == 0) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (r0 + u < n) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) S[(r0 + u) * LD + b + c0 + v] = acc[u][v];
-                    }
+                // L21 is needed only transposed, in Lt (its rows of S are never read again)
 #pragma unroll
                 for (int v = 0; v < 4; ++v)
-                    *reinterpret_cast<float4*>(Lt + (c0 + v) * LDX + r0) =
-                        make_float4(acc[0][v], r0 + 1 < n ? acc[1][v] : 0.0f, r0 + 2 < n ? acc[2][v] : 0.0f,
-                                    r0 + 3 < n ? acc[3][v] : 0.0f);
+                    *reinterpret_cast<float2*>(Lt + (c0 + v) * LDX + r0) =
+                        make_float2(r0 < n ? acc[0][v] : 0.0f, r0 + 1 < n ? acc[1][v] : 0.0f);
             } else if (kind == 1) {
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
@@ -412,45 +395,52 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(const float* __restrict
         if (m <= 0) break;
         __syncthreads();
         // ---- 3. A22 -= L21 L21^T (lower tiles) and B[below, :b+32] -= L21 X[b, :b+32] ----
-        // Warp 0 updates the next diagonal block (4 x 4 tiles) and then factors it, while
-        // the 12 warps outside its SM sub-partition (warp % 4 != 0) do the rest in 8 x 4
-        // tiles (three 16-byte loads per 32 FMAs, so the shared-memory traffic leaves room
-        // for the factorisation); warps 4, 8 and 12 stay idle so the latency-bound
-        // factorisation has its issue slots to itself.
+        // Warps 1-3 update the next diagonal block first (4 x 4 tiles, one per thread) and
+        // hand it to warp 0 through a named barrier; warp 0 factors it while the 12 warps
+        // outside its SM sub-partition (warp % 4 != 0) do the rest in 8 x 4 tiles (three
+        // 16-byte loads per 32 FMAs, so the shared-memory traffic leaves room for the
+        // factorisation); warps 4, 8 and 12 stay idle so the latency-bound factorisation
+        // has its issue slots to itself.
         if (tid < 32) {
-            const int D = min(tm, 8), Td = D * (D + 1) / 2;
-            for (int t = tid; t < Td; t += 32) {
-                int ti, tj;
-                tri_tile(t, ti, tj);
-                const int r0 = rb + 4 * ti, c0 = rb + 4 * tj;
-                float acc[4][4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) acc[u][v] = 0.0f;
-#pragma unroll 4
-                for (int k = 0; k < 32; ++k) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(Lt + k * LDX + r0);
-                    const float4 b4 = *reinterpret_cast<const float4*>(Lt + k * LDX + c0);
-                    const float ar[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        acc[u][0] = fmaf(ar[u], b4.x, acc[u][0]);
-                        acc[u][1] = fmaf(ar[u], b4.y, acc[u][1]);
-                        acc[u][2] = fmaf(ar[u], b4.z, acc[u][2]);
-                        acc[u][3] = fmaf(ar[u], b4.w, acc[u][3]);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        if (r0 + u < n && c0 + v <= r0 + u) S[(r0 + u) * LD + c0 + v] -= acc[u][v];
-            }
-            __syncwarp();
+            bar_sync_diag();   // warps 1-3 have updated the next diagonal block
             chol_inv_32<LD, LDX>(S + rb * LD + rb, X + rb * LDX + rb, XT, min(32, m), lt, status);
         } else if ((tid >> 5) & 3) {
             const int w = tid >> 5, p = (w - 1 - (w >> 2)) * 32 + (tid & 31);  // 0 .. 383
+            if (w < 4) {
+                // warps 1-3 (one per other SM sub-partition): the next diagonal block first,
+                // A22' -= L21' L21'^T in 4 x 4 tiles (at most 36: one per thread)
+                const int D = min(tm, 8), Td = D * (D + 1) / 2;
+                if (p < Td) {
+                    const int t = p;
+                    int ti, tj;
+                    tri_tile(t, ti, tj);
+                    const int r0 = rb + 4 * ti, c0 = rb + 4 * tj;
+                    float acc[4][4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) acc[u][v] = 0.0f;
+#pragma unroll 4
+                    for (int k = 0; k < 32; ++k) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(Lt + k * LDX + r0);
+                        const float4 b4 = *reinterpret_cast<const float4*>(Lt + k * LDX + c0);
+                        const float ar[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            acc[u][0] = fmaf(ar[u], b4.x, acc[u][0]);
+                            acc[u][1] = fmaf(ar[u], b4.y, acc[u][1]);
+                            acc[u][2] = fmaf(ar[u], b4.z, acc[u][2]);
+                            acc[u][3] = fmaf(ar[u], b4.w, acc[u][3]);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            if (r0 + u < n && c0 + v <= r0 + u) S[(r0 + u) * LD + c0 + v] -= acc[u][v];
+                }
+                bar_arrive_diag();
+            }
             const int t8 = (m + 7) >> 3;                  // 8-row tiles below the sub-panel
             // SYRK: 8 x 8 blocks below the next diagonal block, each as two 8 x 4 tiles
             const int Ts = 2 * max(0, t8 * (t8 + 1) / 2 - 10);
