@@ -265,7 +265,9 @@ __device__ __forceinline__ void tri_tile(int t, int& ti, int& tj) {
 }
 
 // One CTA factors the diagonal block A[k0:k0+n, k0:k0+n] = L L^T and forms L^-1 (lower,
-// NB x NB, zeros above): optionally written to Linv, and as its TF32 split to Lhi/Llo.
+// NB x NB, zeros above): optionally written to Linv, and as its TF32 split to Lhi/Llo
+// (its zero upper triangle only when split_upper; otherwise the buffer must hold zeros
+// there already).
 // A is only read: the callers need L^-1 alone. A non-positive or non-finite pivot records
 // GPTQ_ERR_NOT_SPD (the kernel still finishes; its outputs are then not finite).
 //
@@ -285,7 +287,8 @@ constexpr size_t potrf_smem_bytes() {
 }
 __global__ void __launch_bounds__(512) potrf_diag_kernel(const float* __restrict__ A, int64_t lda, int64_t k0, int n,
                                                         float* __restrict__ Linv, float* __restrict__ Lhi,
-                                                        float* __restrict__ Llo, int* __restrict__ status) {
+                                                        float* __restrict__ Llo, int split_upper,
+                                                        int* __restrict__ status) {
     extern __shared__ __align__(16) float sm[];
     constexpr int LD = POTRF_LDS, LDX = POTRF_LDX;
     float* S = sm;                   // NB x LD: the block (lower triangle), updated in place
@@ -513,7 +516,10 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(const float* __restrict
         if (j4 + 2 > i || j4 + 2 >= n) v.z = 0.0f;
         if (j4 + 3 > i || j4 + 3 >= n) v.w = 0.0f;
         if (Linv) *reinterpret_cast<float4*>(Linv + 4 * idx) = v;
-        if (Lhi) {  // TF32 split for the tensor-core products that use L_kk^-1
+        // TF32 split for the tensor-core products that use L_kk^-1; the groups of four
+        // entirely above the diagonal are zero and, unless split_upper, already zero in
+        // the buffer (written by an earlier call on it)
+        if (Lhi && (split_upper || j4 <= i)) {
             float4 h;
             h.x = __uint_as_float(__float_as_uint(v.x) & 0xFFFFE000u);
             h.y = __uint_as_float(__float_as_uint(v.y) & 0xFFFFE000u);
@@ -704,12 +710,14 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
             }
             if (cs_k) {
                 cudaError_t le = cudaSuccess;
-                GPTQ_LAUNCH(K_POTRF, cs, le = launch_pdl(potrf_diag_kernel, dim3(1), dim3(512), potrf_smem, cs, w.A,
-                                                         d, k0, n, (float*)nullptr, lhi, llo, w.status));
+                // each of the two L_kk^-1 buffers gets its zero upper triangle on its first use
+                GPTQ_LAUNCH(K_POTRF, cs, le = launch_pdl(potrf_diag_kernel, dim3(1), dim3(512), potrf_smem, cs,
+                                                         (const float*)w.A, d, k0, n, (float*)nullptr, lhi, llo,
+                                                         (int)(kb < 2), w.status));
                 GPTQ_CUDA_TRY(le);
             } else {
                 GPTQ_LAUNCH(K_POTRF, cs, potrf_diag_kernel<<<1, 512, potrf_smem, cs>>>(w.A, d, k0, n, nullptr, lhi,
-                                                                                      llo, w.status));
+                                                                                      llo, (int)(kb < 2), w.status));
             }
             GPTQ_LAUNCH_CHECK();
             cs_k = true;
@@ -825,7 +833,7 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
             const int n = (int)std::min<int64_t>(NB, d - k0);
             float* LinvK = w.LinvD + kb * NB * NB;
             GPTQ_LAUNCH(K_POTRF, s, potrf_diag_kernel<<<1, 512, potrf_smem, s>>>(w.A, d, k0, n, LinvK, nullptr,
-                                                                                 nullptr, w.status));
+                                                                                 nullptr, 1, w.status));
             GPTQ_LAUNCH_CHECK();
             const int64_t m = d - k0 - n;
             if (m <= 0) continue;
