@@ -664,6 +664,7 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
         GemmOpts side_opts, chain_opts;
         side_opts.max_ctas = two ? std::max(1, device_sm_count() - kChainSMs) : 0;
         chain_opts.max_ctas = two ? kChainSMs : 0;
+        chain_opts.narrow_ok = true;   // the factorisation chain is latency-bound
         // Programmatic dependent launch only where the previous item in the stream is one
         // of these kernels (not an event wait): cs_k / ss_k say whether it is.
         bool cs_k = !two, ss_k = false;

@@ -7,12 +7,13 @@
 // (the dropped Alo*Blo and the TF32 rounding of the lo parts), against 2^-11 for one TF32
 // pass. Accumulation is fp32 in TMEM.
 //
-// Structure (one CTA per SM, persistent over 128 x 128 output tiles):
-//   warp 0      TMA producer: per 32-wide K step, the four 128 x 32 fp32 boxes
-//               (Ahi, Alo, Bhi, Blo; 128-byte swizzle, K-major) into a 2-stage ring
-//   warp 1      single-thread tcgen05.mma issuer, kind::tf32, M = N = 128, K = 8 per
+// Structure (one CTA per SM, persistent over 128 x BN output tiles, BN = 128, or 64 for a
+// latency-critical launch too small to fill its SMs with 128-wide tiles):
+//   warp 0      TMA producer: per 32-wide K step, the four fp32 boxes Ahi, Alo (128 x 32)
+//               and Bhi, Blo (BN x 32) (128-byte swizzle, K-major) into a 2-stage ring
+//   warp 1      single-thread tcgen05.mma issuer, kind::tf32, M = 128, N = BN, K = 8 per
 //               instruction, three products per K step, into one of two TMEM
-//               accumulators (128 columns each)
+//               accumulators (BN columns each)
 //   warps 2..5  epilogue: TMEM -> registers, combined with the C tile that the producer
 //               brought into shared memory by TMA, stored back by TMA in four 32-column
 //               chunks (the next tile's chunk loads as soon as this one's has been read
@@ -31,21 +32,32 @@ namespace gptq {
 
 namespace {
 
-constexpr int G_BM = 128, G_BN = 128, G_BK = 32, G_STAGES = 2, G_THREADS = 192;
-constexpr int G_BOX = G_BM * G_BK * 4;         // 16 KB: one 128 x 32 fp32 box
-constexpr int G_STAGE = 4 * G_BOX;             // Ahi, Alo, Bhi, Blo
-constexpr int G_CBUF = 4 * G_BOX;              // the 128 x 128 C tile as four 32-column boxes
-constexpr int G_SMEM = G_STAGES * G_STAGE + G_CBUF + 1024 + 256;
-constexpr uint32_t G_TMEM_COLS = 2 * G_BN;
+// Output tiles are 128 rows x BN columns, BN = 128, or 64 for launches too small to fill
+// their SMs with 128-wide tiles (twice the CTAs, each with half the MMAs and epilogue).
+constexpr int G_BM = 128, G_BK = 32, G_THREADS = 192;
+constexpr int G_BOX = G_BM * G_BK * 4;         // 16 KB: one 128 x 32 fp32 box (A, and a C chunk)
+template <int BN>
+struct GTile {
+    static constexpr int BBOX = BN * G_BK * 4;                      // one BN x 32 fp32 box of B
+    static constexpr int STAGE = 2 * G_BOX + 2 * BBOX;              // Ahi, Alo, Bhi, Blo
+    static constexpr int STAGES = 2;                                 // ring depth
+    static constexpr int NCH = BN / 32;                             // 32-column C chunks
+    static constexpr int CBUF = NCH * G_BOX;                        // the 128 x BN C tile
+    static constexpr int SMEM = STAGES * STAGE + CBUF + 1024 + 256;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;                   // two accumulators
+    // kind::tf32: D fp32 (bits 4-5 = 1), A/B TF32 (2), both K-major, N >> 3, M >> 4
+    static constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                      ((uint32_t)(G_BM >> 4) << 24);
+};
 
-// kind::tf32: D fp32 (bits 4-5 = 1), A/B TF32 (2), both K-major, N >> 3, M >> 4
-constexpr uint32_t G_IDESC = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(G_BN >> 3) << 17) |
-                             ((uint32_t)(G_BM >> 4) << 24);
+static_assert(GTile<64>::SMEM <= 232448 && GTile<128>::SMEM <= 232448, "shared memory per CTA");
+static_assert(2 * GTile<64>::STAGES + 12 < 30 && 2 * GTile<128>::STAGES + 12 < 30, "barrier slots");
 
 struct GParams {
     int M, N, K;
     float alpha, beta;
     int tiles_m, tiles_n, ntiles, lower_only;
+    int bn;     // tile width in columns
     int* status;
     // optional TF32 split of the result: mode 1 hi[r][c], mode 2 (transposed) hi[c][r]
     float* ohi;
@@ -103,7 +115,14 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, int* s
     return true;
 }
 
-// linear tile index -> (tm, tn); with lower_only the tiles tn <= tm, row by row
+// tiles of tile row r that reach the diagonal or below it (lower_only)
+__host__ __device__ __forceinline__ int lower_tiles_in_row(int r, int bn, int tiles_n) {
+    const int c = (r * G_BM + G_BM - 1) / bn + 1;
+    return c < tiles_n ? c : tiles_n;
+}
+
+// linear tile index -> (tm, tn); with lower_only the tiles that reach the diagonal or
+// below it, row by row
 __device__ __forceinline__ void tile_of(const GParams& p, int t, int& tm, int& tn) {
     if (!p.lower_only) {
         tm = t / p.tiles_n;
@@ -112,7 +131,7 @@ __device__ __forceinline__ void tile_of(const GParams& p, int t, int& tm, int& t
     }
     int r = 0;
     for (;;) {
-        const int c = min(r + 1, p.tiles_n);
+        const int c = lower_tiles_in_row(r, p.bn, p.tiles_n);
         if (t < c) break;
         t -= c;
         ++r;
@@ -124,6 +143,7 @@ __device__ __forceinline__ void tile_of(const GParams& p, int t, int& tm, int& t
 // The C tile moves through shared memory by TMA in both directions: the producer loads it
 // (when beta != 0) while the MMAs of the tile run, the epilogue combines it with the
 // accumulator in place and stores it back with TMA, so no thread waits on a global load.
+template <int BN>
 __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_constant__ CUtensorMap tAh,
                                                                   const __grid_constant__ CUtensorMap tAl,
                                                                   const __grid_constant__ CUtensorMap tBh,
@@ -132,10 +152,13 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                                                                   const GParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* cbuf = smem + G_STAGES * G_STAGE;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(cbuf + G_CBUF);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
+    using T = GTile<BN>;
+    constexpr int G_STAGES = T::STAGES;
+    uint8_t* cbuf = smem + G_STAGES * T::STAGE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(cbuf + T::CBUF);
+    // barriers occupy slots 0 .. 2 * STAGES + 12 (at most 20) of the 32 in the 256-byte area
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 30);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 31);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sbase = smem_u32(smem), cbase = smem_u32(cbuf), bar0 = smem_u32(bars);
@@ -159,7 +182,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
             mbar_init(tfull_bar(b), 1);
             mbar_init(tempty_bar(b), 4);
         }
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < T::NCH; ++c) {
             mbar_init(cfull_bar(c), 1);
             mbar_init(cempty_bar(c), 1);
         }
@@ -175,7 +198,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
         tma_prefetch_desc(&tC);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), G_TMEM_COLS);
+        tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -200,13 +223,13 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(full_bar(stage), G_STAGE);
-                    const uint32_t sa = sbase + stage * G_STAGE;
+                    mbar_expect_tx(full_bar(stage), T::STAGE);
+                    const uint32_t sa = sbase + stage * T::STAGE;
                     const int x = kt * G_BK;
                     tma_load_2d(sa, &tAh, full_bar(stage), x, tm * G_BM);
                     tma_load_2d(sa + G_BOX, &tAl, full_bar(stage), x, tm * G_BM);
-                    tma_load_2d(sa + 2 * G_BOX, &tBh, full_bar(stage), x, tn * G_BN);
-                    tma_load_2d(sa + 3 * G_BOX, &tBl, full_bar(stage), x, tn * G_BN);
+                    tma_load_2d(sa + 2 * G_BOX, &tBh, full_bar(stage), x, tn * BN);
+                    tma_load_2d(sa + 2 * G_BOX + T::BBOX, &tBl, full_bar(stage), x, tn * BN);
                     issued |= 1u << stage;
                     issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == G_STAGES) {
@@ -218,13 +241,13 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                 if (load_c) {
                     // chunk c of the C buffer is free once the previous tile's store of it
                     // has been read
-                    for (int c = 0; c < 4 && ok; ++c) {
+                    for (int c = 0; c < T::NCH && ok; ++c) {
                         if (!mbar_wait(cempty_bar(c), cph ^ 1u, abort_flag, p.status)) {
                             ok = false;
                             break;
                         }
                         mbar_expect_tx(cfull_bar(c), G_BOX);
-                        tma_load_2d(cbase + c * G_BOX, &tC, cfull_bar(c), tn * G_BN + 32 * c, tm * G_BM);
+                        tma_load_2d(cbase + c * G_BOX, &tC, cfull_bar(c), tn * BN + 32 * c, tm * G_BM);
                         c_issued |= 1u << c;
                         c_par = (c_par & ~(1u << c)) | (cph << c);
                     }
@@ -234,7 +257,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
             }
             for (int s = 0; s < G_STAGES; ++s)
                 if (issued & (1u << s)) drain_wait(full_bar(s), (issued_par >> s) & 1u, p.status);
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < T::NCH; ++c)
                 if (c_issued & (1u << c)) drain_wait(cfull_bar(c), (c_par >> c) & 1u, p.status);
         }
     } else if (warp == 1) {
@@ -246,14 +269,14 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
             for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
                 if (!mbar_wait(tempty_bar(abuf), aphase ^ 1u, abort_flag, p.status)) break;
                 tc_fence_after();
-                const uint32_t dt = tmem_base + (uint32_t)(abuf * G_BN);
+                const uint32_t dt = tmem_base + (uint32_t)(abuf * BN);
                 for (int kt = 0; kt < ktiles; ++kt) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = sbase + stage * G_STAGE;
+                    const uint32_t sa = sbase + stage * T::STAGE;
 #pragma unroll
                     for (int kk = 0; kk < G_BK / 8; ++kk) {
                         // 8 TF32 = 32 bytes along K inside the 128-byte swizzle row
@@ -261,10 +284,10 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                         const uint64_t ah = smem_desc(sa + off, 16, 1024, kSwizzle128B);
                         const uint64_t al = smem_desc(sa + G_BOX + off, 16, 1024, kSwizzle128B);
                         const uint64_t bh = smem_desc(sa + 2 * G_BOX + off, 16, 1024, kSwizzle128B);
-                        const uint64_t bl = smem_desc(sa + 3 * G_BOX + off, 16, 1024, kSwizzle128B);
-                        umma_tf32(dt, ah, bh, G_IDESC, (kt > 0 || kk > 0) ? 1u : 0u);
-                        umma_tf32(dt, ah, bl, G_IDESC, 1u);
-                        umma_tf32(dt, al, bh, G_IDESC, 1u);
+                        const uint64_t bl = smem_desc(sa + 2 * G_BOX + T::BBOX + off, 16, 1024, kSwizzle128B);
+                        umma_tf32(dt, ah, bh, T::IDESC, (kt > 0 || kk > 0) ? 1u : 0u);
+                        umma_tf32(dt, ah, bl, T::IDESC, 1u);
+                        umma_tf32(dt, al, bh, T::IDESC, 1u);
                     }
                     umma_commit(empty_bar(stage));
                     if (++stage == G_STAGES) {
@@ -296,9 +319,9 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
             if (!epi_all(mbar_wait(tfull_bar(abuf), aphase, abort_flag, p.status))) break;
             tc_fence_after();
             const int row = tm * G_BM + rl;
-            const uint32_t ta = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(abuf * G_BN);
+            const uint32_t ta = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(abuf * BN);
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < T::NCH; ++c) {
                 if (load_c && !epi_all(mbar_wait(cfull_bar(c), cph, abort_flag, p.status))) {
                     alive = false;
                     break;
@@ -321,7 +344,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                         o.w = fmaf(p.beta, cv.w, o.w);
                     }
                     *ptr = o;
-                    const int gc0 = tn * G_BN + 32 * c + 4 * j;
+                    const int gc0 = tn * BN + 32 * c + 4 * j;
                     if (p.omode == 1 && row < p.M && row >= p.orow0 && gc0 + 3 < p.N && p.ovec) {
                         // row-major split, four columns at once (16-byte stores)
                         float4 h4;
@@ -336,7 +359,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                         const float o4[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int gc = tn * G_BN + 32 * c + 4 * j + e;
+                            const int gc = tn * BN + 32 * c + 4 * j + e;
                             if (gc < p.N) {
                                 const float h = __uint_as_float(__float_as_uint(o4[e]) & 0xFFFFE000u);
                                 const int64_t orow = row - p.orow0;
@@ -353,7 +376,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                     // store chunk c; once the store of chunk c-1 has read its buffer, the
                     // producer may load the next tile's chunk c-1 there. (Writes of the next
                     // tile's chunk c-1 by the other threads come after a later barrier.)
-                    tma_store_2d(&tC, cbase + c * G_BOX, tn * G_BN + 32 * c, tm * G_BM);
+                    tma_store_2d(&tC, cbase + c * G_BOX, tn * BN + 32 * c, tm * G_BM);
                     bulk_commit();
                     if (c > 0) {
                         bulk_wait_read1();
@@ -367,7 +390,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
             if (lane == 0) mbar_arrive(tempty_bar(abuf));   // the accumulator is free again
             if (storer) {
                 bulk_wait_read0();
-                if (load_c) mbar_arrive(cempty_bar(3));
+                if (load_c) mbar_arrive(cempty_bar(T::NCH - 1));
             }
             if (++abuf == 2) {
                 abuf = 0;
@@ -383,7 +406,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, G_TMEM_COLS);
+        tmem_dealloc(tmem_base, T::TMEM_COLS);
     }
 }
 
@@ -451,12 +474,12 @@ __global__ void __launch_bounds__(256) split_cols_kernel(const float* __restrict
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() { return tma_encoder(); }
 
-bool make_map(CUtensorMap* m, const float* base, int rows, int K, int64_t ldk) {
+bool make_map(CUtensorMap* m, const float* base, int rows, int K, int64_t ldk, int box_rows = G_BM) {
     auto enc = encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ldk * 4};
-    cuuint32_t box[2] = {(cuuint32_t)G_BK, (cuuint32_t)G_BM};
+    cuuint32_t box[2] = {(cuuint32_t)G_BK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -524,9 +547,26 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
                        cudaStream_t s, GemmOpts out) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     if (out.ldb == 0) out.ldb = ldk;
+    static const int sms = device_sm_count();
+    const int cap = out.max_ctas > 0 ? std::min(out.max_ctas, sms) : sms;
+    auto count_tiles = [&](int bn, int& tiles_n) {
+        const int tiles_m = (M + G_BM - 1) / G_BM;
+        tiles_n = (N + bn - 1) / bn;
+        if (!lower_only) return tiles_m * tiles_n;
+        int cnt = 0;
+        for (int r = 0; r < tiles_m; ++r) cnt += lower_tiles_in_row(r, bn, tiles_n);
+        return cnt;
+    };
+    // 64-column tiles for a latency-critical launch whose 64-wide tiles still fit in one
+    // wave of its CTAs: twice the CTAs, each with half the epilogue (the per-CTA MMA time
+    // stays: a tcgen05.mma with N = 64 takes about as long as one with N = 128)
+    int tn128 = 0, tn64 = 0;
+    const int nt128 = count_tiles(128, tn128), nt64 = count_tiles(64, tn64);
+    const int bn = (out.narrow_ok && nt128 < cap && nt64 <= cap) ? 64 : 128;
     CUtensorMap tah, tal, tbh, tbl, tcm;
-    if (!make_map(&tah, Ahi, M, K, ldk) || !make_map(&tal, Alo, M, K, ldk) || !make_map(&tbh, Bhi, N, K, out.ldb) ||
-        !make_map(&tbl, Blo, N, K, out.ldb) || !make_map(&tcm, C, M, N, ldc))
+    if (!make_map(&tah, Ahi, M, K, ldk) || !make_map(&tal, Alo, M, K, ldk) ||
+        !make_map(&tbh, Bhi, N, K, out.ldb, bn) || !make_map(&tbl, Blo, N, K, out.ldb, bn) ||
+        !make_map(&tcm, C, M, N, ldc))
         return cudaErrorInvalidValue;
     GParams p;
     p.M = M;
@@ -534,16 +574,11 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
     p.K = K;
     p.alpha = alpha;
     p.beta = beta;
+    p.bn = bn;
     p.tiles_m = (M + G_BM - 1) / G_BM;
-    p.tiles_n = (N + G_BN - 1) / G_BN;
+    p.tiles_n = bn == 64 ? tn64 : tn128;
     p.lower_only = lower_only ? 1 : 0;
-    if (lower_only) {
-        int cnt = 0;
-        for (int r = 0; r < p.tiles_m; ++r) cnt += std::min(r + 1, p.tiles_n);
-        p.ntiles = cnt;
-    } else {
-        p.ntiles = p.tiles_m * p.tiles_n;
-    }
+    p.ntiles = bn == 64 ? nt64 : nt128;
     p.status = status;
     p.ohi = out.hi;
     p.olo = out.lo;
@@ -553,16 +588,17 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
     p.ovec = (out.hi && (out.ld % 4 == 0) &&
               ((reinterpret_cast<uintptr_t>(out.hi) | reinterpret_cast<uintptr_t>(out.lo)) % 16 == 0)) ? 1 : 0;
     if (p.ntiles == 0) return cudaSuccess;
-    static const int sms = device_sm_count();
-    const int grid = std::min(p.ntiles, out.max_ctas > 0 ? std::min(out.max_ctas, sms) : sms);
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_nt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
+    const int grid = std::min(p.ntiles, cap);
+    auto kern = bn == 64 ? tc_gemm_nt_kernel<64> : tc_gemm_nt_kernel<128>;
+    const int smem = bn == 64 ? GTile<64>::SMEM : GTile<128>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (out.pdl) {
-        GPTQ_LAUNCH(id, s, e = launch_pdl(tc_gemm_nt_kernel, dim3(grid), dim3(G_THREADS), (size_t)G_SMEM, s, tah, tal,
-                                          tbh, tbl, tcm, p));
+        GPTQ_LAUNCH(id, s, e = launch_pdl(kern, dim3(grid), dim3(G_THREADS), (size_t)smem, s, tah, tal, tbh, tbl, tcm,
+                                          p));
         if (e != cudaSuccess) return e;
     } else {
-        GPTQ_LAUNCH(id, s, tc_gemm_nt_kernel<<<grid, G_THREADS, G_SMEM, s>>>(tah, tal, tbh, tbl, tcm, p));
+        GPTQ_LAUNCH(id, s, kern<<<grid, G_THREADS, smem, s>>>(tah, tal, tbh, tbl, tcm, p));
     }
     return cudaGetLastError();
 }

@@ -35,7 +35,9 @@ cudaError_t split_cols(int id, const float* B, int64_t ld, int K, int N, float* 
 // (transposed) hi[c][r], with row stride ld; max_ctas, a cap on the persistent grid
 // (0 = one CTA per SM) that leaves SMs free for work on another stream; and pdl, launch
 // as a programmatic dependent of the previous kernel in the stream (set up shared
-// memory and TMEM while it finishes); row0, the first row of C the split output covers.
+// memory and TMEM while it finishes); row0, the first row of C the split output covers;
+// narrow_ok, a latency-critical launch that may use 128 x 64 tiles (twice the CTAs, each
+// with half the epilogue) when those still fit in one wave.
 struct GemmOpts {
     float* hi = nullptr;
     float* lo = nullptr;
@@ -45,6 +47,7 @@ struct GemmOpts {
     int max_ctas = 0;
     bool pdl = false;
     int64_t row0 = 0;   // the split output covers rows >= row0 of C, stored from row 0
+    bool narrow_ok = false;   // latency-critical: 64-column tiles allowed when they fit one wave
 };
 bool tc_gemm_nt_ok(const float* C, int64_t ldc);
 cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ahi, const float* Alo, const float* Bhi,
