@@ -320,9 +320,12 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
         const float id = invd[jj];
         const float4 uc = *reinterpret_cast<const float4*>(ur + 4 * cc);
         const float4 un = *reinterpret_cast<const float4*>(ur + min(4 * cc + 4, QB - 4));
+        // this thread's chunks mm < m lie left of the current chunk for every lane (U is zero
+        // there): neither loaded nor updated (m is a compile-time constant at each call)
         float4 uo[NCH];
 #pragma unroll
-        for (int mm = 0; mm < NCH; ++mm) uo[mm] = *reinterpret_cast<const float4*>(ur + col_of(mm, 0));
+        for (int mm = 0; mm < NCH; ++mm)
+            if (mm >= m) uo[mm] = *reinterpret_cast<const float4*>(ur + col_of(mm, 0));
         const float wj = cur[e];
         const float cf = grid_code_f(wj, g, sym, flo, fhi);
         const float q = grid_dequant_f(cf, g, sym);
@@ -342,6 +345,7 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
         nxt[3] = fmaf(-err, un.w, nxt[3]);
 #pragma unroll
         for (int mm = 0; mm < NCH; ++mm) {
+            if (mm < m) continue;
             const float4 u4 = uo[mm];
             w[4 * mm] = fmaf(-err, u4.x, w[4 * mm]);
             w[4 * mm + 1] = fmaf(-err, u4.y, w[4 * mm + 1]);
@@ -660,6 +664,7 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
                 GemmOpts o;
                 o.ldb = cols;
                 o.pdl = true;
+                o.narrow_ok = true;   // on the loop's critical path: 128x64 tiles when they fit one wave
                 if (e < sb_end) {
                     GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_TRAIL, (int)rows, (int)(sb_end - e), bw, -1.0f, w.ehi + (j0 - sb0),
                                              w.elo + (j0 - sb0), w.uhi + e * cols + j0, w.ulo + e * cols + j0, SB * QB,
