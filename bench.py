@@ -455,6 +455,9 @@ def run_ours(args, ws, rank, local):
 
     wl, layers = build_layers(args.config, dev)
     runner = Runner(lib, layers, dev)
+    # deferred status reporting: the calls of a step only enqueue work (no host round trip
+    # between them); device-side errors are checked once per step with status_sync
+    lib.set_status_mode(True)
     in_bytes = sum(L.X.numel() * L.X.element_size() + sum(W.numel() * 4 for W in L.Ws) for L in layers)
     flush = in_bytes < 2 * L2_BYTES
     fbuf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
@@ -465,6 +468,7 @@ def run_ours(args, ws, rank, local):
 
     for _ in range(args.warmup):
         runner.step()
+    lib.status_sync()
     torch.cuda.synchronize()
 
     clocks = Clocks(local)
@@ -481,7 +485,7 @@ def run_ours(args, ws, rank, local):
         a.record()
         runner.step()
         b.record()
-        b.synchronize()
+        lib.status_sync()   # synchronises the stream: the step's errors, after its end event
         times.append(a.elapsed_time(b))
     torch.cuda.synchronize()
     barrier()
@@ -500,6 +504,7 @@ def run_ours(args, ws, rank, local):
             if flush:
                 flush_l2(fbuf)
             runner.step(events=evs)
+            lib.status_sync()
         torch.cuda.synchronize()
         lib.gptq_profile_enable(False)
         prof = lib.gptq_profile_read()
@@ -555,7 +560,7 @@ def run_ours(args, ws, rank, local):
             for i, o in enumerate(outs):
                 for k in h_out[i]:
                     h_out[i][k].copy_(o[k], non_blocking=True)
-            torch.cuda.current_stream().synchronize()
+            lib.status_sync()   # synchronises the stream, then raises on a device-side error
 
         for _ in range(max(1, args.warmup)):
             e2e_step()

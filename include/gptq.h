@@ -89,7 +89,8 @@ int gptq_hessian_accumulate(gptq_hessian* h, const void* X, int dtype, int64_t n
 
 /* H = 2 S / n written to H (device, d*d fp32, both triangles), diag_xtx[j] = S[j][j]
  * (device, d fp32, the raw diag(X^T X) act_order sorts on; may be NULL), *n_tokens = n
- * (host; may be NULL). Synchronises `stream` to report a device-side timeout.
+ * (host; may be NULL). Synchronises `stream` to report a device-side timeout (not in the
+ * deferred status mode, below).
  * Errors: INVALID_ARG (n == 0), TIMEOUT, CUDA. */
 int gptq_hessian_finalize(gptq_hessian* h, float* H, float* diag_xtx, int64_t* n_tokens,
                           void* stream);
@@ -110,7 +111,8 @@ int gptq_hessian_destroy(gptq_hessian* h);
  * the diagonal), perm (d int32: loop position k quantises original column perm[k]),
  * dead (d uint8, original column order).
  * ws: device workspace of at least gptq_prepare_workspace_bytes(d, act_order) bytes.
- * Synchronises `stream` at the end to report a failed factorisation.
+ * Synchronises `stream` at the end to report a failed factorisation (not in the deferred
+ * status mode, below: the status is then kept for gptq_status_sync).
  * Errors: INVALID_ARG, WORKSPACE, NOT_SPD, CUDA. */
 size_t gptq_prepare_workspace_bytes(int64_t d, int act_order);
 int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, float damp, int act_order,
@@ -149,7 +151,8 @@ int gptq_prepare_noalloc(const float* H, const float* diag_xtx, int64_t d, float
  *           LSB-first bitstream of unsigned codes u (sym u = code + 2^(bits-1))
  *   row_loss rows fp32 (may be NULL): sum_k err_k^2 per row
  * ws: device workspace of at least gptq_quantize_workspace_bytes(rows, cols, q) bytes.
- * Synchronises `stream` at the end to report a device-side timeout.
+ * Synchronises `stream` at the end to report a device-side timeout (not in the deferred
+ * status mode, below).
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, TIMEOUT, CUDA. */
 size_t gptq_quantize_workspace_bytes(int64_t rows, int64_t cols, gptq_qconfig q);
 int gptq_quantize(const float* W, int64_t rows, int64_t cols, const float* U,
@@ -196,7 +199,7 @@ int gptq_pack(const int8_t* codes, int64_t rows, int64_t cols, int bits, int sym
  *   Y       device, (T, N) row-major, row stride ldy elements
  * The weights are expanded to bf16 on chip (rounding each to 8 significant bits) and
  * multiplied on the tensor cores with fp32 accumulation. Synchronises the stream and
- * returns the device status. Errors: INVALID_ARG, UNSUPPORTED (bits not 2-4, K % 64,
+ * returns the device status (in the deferred status mode, below, neither). Errors: INVALID_ARG, UNSUPPORTED (bits not 2-4, K % 64,
  * alignment, K or G too large for the shared-memory plan), TIMEOUT, CUDA. */
 enum { GPTQ_DQ_RELU = 1, GPTQ_DQ_BF16_OUT = 2 };
 int gptq_dequant_matmul(const void* X, int64_t T, int64_t K, int64_t ldx, const uint32_t* packed,
@@ -205,6 +208,26 @@ int gptq_dequant_matmul(const void* X, int64_t T, int64_t K, int64_t ldx, const 
 
 /* Static text for a status code. */
 const char* gptq_status_string(int status);
+
+/* ------------------------------------------------------------------------------------
+ * Status reporting (no counterpart on the pages). Errors found on the host (arguments,
+ * workspace, CUDA calls) are always returned at once. Errors found on the device (a
+ * timed-out wait, a non-positive-definite block) are reported, in the default mode
+ * GPTQ_STATUS_SYNC, by the call itself, which synchronises its stream before returning.
+ * In mode GPTQ_STATUS_DEFERRED the calls that say "Synchronises" do not: they return
+ * GPTQ_OK once their work is enqueued, and a final one-thread kernel of each call folds
+ * its device status into one sticky status word per device (the first error is kept).
+ * gptq_status_sync then reports it. The mode is process-wide.
+ * ------------------------------------------------------------------------------------ */
+enum { GPTQ_STATUS_SYNC = 0, GPTQ_STATUS_DEFERRED = 1 };
+/* Errors: INVALID_ARG (unknown mode). Host only. */
+int gptq_set_status_mode(int mode);
+int gptq_status_mode(void);
+/* Synchronises `stream`, returns the current device's sticky status (GPTQ_OK if no call
+ * enqueued in deferred mode on this device since the last gptq_status_sync failed) and
+ * clears it. Calls made on other streams must be ordered before `stream` by the caller.
+ * Errors: CUDA. */
+int gptq_status_sync(void* stream);
 
 /* ------------------------------------------------------------------------------------
  * Instrumentation (no counterpart on the pages). Every kernel the library launches is

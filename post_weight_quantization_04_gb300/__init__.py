@@ -32,7 +32,7 @@ EXPORTS = [
     "gptq_hessian_destroy", "gptq_prepare_workspace_bytes", "gptq_prepare", "gptq_prepare_noalloc",
     "gptq_quantize_workspace_bytes",
     "gptq_quantize", "rtn_quantize", "gptq_packed_words_per_row", "gptq_pack", "gptq_dequant_matmul",
-    "gptq_status_string",
+    "gptq_status_string", "gptq_set_status_mode", "gptq_status_mode", "gptq_status_sync",
     "gptq_launch_count", "gptq_profile_enable", "gptq_profile_read", "gptq_profile_kernel_count",
     "gptq_profile_kernel_name",
 ]
@@ -75,6 +75,9 @@ def _declare(lib: ctypes.CDLL) -> None:
         "gptq_pack": (_I, [_P, _I64, _I64, _I, _I, _P, _P]),
         "gptq_dequant_matmul": (_I, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _I64, _I64, _I, _I, _P, _I64, _P]),
         "gptq_status_string": (ctypes.c_char_p, [_I]),
+        "gptq_set_status_mode": (_I, [_I]),
+        "gptq_status_mode": (_I, []),
+        "gptq_status_sync": (_I, [_P]),
         "gptq_launch_count": (ctypes.c_ulonglong, []),
         "gptq_profile_enable": (None, [_I]),
         "gptq_profile_read": (_I, [_P, _P, _I]),
@@ -296,6 +299,35 @@ def gptq_pack(codes: torch.Tensor, bits: int, sym: bool = True, out: Optional[to
     return p
 
 
+STATUS_SYNC, STATUS_DEFERRED = 0, 1
+
+
+def set_status_mode(deferred: bool) -> None:
+    """Deferred: the calls that synchronise to report device-side errors return once their
+    work is enqueued; `status_sync` reports the first such error since its last call."""
+    _check("gptq_set_status_mode", load().gptq_set_status_mode(STATUS_DEFERRED if deferred else STATUS_SYNC))
+
+
+def status_sync(stream=None) -> None:
+    """Synchronise the stream and raise the first device-side error recorded in deferred
+    mode since the last call (clearing it)."""
+    _check("gptq_status_sync", load().gptq_status_sync(_stream(stream)))
+
+
+class deferred_status:
+    """Context manager: deferred status reporting inside, the previous mode restored after
+    (pending errors are left for `status_sync`)."""
+
+    def __enter__(self):
+        self._prev = int(load().gptq_status_mode())
+        _check("gptq_set_status_mode", load().gptq_set_status_mode(STATUS_DEFERRED))
+        return self
+
+    def __exit__(self, *exc):
+        load().gptq_set_status_mode(self._prev)
+        return False
+
+
 DQ_RELU, DQ_BF16_OUT = 1, 2
 
 
@@ -376,5 +408,6 @@ __all__ = [
     "gptq_hessian_finalize", "gptq_prepare", "gptq_prepare_workspace_bytes", "gptq_quantize",
     "gptq_quantize_workspace_bytes", "rtn_quantize", "gptq_pack", "gptq_packed_words_per_row",
     "gptq_dequant_matmul", "gptq_layerwise", "gptq_status_string", "gptq_launch_count", "gptq_profile_enable", "gptq_profile_read",
+    "set_status_mode", "status_sync", "deferred_status", "STATUS_SYNC", "STATUS_DEFERRED",
     "EXPORTS", "LIB_PATH",
 ]

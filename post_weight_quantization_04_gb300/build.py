@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgptq.so")
 
-SOURCES = ["hessian.cu", "prepare.cu", "quantize.cu", "sgemm.cu", "tc_gemm.cu", "dequant_matmul.cu", "profile.cu"]
+SOURCES = ["hessian.cu", "prepare.cu", "quantize.cu", "sgemm.cu", "tc_gemm.cu", "dequant_matmul.cu", "profile.cu",
+           "status.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]
 

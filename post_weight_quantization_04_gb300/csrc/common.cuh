@@ -30,7 +30,7 @@ namespace gptq {
 enum KernelId {
     K_HESS_TC, K_HESS_SIMT, K_FINALIZE, K_PREP_DIAG, K_PREP_PERM, K_PREP_GATHER, K_POTRF, K_SGEMM_PREP,
     K_EYE, K_SCATTER, K_INIT_WORK, K_ROW_PARAMS, K_BLOCK, K_SGEMM_TRAIL, K_G_IDX, K_PACK, K_RTN,
-    K_SPLIT, K_TC_PREP, K_TC_TRAIL, K_DEQUANT_MM, K_COUNT
+    K_SPLIT, K_TC_PREP, K_TC_TRAIL, K_DEQUANT_MM, K_STATUS, K_COUNT
 };
 void prof_begin(int id, cudaStream_t s);
 void prof_end(int id, cudaStream_t s);
@@ -46,6 +46,10 @@ void prof_end(int id, cudaStream_t s);
 constexpr int kSMs = 152;  // fallback only; the real count is queried per device
 
 int device_sm_count();
+
+// The end of an entry point: report the call's device status word at once (synchronising
+// the stream) or, in deferred mode, fold it into the device's sticky status and return OK.
+int finish_call(const int* status, cudaStream_t s);
 
 static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

@@ -952,9 +952,7 @@ extern "C" int gptq_dequant_matmul(const void* X, int64_t T, int64_t K, int64_t 
     GPTQ_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
     GPTQ_LAUNCH(K_DEQUANT_MM, s, kern<<<grid, D_THREADS, smem, s>>>(tx, p));
     GPTQ_LAUNCH_CHECK();
-    int hstatus = 0;
-    GPTQ_CUDA_TRY(cudaMemcpyAsync(&hstatus, status, sizeof(int), cudaMemcpyDeviceToHost, s));
+    const int rc = finish_call(status, s);   // reads the status word before it is freed
     GPTQ_CUDA_TRY(cudaFreeAsync(words2, s));
-    GPTQ_CUDA_TRY(cudaStreamSynchronize(s));
-    return hstatus;
+    return rc;
 }

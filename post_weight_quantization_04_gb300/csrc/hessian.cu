@@ -533,10 +533,7 @@ extern "C" int gptq_hessian_finalize(gptq_hessian* h, float* H, float* diag_xtx,
     GPTQ_LAUNCH(K_FINALIZE, s, finalize_kernel<<<dim3(nt, nt), 256, 0, s>>>(h->S, h->d, scale, H, diag_xtx));
     GPTQ_LAUNCH_CHECK();
     if (n_tokens) *n_tokens = h->n;
-    int hs = 0;
-    GPTQ_CUDA_TRY(cudaMemcpyAsync(&hs, h->status, sizeof(int), cudaMemcpyDeviceToHost, s));
-    GPTQ_CUDA_TRY(cudaStreamSynchronize(s));
-    return hs;
+    return finish_call(h->status, s);
 }
 
 extern "C" int gptq_hessian_destroy(gptq_hessian* h) {

@@ -864,10 +864,7 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
         GPTQ_LAUNCH_CHECK();
     }
 
-    int hstatus = 0;
-    GPTQ_CUDA_TRY(cudaMemcpyAsync(&hstatus, w.status, sizeof(int), cudaMemcpyDeviceToHost, s));
-    GPTQ_CUDA_TRY(cudaStreamSynchronize(s));
-    return hstatus;
+    return finish_call(w.status, s);
 }
 
 }  // namespace

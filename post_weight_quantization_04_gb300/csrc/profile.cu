@@ -47,7 +47,7 @@ const char* kNames[K_COUNT] = {
     "eye_kernel",          "prep_scatter_kernel", "init_work_kernel",  "row_params_kernel",
     "gptq_block_kernel",   "sgemm_kernel[trailing]", "g_idx_kernel",
     "pack_kernel",         "rtn_kernel",          "split_kernel",      "tc_gemm_nt_kernel[prepare]",
-    "tc_gemm_nt_kernel[trailing]", "dequant_matmul_kernel",
+    "tc_gemm_nt_kernel[trailing]", "dequant_matmul_kernel", "merge_status_kernel",
 };
 
 }  // namespace

@@ -691,10 +691,7 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         const int rc = launch_pack(codes, rows, cols, q.bits, q.sym, packed, s);
         if (rc != GPTQ_OK) return rc;
     }
-    int hstatus = 0;
-    GPTQ_CUDA_TRY(cudaMemcpyAsync(&hstatus, w.status, sizeof(int), cudaMemcpyDeviceToHost, s));
-    GPTQ_CUDA_TRY(cudaStreamSynchronize(s));
-    return hstatus;
+    return finish_call(w.status, s);
 }
 
 extern "C" int rtn_quantize(const float* W, int64_t rows, int64_t cols, const uint8_t* dead, gptq_qconfig q,

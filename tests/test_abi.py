@@ -68,3 +68,11 @@ def test_argument_validation_happens_before_any_launch(clib):
                               p, 16, s) == 6
     h = ctypes.c_void_p()
     assert clib.gptq_hessian_create(0, ctypes.byref(h)) == 1
+
+
+def test_status_mode_switch(clib):
+    assert clib.gptq_set_status_mode(2) == 1          # INVALID_ARG
+    prev = clib.gptq_status_mode()
+    assert clib.gptq_set_status_mode(1) == 0
+    assert clib.gptq_status_mode() == 1
+    assert clib.gptq_set_status_mode(prev) == 0
