@@ -88,6 +88,11 @@ class Clocks:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            # wait (at most 3 s) for the first sample, so that a short timed region that
+            # follows is still bracketed by samples
+            t0 = time.perf_counter()
+            while time.perf_counter() - t0 < 3.0 and os.path.getsize(self.path) == 0:
+                time.sleep(0.02)
         except Exception:  # noqa: BLE001
             self.proc = None
 
@@ -467,6 +472,10 @@ def run_ours(args, ws, rank, local):
         if ws > 1:
             dist.barrier()
 
+    # clocks are sampled every 200 ms from before the warm-up to the end of the timed
+    # region (at the small workloads the timed region itself is a few milliseconds)
+    clocks = Clocks(local)
+    clocks.start()
     for _ in range(args.warmup):
         runner.step()
     lib.status_sync()
@@ -492,8 +501,6 @@ def run_ours(args, ws, rank, local):
         lib.status_sync()
         torch.cuda.synchronize()
 
-    clocks = Clocks(local)
-    clocks.start()
     barrier()
     torch.cuda.synchronize()
     n0 = lib.gptq_launch_count()
