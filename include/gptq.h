@@ -13,6 +13,8 @@
  *   gptq_pack                 codes -> LSB-first bitstream of b-bit unsigned codes
  *   gptq_dequant_matmul       Y = X Wq^T read straight from the packed codes, scales,
  *                             zeros and g_idx (the consumer of the stored form)
+ *   gptq_set_status_mode,     device-side errors reported by each call (synchronising)
+ *   gptq_status_sync          or deferred to one check (calls only enqueue work)
  *
  * Conventions shared by every entry point
  *   - Pointers named as device pointers must be CUDA device (or managed) memory of the
