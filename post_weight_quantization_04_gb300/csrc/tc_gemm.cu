@@ -8,7 +8,8 @@
 // pass. Accumulation is fp32 in TMEM.
 //
 // Structure (one CTA per SM, persistent over 128 x BN output tiles, BN = 128, or 64 for a
-// latency-critical launch too small to fill its SMs with 128-wide tiles):
+// latency-critical launch too small to fill its SMs with 128-wide tiles; large launches
+// with long K use a deep variant, a 3-stage ring with C in two rotating chunk buffers):
 //   warp 0      TMA producer: per 32-wide K step, the four fp32 boxes Ahi, Alo (128 x 32)
 //               and Bhi, Blo (BN x 32) (128-byte swizzle, K-major) into a 2-stage ring
 //   warp 1      single-thread tcgen05.mma issuer, kind::tf32, M = 128, N = BN, K = 8 per
@@ -36,13 +37,17 @@ namespace {
 // their SMs with 128-wide tiles (twice the CTAs, each with half the MMAs and epilogue).
 constexpr int G_BM = 128, G_BK = 32, G_THREADS = 192;
 constexpr int G_BOX = G_BM * G_BK * 4;         // 16 KB: one 128 x 32 fp32 box (A, and a C chunk)
-template <int BN>
+template <int BN, bool DEEP = false>
 struct GTile {
     static constexpr int BBOX = BN * G_BK * 4;                      // one BN x 32 fp32 box of B
     static constexpr int STAGE = 2 * G_BOX + 2 * BBOX;              // Ahi, Alo, Bhi, Blo
-    static constexpr int STAGES = 2;                                 // ring depth
+    // ring depth: 3 for the deep variant (large launches with long K: a stage arrives
+    // ~1.1-1.2k cycles after its TMA issue under full load, more than one K step of MMAs),
+    // whose C tile then streams through two rotating 32-column chunk buffers; else 2
+    static constexpr int STAGES = DEEP ? 3 : 2;
+    static constexpr int CB = DEEP ? 2 : BN / 32;                   // C chunk buffers
     static constexpr int NCH = BN / 32;                             // 32-column C chunks
-    static constexpr int CBUF = NCH * G_BOX;                        // the 128 x BN C tile
+    static constexpr int CBUF = CB * G_BOX;                         // C chunk buffers
     static constexpr int SMEM = STAGES * STAGE + CBUF + 1024 + 256;
     static constexpr uint32_t TMEM_COLS = 2 * BN;                   // two accumulators
     // kind::tf32: D fp32 (bits 4-5 = 1), A/B TF32 (2), both K-major, N >> 3, M >> 4
@@ -50,8 +55,9 @@ struct GTile {
                                       ((uint32_t)(G_BM >> 4) << 24);
 };
 
-static_assert(GTile<64>::SMEM <= 232448 && GTile<128>::SMEM <= 232448, "shared memory per CTA");
-static_assert(2 * GTile<64>::STAGES + 12 < 30 && 2 * GTile<128>::STAGES + 12 < 30, "barrier slots");
+static_assert(GTile<64>::SMEM <= 232448 && GTile<128>::SMEM <= 232448 && GTile<128, true>::SMEM <= 232448,
+              "shared memory per CTA");
+static_assert(2 * GTile<128, true>::STAGES + 12 < 30, "barrier slots");
 
 struct GParams {
     int M, N, K;
@@ -143,7 +149,7 @@ __device__ __forceinline__ void tile_of(const GParams& p, int t, int& tm, int& t
 // The C tile moves through shared memory by TMA in both directions: the producer loads it
 // (when beta != 0) while the MMAs of the tile run, the epilogue combines it with the
 // accumulator in place and stores it back with TMA, so no thread waits on a global load.
-template <int BN>
+template <int BN, bool DEEP>
 __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_constant__ CUtensorMap tAh,
                                                                   const __grid_constant__ CUtensorMap tAl,
                                                                   const __grid_constant__ CUtensorMap tBh,
@@ -152,7 +158,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                                                                   const GParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    using T = GTile<BN>;
+    using T = GTile<BN, DEEP>;
     constexpr int G_STAGES = T::STAGES;
     uint8_t* cbuf = smem + G_STAGES * T::STAGE;
     uint64_t* bars = reinterpret_cast<uint64_t*>(cbuf + T::CBUF);
@@ -182,7 +188,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
             mbar_init(tfull_bar(b), 1);
             mbar_init(tempty_bar(b), 4);
         }
-        for (int c = 0; c < T::NCH; ++c) {
+        for (int c = 0; c < T::CB; ++c) {
             mbar_init(cfull_bar(c), 1);
             mbar_init(cempty_bar(c), 1);
         }
@@ -238,7 +244,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                     }
                 }
                 if (!ok) break;
-                if (load_c) {
+                if (load_c && !DEEP) {
                     // chunk c of the C buffer is free once the previous tile's store of it
                     // has been read
                     for (int c = 0; c < T::NCH && ok; ++c) {
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
             }
             for (int s = 0; s < G_STAGES; ++s)
                 if (issued & (1u << s)) drain_wait(full_bar(s), (issued_par >> s) & 1u, p.status);
-            for (int c = 0; c < T::NCH; ++c)
+            for (int c = 0; c < (DEEP ? 0 : T::NCH); ++c)
                 if (c_issued & (1u << c)) drain_wait(cfull_bar(c), (c_par >> c) & 1u, p.status);
         }
     } else if (warp == 1) {
@@ -304,6 +310,123 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
             }
             umma_commit(drain_bar);
             drain_wait(drain_bar, 0, p.status);
+        }
+    } else if constexpr (DEEP) {
+        // ------------- epilogue (4 warps), C through two rotating chunk buffers ------------
+        // The storer keeps each buffer filled one use ahead: chunks 0 and 1 of the CTA's first
+        // tile at the start; chunk c + 2, or chunk c - 2 of the CTA's next tile, as soon as
+        // the store of chunk c has read the buffer (a TMA load of C, or without C just an
+        // arrive). Every thread waits for a buffer's fill before using it.
+        const int q = warp & 3;
+        const int rl = 32 * q + lane;            // row of the tile this thread owns
+        const bool storer = (threadIdx.x == 64);
+        int abuf = 0;
+        uint32_t aphase = 0, cph = 0;            // cph bit b: phase of buffer b's next fill
+        uint32_t issued0 = 0, issued1 = 0, consumed0 = 0, consumed1 = 0;   // per buffer
+        auto fill = [&](int b, int ftm, int ftn, int c) {
+            if (load_c) {
+                mbar_expect_tx(cfull_bar(b), G_BOX);
+                tma_load_2d(cbase + b * G_BOX, &tC, cfull_bar(b), ftn * BN + 32 * c, ftm * G_BM);
+            } else {
+                mbar_arrive(cfull_bar(b));
+            }
+            if (b) ++issued1; else ++issued0;
+        };
+        if (storer && (int)blockIdx.x < p.ntiles) {
+            int tm0, tn0;
+            tile_of(p, blockIdx.x, tm0, tn0);
+            fill(0, tm0, tn0, 0);
+            fill(1, tm0, tn0, 1);
+        }
+        bool alive = true;
+        for (int t = blockIdx.x; t < p.ntiles && alive; t += gridDim.x) {
+            int tm, tn, ntm = 0, ntn = 0;
+            tile_of(p, t, tm, tn);
+            const bool has_next = t + (int)gridDim.x < p.ntiles;
+            if (has_next) tile_of(p, t + (int)gridDim.x, ntm, ntn);
+            if (!epi_all(mbar_wait(tfull_bar(abuf), aphase, abort_flag, p.status))) break;
+            tc_fence_after();
+            const int row = tm * G_BM + rl;
+            const uint32_t ta = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(abuf * BN);
+#pragma unroll 1
+            for (int c = 0; c < T::NCH; ++c) {
+                const int b = c & 1;
+                if (!epi_all(mbar_wait(cfull_bar(b), (cph >> b) & 1u, abort_flag, p.status))) {
+                    alive = false;
+                    break;
+                }
+                cph ^= 1u << b;
+                if (b) ++consumed1; else ++consumed0;
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(ta + 32 * c, v);
+                tmem_ld_wait();
+                uint8_t* brow = cbuf + b * G_BOX + rl * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float4* ptr = reinterpret_cast<float4*>(brow + ((j ^ (rl & 7)) << 4));
+                    float4 o = make_float4(p.alpha * __uint_as_float(v[4 * j]), p.alpha * __uint_as_float(v[4 * j + 1]),
+                                           p.alpha * __uint_as_float(v[4 * j + 2]),
+                                           p.alpha * __uint_as_float(v[4 * j + 3]));
+                    if (load_c) {
+                        const float4 cv = *ptr;
+                        o.x = fmaf(p.beta, cv.x, o.x);
+                        o.y = fmaf(p.beta, cv.y, o.y);
+                        o.z = fmaf(p.beta, cv.z, o.z);
+                        o.w = fmaf(p.beta, cv.w, o.w);
+                    }
+                    *ptr = o;
+                    const int gc0 = tn * BN + 32 * c + 4 * j;
+                    if (p.omode == 1 && row < p.M && row >= p.orow0 && gc0 + 3 < p.N && p.ovec) {
+                        // row-major split, four columns at once (16-byte stores)
+                        float4 h4;
+                        h4.x = __uint_as_float(__float_as_uint(o.x) & 0xFFFFE000u);
+                        h4.y = __uint_as_float(__float_as_uint(o.y) & 0xFFFFE000u);
+                        h4.z = __uint_as_float(__float_as_uint(o.z) & 0xFFFFE000u);
+                        h4.w = __uint_as_float(__float_as_uint(o.w) & 0xFFFFE000u);
+                        const int64_t at = (int64_t)(row - p.orow0) * p.old_ + gc0;
+                        *reinterpret_cast<float4*>(p.ohi + at) = h4;
+                        *reinterpret_cast<float4*>(p.olo + at) = make_float4(o.x - h4.x, o.y - h4.y, o.z - h4.z, o.w - h4.w);
+                    } else if (p.omode && row < p.M && row >= p.orow0) {
+                        const float o4[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int gc = tn * BN + 32 * c + 4 * j + e;
+                            if (gc < p.N) {
+                                const float h = __uint_as_float(__float_as_uint(o4[e]) & 0xFFFFE000u);
+                                const int64_t orow = row - p.orow0;
+                                const int64_t at = (p.omode == 1) ? orow * p.old_ + gc : (int64_t)gc * p.old_ + orow;
+                                p.ohi[at] = h;
+                                p.olo[at] = o4[e] - h;
+                            }
+                        }
+                    }
+                }
+                fence_proxy_async_smem();   // make the chunk visible to TMA
+                epi_barrier();
+                if (storer) {
+                    tma_store_2d(&tC, cbase + b * G_BOX, tn * BN + 32 * c, tm * G_BM);
+                    bulk_commit();
+                    bulk_wait_read0();       // the store has read buffer b: refill it
+                    if (c + 2 < T::NCH)
+                        fill(b, tm, tn, c + 2);
+                    else if (has_next)
+                        fill(b, ntm, ntn, c + 2 - T::NCH);
+                }
+            }
+            if (!alive) break;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(abuf));   // the accumulator is free again
+            if (++abuf == 2) {
+                abuf = 0;
+                aphase ^= 1u;
+            }
+        }
+        if (storer) {
+            bulk_wait0();
+            // a fill issued but never waited for (an aborted tile): let its copy land first
+            if (issued0 > consumed0) drain_wait(cfull_bar(0), (issued0 - 1u) & 1u, p.status);
+            if (issued1 > consumed1) drain_wait(cfull_bar(1), (issued1 - 1u) & 1u, p.status);
         }
     } else {
         // ------------------------------- epilogue (4 warps) -------------------------
@@ -563,6 +686,8 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
     int tn128 = 0, tn64 = 0;
     const int nt128 = count_tiles(128, tn128), nt64 = count_tiles(64, tn64);
     const int bn = (out.narrow_ok && nt128 < cap && nt64 <= cap) ? 64 : 128;
+    // the deep variant for large launches: at least two waves of tiles, K of 8 steps or more
+    const bool deep = bn == 128 && nt128 >= 2 * cap && K >= 8 * G_BK;
     CUtensorMap tah, tal, tbh, tbl, tcm;
     if (!make_map(&tah, Ahi, M, K, ldk) || !make_map(&tal, Alo, M, K, ldk) ||
         !make_map(&tbh, Bhi, N, K, out.ldb, bn) || !make_map(&tbl, Blo, N, K, out.ldb, bn) ||
@@ -589,8 +714,10 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
               ((reinterpret_cast<uintptr_t>(out.hi) | reinterpret_cast<uintptr_t>(out.lo)) % 16 == 0)) ? 1 : 0;
     if (p.ntiles == 0) return cudaSuccess;
     const int grid = std::min(p.ntiles, cap);
-    auto kern = bn == 64 ? tc_gemm_nt_kernel<64> : tc_gemm_nt_kernel<128>;
-    const int smem = bn == 64 ? GTile<64>::SMEM : GTile<128>::SMEM;
+    auto kern = bn == 64 ? tc_gemm_nt_kernel<64, false>
+              : deep    ? tc_gemm_nt_kernel<128, true>
+                        : tc_gemm_nt_kernel<128, false>;
+    const int smem = bn == 64 ? GTile<64>::SMEM : deep ? GTile<128, true>::SMEM : GTile<128>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (out.pdl) {
