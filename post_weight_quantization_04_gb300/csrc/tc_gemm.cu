@@ -44,7 +44,7 @@ struct GTile {
     // ring depth: 3 for the deep variant (large launches with long K: a stage arrives
     // ~1.1-1.2k cycles after its TMA issue under full load, more than one K step of MMAs),
     // whose C tile then streams through two rotating 32-column chunk buffers; else 2
-    static constexpr int STAGES = DEEP ? 3 : 2;
+    static constexpr int STAGES = (DEEP && BN == 128) ? 3 : 2;
     static constexpr int CB = DEEP ? 2 : BN / 32;                   // C chunk buffers
     static constexpr int NCH = BN / 32;                             // 32-column C chunks
     static constexpr int CBUF = CB * G_BOX;                         // C chunk buffers
@@ -55,7 +55,8 @@ struct GTile {
                                       ((uint32_t)(G_BM >> 4) << 24);
 };
 
-static_assert(GTile<64>::SMEM <= 232448 && GTile<128>::SMEM <= 232448 && GTile<128, true>::SMEM <= 232448,
+static_assert(GTile<64>::SMEM <= 232448 && GTile<128>::SMEM <= 232448 && GTile<128, true>::SMEM <= 232448 &&
+                  GTile<256, true>::SMEM <= 232448,
               "shared memory per CTA");
 static_assert(2 * GTile<128, true>::STAGES + 12 < 30, "barrier slots");
 
@@ -686,11 +687,17 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
     int tn128 = 0, tn64 = 0;
     const int nt128 = count_tiles(128, tn128), nt64 = count_tiles(64, tn64);
     const int bn = (out.narrow_ok && nt128 < cap && nt64 <= cap) ? 64 : 128;
-    // the deep variant for large launches: at least two waves of tiles, K of 8 steps or more
+    // the deep variant for large launches: at least two waves of tiles, K of 8 steps or
+    // more; 128 x 256 tiles (two 96 KB stages: each K step's MMAs take twice as long, which
+    // covers a stage's load, and a quarter less operand traffic per flop) when N is large
+    int tn256 = 0;
+    const int nt256 = count_tiles(256, tn256);
     const bool deep = bn == 128 && nt128 >= 2 * cap && K >= 8 * G_BK;
+    const bool wide = deep && N >= 1024 && nt256 >= cap;
+    const int tw = wide ? 256 : bn;   // the launch's tile width
     CUtensorMap tah, tal, tbh, tbl, tcm;
     if (!make_map(&tah, Ahi, M, K, ldk) || !make_map(&tal, Alo, M, K, ldk) ||
-        !make_map(&tbh, Bhi, N, K, out.ldb, bn) || !make_map(&tbl, Blo, N, K, out.ldb, bn) ||
+        !make_map(&tbh, Bhi, N, K, out.ldb, tw) || !make_map(&tbl, Blo, N, K, out.ldb, tw) ||
         !make_map(&tcm, C, M, N, ldc))
         return cudaErrorInvalidValue;
     GParams p;
@@ -699,11 +706,11 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
     p.K = K;
     p.alpha = alpha;
     p.beta = beta;
-    p.bn = bn;
+    p.bn = tw;
     p.tiles_m = (M + G_BM - 1) / G_BM;
-    p.tiles_n = bn == 64 ? tn64 : tn128;
+    p.tiles_n = tw == 64 ? tn64 : tw == 256 ? tn256 : tn128;
     p.lower_only = lower_only ? 1 : 0;
-    p.ntiles = bn == 64 ? nt64 : nt128;
+    p.ntiles = tw == 64 ? nt64 : tw == 256 ? nt256 : nt128;
     p.status = status;
     p.ohi = out.hi;
     p.olo = out.lo;
@@ -715,9 +722,13 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
     if (p.ntiles == 0) return cudaSuccess;
     const int grid = std::min(p.ntiles, cap);
     auto kern = bn == 64 ? tc_gemm_nt_kernel<64, false>
+              : wide    ? tc_gemm_nt_kernel<256, true>
               : deep    ? tc_gemm_nt_kernel<128, true>
                         : tc_gemm_nt_kernel<128, false>;
-    const int smem = bn == 64 ? GTile<64>::SMEM : deep ? GTile<128, true>::SMEM : GTile<128>::SMEM;
+    const int smem = bn == 64 ? GTile<64>::SMEM
+                   : wide    ? GTile<256, true>::SMEM
+                   : deep    ? GTile<128, true>::SMEM
+                             : GTile<128>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (out.pdl) {
