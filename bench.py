@@ -318,8 +318,8 @@ ROOF = {
 # launched with many shapes per step, the average over one whole step's launches; a
 # kernel changed since its capture has no entry here.
 TRAFFIC = {
-    (1, "tc_gemm_nt_kernel[prepare]"): 768942.08,
-    (1, "tc_gemm_nt_kernel[trailing]"): 10274816.0,
+    (1, "tc_gemm_nt_kernel[prepare]"): 768972.8,
+    (1, "tc_gemm_nt_kernel[trailing]"): 10273228.8,
     (2, "hessian_tc_kernel"): 4.827069e9 + 159.446272e6,
     (2, "pack_kernel"): 16.788224e6,
 }
