@@ -591,11 +591,12 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         GPTQ_LAUNCH_CHECK();
     }
 
-    // threads per row: as many as keep every CTA resident at once (<= 2 per SM)
+    // threads per row: as many as keep every CTA resident at once (3 per SM: 64.5 KB of
+    // shared memory and at most 128 threads x 167 registers each)
     const int sms = device_sm_count();
     int tpr = 4;
     for (int t : {32, 16, 8}) {
-        if (ceil_div(rows * t, 128) <= 2 * sms) {
+        if (ceil_div(rows * t, 128) <= 3 * sms) {
             tpr = t;
             break;
         }
