@@ -301,20 +301,40 @@ __global__ void __launch_bounds__(512) potrf_diag_kernel(const float* __restrict
     pdl_trigger();
 
     {
-        // the lower triangle, one element per thread and step with consecutive columns
-        // across a warp: 128-byte global reads, conflict-free shared stores; all loads of
-        // a thread in flight at once
-        float v[NB * NB / 512];
+        // the lower triangle in 16-byte pieces, the lanes of a warp on 32 consecutive rows
+        // (conflict-free stores into the odd-stride block); all loads of a thread in flight
+        // at once
+        const bool vec = ((lda & 3) == 0) && ((k0 & 3) == 0) && ((reinterpret_cast<uintptr_t>(A) & 15) == 0);
+        float4 v[NB * NB / 4 / 512];
 #pragma unroll
-        for (int u = 0; u < NB * NB / 512; ++u) {
+        for (int u = 0; u < NB * NB / 4 / 512; ++u) {
             const int idx = tid + 512 * u;
-            const int i = idx >> 7, j = idx & (NB - 1);
-            v[u] = (i < n && j <= i) ? A[(k0 + i) * lda + k0 + j] : 0.0f;
+            const int i = idx & (NB - 1), j4 = (idx >> 7) << 2;
+            float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (i < n && j4 <= i) {
+                const float* src = A + (k0 + i) * lda + k0 + j4;
+                if (vec && j4 + 3 < n) {
+                    x = *reinterpret_cast<const float4*>(src);
+                } else {
+                    x.x = src[0];
+                    if (j4 + 1 < n) x.y = src[1];
+                    if (j4 + 2 < n) x.z = src[2];
+                    if (j4 + 3 < n) x.w = src[3];
+                }
+                if (j4 + 1 > i) x.y = 0.0f;
+                if (j4 + 2 > i) x.z = 0.0f;
+                if (j4 + 3 > i) x.w = 0.0f;
+            }
+            v[u] = x;
         }
 #pragma unroll
-        for (int u = 0; u < NB * NB / 512; ++u) {
+        for (int u = 0; u < NB * NB / 4 / 512; ++u) {
             const int idx = tid + 512 * u;
-            S[(idx >> 7) * LD + (idx & (NB - 1))] = v[u];
+            float* d = S + (idx & (NB - 1)) * LD + ((idx >> 7) << 2);
+            d[0] = v[u].x;
+            d[1] = v[u].y;
+            d[2] = v[u].z;
+            d[3] = v[u].w;
         }
         for (int idx = tid; idx < NB * LDX / 4; idx += 512)
             reinterpret_cast<float4*>(X)[idx] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
