@@ -596,6 +596,51 @@ __global__ void __launch_bounds__(256) split_cols_kernel(const float* __restrict
     }
 }
 
+// The same with 16-byte accesses on both sides (N, ld and ldk multiples of 4, 16-byte
+// aligned bases): a 64 x 64 tile per CTA, read as rows of B, written as rows of hi/lo.
+constexpr int SC_T = 64;
+__global__ void __launch_bounds__(256) split_cols4_kernel(const float* __restrict__ B, int64_t ld, int K, int N,
+                                                         float* __restrict__ hi, float* __restrict__ lo, int ldk) {
+    __shared__ float tile[SC_T][SC_T + 1];
+    pdl_wait();
+    pdl_trigger();
+    const int k0 = blockIdx.y * SC_T, n0 = blockIdx.x * SC_T;
+    const int c4 = (threadIdx.x & 15) * 4, r = threadIdx.x >> 4;   // 16 float4 per row, 16 rows per pass
+#pragma unroll
+    for (int rr = 0; rr < SC_T; rr += 16) {
+        const int k = k0 + rr + r, n = n0 + c4;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (k < K && n < N) v = *reinterpret_cast<const float4*>(B + (int64_t)k * ld + n);   // N % 4 == 0
+        tile[rr + r][c4] = v.x;
+        tile[rr + r][c4 + 1] = v.y;
+        tile[rr + r][c4 + 2] = v.z;
+        tile[rr + r][c4 + 3] = v.w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int rr = 0; rr < SC_T; rr += 16) {
+        const int n = n0 + rr + r, k = k0 + c4;
+        if (n >= N || k >= K) continue;
+        float4 h, l;
+        split1(tile[c4][rr + r], h.x, l.x);
+        split1(tile[c4 + 1][rr + r], h.y, l.y);
+        split1(tile[c4 + 2][rr + r], h.z, l.z);
+        split1(tile[c4 + 3][rr + r], h.w, l.w);
+        float* ph = hi + (int64_t)n * ldk + k;
+        float* pl = lo + (int64_t)n * ldk + k;
+        if (k + 3 < K) {
+            *reinterpret_cast<float4*>(ph) = h;
+            *reinterpret_cast<float4*>(pl) = l;
+        } else {
+            const float hs[4] = {h.x, h.y, h.z, h.w}, ls[4] = {l.x, l.y, l.z, l.w};
+            for (int e = 0; e < 4 && k + e < K; ++e) {
+                ph[e] = hs[e];
+                pl[e] = ls[e];
+            }
+        }
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encoder() { return tma_encoder(); }
 
 bool make_map(CUtensorMap* m, const float* base, int rows, int K, int64_t ldk, int box_rows = G_BM) {
@@ -652,8 +697,20 @@ cudaError_t split_rows(int id, const float* A, int64_t lda, int rows, int K, flo
 cudaError_t split_cols(int id, const float* B, int64_t ld, int K, int N, float* hi, float* lo, int ldk,
                        cudaStream_t s, bool pdl) {
     if (K <= 0 || N <= 0) return cudaSuccess;
-    dim3 grid((unsigned)((N + 31) / 32), (unsigned)((K + 31) / 32));
     cudaError_t e = cudaSuccess;
+    const bool vec = (N % 4 == 0) && (ld % 4 == 0) && (ldk % 4 == 0) &&
+                     ((reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(hi) |
+                       reinterpret_cast<uintptr_t>(lo)) % 16 == 0);
+    if (vec) {
+        dim3 grid((unsigned)((N + SC_T - 1) / SC_T), (unsigned)((K + SC_T - 1) / SC_T));
+        if (pdl)
+            GPTQ_LAUNCH(id, s, e = launch_pdl(split_cols4_kernel, grid, dim3(256), 0, s, B, ld, K, N, hi, lo, ldk));
+        else
+            GPTQ_LAUNCH(id, s, split_cols4_kernel<<<grid, 256, 0, s>>>(B, ld, K, N, hi, lo, ldk));
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
+    dim3 grid((unsigned)((N + 31) / 32), (unsigned)((K + 31) / 32));
     if (pdl)
         GPTQ_LAUNCH(id, s, e = launch_pdl(split_cols_kernel, grid, dim3(256), 0, s, B, ld, K, N, hi, lo, ldk));
     else
