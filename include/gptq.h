@@ -219,7 +219,10 @@ const char* gptq_status_string(int status);
  * In mode GPTQ_STATUS_DEFERRED the calls that say "Synchronises" do not: they return
  * GPTQ_OK once their work is enqueued, and a final one-thread kernel of each call folds
  * its device status into one sticky status word per device (the first error is kept).
- * gptq_status_sync then reports it. The mode is process-wide.
+ * gptq_status_sync then reports it. The mode is process-wide. In deferred mode the
+ * calls only enqueue work, so a sequence of them can be captured into a CUDA graph and
+ * replayed (make one call of each kind before capturing: the first gptq_prepare on a
+ * device creates the streams and events its two-stream schedule uses).
  * ------------------------------------------------------------------------------------ */
 enum { GPTQ_STATUS_SYNC = 0, GPTQ_STATUS_DEFERRED = 1 };
 /* Errors: INVALID_ARG (unknown mode). Host only. */
