@@ -54,6 +54,7 @@ __all__ = [
     "obs_bruteforce_row", "auto_compute_hessian", "auto_gptq_quantize_row", "auto_dequantize_row",
     "near_half", "perm_equivalent", "TieMismatch", "unpack_rows", "dequant_stored", "dequant_matmul",
     "round_bf16", "mlp_forward", "apply_layerwise",
+    "prune_saliency", "prune_loop", "prune_layer", "obs_prune_bruteforce_row",
 ]
 
 
@@ -512,6 +513,86 @@ def layer_loss(Q, W0, H) -> np.ndarray:
     """Per row (q - w0) H (q - w0)^T ([guide] "How it works": E(w') up to a constant)."""
     D = np.asarray(Q, F64) - np.asarray(W0, F64)
     return np.sum((D @ np.asarray(H, F64)) * D, axis=1)
+
+
+# ----------------------------------------------------------------------------------------
+# Pruning with the same update ([guide] "Going further": SparseGPT reuses the exact same
+# update for pruning). The pages give the update only; the mask rule is a reading:
+# at the start of each block of columns, in each row, the weights whose removal costs
+# least on their own are pruned -- by [guide] "How it works", removing w_j alone raises the
+# loss by e^2 / (2 Hinv_F[j, j]) with e = w_j, and in the Cholesky form Hinv_F[j, j] is
+# U[j, j]^2, so the saliency is (w_j / U[j, j])^2 (the factor 1/2 dropped). The block's
+# weights are the updated ones at the block start, like the group scales of the loop.
+# ----------------------------------------------------------------------------------------
+
+def prune_saliency(W, U, j0: int, j1: int) -> np.ndarray:
+    """(w_j / U[j, j])^2 for the columns [j0, j1) of W (rows x columns)."""
+    W = np.asarray(W, dtype=F64)
+    u = np.diag(np.asarray(U, dtype=F64))[j0:j1]
+    return (W[:, j0:j1] / u) ** 2
+
+
+def prune_loop(W, U, sparsity: float, block: int = 128) -> Dict[str, np.ndarray]:
+    """The column loop of [loop] with pruning in place of rounding, on an already dead-zeroed,
+    already permuted W: per block of `block` columns, each row prunes its
+    round(sparsity * width) lowest-saliency weights (stable order on ties); then for every
+    column j: q = 0 where pruned, else w_j; err = (w_j - q) / U[j, j];
+    W[:, j+1:] -= outer(err, U[j, j+1:]). Returns the pruned-and-compensated W, the mask and
+    per-row sum err^2."""
+    W = np.array(W, dtype=F64, copy=True)
+    U = np.asarray(U, dtype=F64)
+    o, d = W.shape
+    mask = np.zeros((o, d), dtype=bool)
+    err_sq = np.zeros(o, dtype=F64)
+    for b0 in range(0, d, block):
+        b1 = min(d, b0 + block)
+        k = int(round(sparsity * (b1 - b0)))
+        if k > 0:
+            idx = np.argsort(prune_saliency(W, U, b0, b1), axis=1, kind="stable")[:, :k]
+            np.put_along_axis(mask[:, b0:b1], idx, True, axis=1)
+        for j in range(b0, b1):
+            q = np.where(mask[:, j], 0.0, W[:, j])
+            err = (W[:, j] - q) / U[j, j]
+            W[:, j] = q
+            W[:, j + 1:] -= np.outer(err, U[j, j + 1:])
+            err_sq += err * err
+    return {"W": W, "mask": mask, "err_sq": err_sq}
+
+
+def prune_layer(W, U, perm, dead, sparsity: float, block: int = 128) -> Dict[str, np.ndarray]:
+    """Pruning of one layer given (U, perm, dead) as `gptq_quantize` takes them: W[:, dead] = 0,
+    columns permuted, `prune_loop`, results back in the original column order."""
+    W = np.array(W, dtype=F64, copy=True)
+    o, d = W.shape
+    W[:, np.asarray(dead, dtype=bool)] = 0.0
+    perm = np.arange(d) if perm is None else np.asarray(perm)
+    r = prune_loop(W[:, perm], U, sparsity, block)
+    inv = np.argsort(perm)
+    return {"W": r["W"][:, inv], "mask": r["mask"][:, inv], "err_sq": r["err_sq"]}
+
+
+def obs_prune_bruteforce_row(w, H, mask):
+    """One row pruned by explicit OBS with a given mask: for j in order, the target is 0 where
+    masked and w_j (unchanged) elsewhere; e = w_j - target; delta = -(e / Hinv[j, j]) *
+    Hinv[j, F] over the remaining coordinates F; then Hinv is eliminated as in
+    `obs_bruteforce_row`. Returns the final row."""
+    w = np.array(w, dtype=F64, copy=True)
+    d = w.shape[0]
+    Hinv = np.linalg.inv(np.asarray(H, F64))
+    F = list(range(d))
+    for j in range(d):
+        target = 0.0 if mask[j] else w[j]
+        e = w[j] - target
+        hjj = Hinv[j, j]
+        w[F] = w[F] - (e / hjj) * Hinv[j, F]
+        w[j] = target
+        Fn = F[1:]
+        if Fn:
+            sub = Hinv[np.ix_(Fn, Fn)] - np.outer(Hinv[Fn, j], Hinv[j, Fn]) / hjj
+            Hinv = np.zeros_like(Hinv)
+            Hinv[np.ix_(Fn, Fn)] = sub
+        F = Fn
+    return w
 
 
 # ----------------------------------------------------------------------------------------

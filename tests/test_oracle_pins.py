@@ -481,3 +481,92 @@ def test_layerwise_gptq_beats_rtn_end_to_end():
     _, _, y_g = O.apply_layerwise(X, Ws, lambda W, h: O.gptq_layer(W, h, 3, 0, True)["Wq"])
     _, _, y_r = O.apply_layerwise(X, Ws, lambda W, h: O.rtn_quantize(W, 3, 0, True)["Wq"])
     assert err(y_g) < err(y_r)
+
+
+# ------------------------------------------------------- pruning with the same update
+
+def _corr_layer(seed, d, o, n_mult=4):
+    rng = _rng(seed)
+    X = rng.standard_normal((n_mult * d, d)) @ rng.standard_normal((d, d))
+    H = _damped(O.hessian(X))
+    return rng, X, H, rng.standard_normal((o, d)) * 0.1
+
+
+@pytest.mark.parametrize("d,block,sparsity", [(8, 4, 0.5), (8, 8, 0.25), (6, 4, 0.5)])
+def test_prune_loop_equals_bruteforce_obs(d, block, sparsity):
+    """The Cholesky-form loop with pruning equals explicit OBS with Gaussian elimination on
+    H^-1 given the same mask (the update the pages say pruning reuses)."""
+    rng, X, H, W = _corr_layer(40 + d + block, d, 5)
+    U = O.upper_cholesky_of_inverse(H)
+    r = O.prune_loop(W, U, sparsity, block)
+    for i in range(W.shape[0]):
+        w = O.obs_prune_bruteforce_row(W[i], H, r["mask"][i])
+        np.testing.assert_allclose(r["W"][i], w, rtol=0, atol=1e-12)
+
+
+def test_prune_mask_counts_zeros_and_loss_closed_form():
+    """Per row and block exactly round(sparsity * width) weights are pruned and come out 0;
+    the kept ones after the first pruned one are changed by the compensation; and per row
+    (q - w0) H (q - w0)^T equals sum_j err_j^2 (the same closed form as the quantiser's, P-3)."""
+    rng, X, H, W = _corr_layer(50, 48, 6)
+    U = O.upper_cholesky_of_inverse(H)
+    r = O.prune_loop(W, U, 0.5, 16)
+    for b0 in range(0, 48, 16):
+        np.testing.assert_array_equal(r["mask"][:, b0:b0 + 16].sum(axis=1), 8)
+    assert np.all(r["W"][r["mask"]] == 0.0)
+    # every kept weight after its row's first pruned one has received compensation
+    first = r["mask"].argmax(axis=1)
+    after = np.arange(48)[None, :] > first[:, None]
+    keep = ~r["mask"] & after
+    assert np.all(r["W"][keep] != W[keep])
+    D = r["W"] - W
+    np.testing.assert_allclose(np.einsum("ij,jk,ik->i", D, H, D), r["err_sq"], rtol=1e-10)
+
+
+def test_prune_zero_sparsity_is_identity():
+    rng, X, H, W = _corr_layer(51, 32, 4)
+    r = O.prune_loop(W, O.upper_cholesky_of_inverse(H), 0.0, 16)
+    np.testing.assert_array_equal(r["W"], W)
+    assert not r["mask"].any()
+
+
+def test_prune_with_diagonal_hessian_is_magnitude_pruning():
+    """X = Hadamard columns gives H = 2I (U diagonal): no compensation reaches other columns,
+    so the result is W with each row-block's smallest-|w| half set to 0."""
+    spec = synth.XSpec(n=64, d=32, kind="hadamard", dtype="f32")
+    X = synth.to_numpy_f64(synth.make_x(spec, 0, device="cpu"))
+    H = O.hessian(X)
+    np.testing.assert_allclose(H, 2.0 * np.eye(32), atol=0)
+    W = _rng(52).standard_normal((5, 32))
+    r = O.prune_loop(W, O.upper_cholesky_of_inverse(H), 0.5, 8)
+    ref = W.copy()
+    for b0 in range(0, 32, 8):
+        blk = ref[:, b0:b0 + 8]
+        small = np.argsort(np.abs(blk), axis=1, kind="stable")[:, :4]
+        np.put_along_axis(blk, small, 0.0, axis=1)
+    np.testing.assert_allclose(r["W"], ref, rtol=0, atol=1e-15)
+
+
+def test_prune_compensation_beats_plain_masking():
+    """On correlated inputs the compensated result has a smaller output error than the same
+    mask applied without the update (the pages' claim for the update, on pruning)."""
+    rng, X, H, W = _corr_layer(53, 64, 16)
+    U = O.upper_cholesky_of_inverse(H)
+    r = O.prune_loop(W, U, 0.5, 32)
+    plain = np.where(r["mask"], 0.0, W)
+    assert O.rel_output_error(X, W, r["W"]) < 0.8 * O.rel_output_error(X, W, plain)
+
+
+def test_prune_layer_permutation_and_dead():
+    """prune_layer = prune_loop on (W[:, perm] with dead columns zeroed), unpermuted."""
+    rng, X, H, W = _corr_layer(54, 24, 5)
+    X[:, 3] = 0.0
+    Hd = O.hessian(X)
+    U, perm, dead = O.prepare(Hd, 0.01, True, np.diag(O.xtx(X)))
+    r = O.prune_layer(W, U, perm, dead, 0.5, 8)
+    W0 = W.copy()
+    W0[:, dead] = 0.0
+    r2 = O.prune_loop(W0[:, perm], U, 0.5, 8)
+    inv = np.argsort(perm)
+    np.testing.assert_array_equal(r["W"], r2["W"][:, inv])
+    assert np.all(r["W"][:, dead] == 0.0)
