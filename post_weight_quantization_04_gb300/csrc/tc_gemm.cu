@@ -7,18 +7,23 @@
 // (the dropped Alo*Blo and the TF32 rounding of the lo parts), against 2^-11 for one TF32
 // pass. Accumulation is fp32 in TMEM.
 //
-// Structure (one CTA per SM, persistent over 128 x BN output tiles, BN = 128, or 64 for a
-// latency-critical launch too small to fill its SMs with 128-wide tiles; large launches
-// with long K use a deep variant, a 3-stage ring with C in two rotating chunk buffers):
+// Structure (one CTA per SM, persistent over 128 x BN output tiles). Variants:
+//   BN = 128, 2-stage ring, the C tile in four chunk buffers (the default);
+//   BN = 64, the same for a latency-critical launch too small to fill its SMs with
+//     128-wide tiles;
+//   deep (large launches with long K): C in two rotating chunk buffers, which frees the
+//     shared memory for a third 64 KB stage (BN = 128) or for 128 x 256 tiles (two 96 KB
+//     stages, when N >= 1024).
 //   warp 0      TMA producer: per 32-wide K step, the four fp32 boxes Ahi, Alo (128 x 32)
-//               and Bhi, Blo (BN x 32) (128-byte swizzle, K-major) into a 2-stage ring
+//               and Bhi, Blo (BN x 32) (128-byte swizzle, K-major) into the ring
 //   warp 1      single-thread tcgen05.mma issuer, kind::tf32, M = 128, N = BN, K = 8 per
 //               instruction, three products per K step, into one of two TMEM
 //               accumulators (BN columns each)
-//   warps 2..5  epilogue: TMEM -> registers, combined with the C tile that the producer
-//               brought into shared memory by TMA, stored back by TMA in four 32-column
-//               chunks (the next tile's chunk loads as soon as this one's has been read
-//               by its store); overlaps the MMAs of the next tile in the other accumulator
+//   warps 2..5  epilogue: TMEM -> registers, combined with the C tile in shared memory
+//               (brought by TMA: by the producer while the tile's MMAs run, or, in the
+//               deep variant, by the epilogue's storer one chunk buffer ahead), stored
+//               back by TMA in 32-column chunks; overlaps the MMAs of the next tile in the
+//               other accumulator
 // Every mbarrier wait is bounded (GPTQ_ERR_TIMEOUT into *status, then unwind).
 #include <cuda.h>
 #include <cudaTypedefs.h>
