@@ -53,3 +53,23 @@ def test_two_gloo_ranks_take_the_slowest_step_and_report_per_replica():
 def test_single_rank_is_untouched():
     assert bench.max_over_ranks(3.25, 1, "cpu") == 3.25
     assert bench.replica_value(3.25, 1) == 3.25
+
+
+def test_reference_arm_json_contract():
+    """`bench.py --impl reference` (the CPU oracle on the host cores) prints one JSON line with
+    the contract's keys, e2e without copies and a cpu_baseline describing the run."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--config", "0", "--steps", "1",
+                          "--warmup", "0"], cwd=root, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["higher_is_better"] is False and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
