@@ -34,6 +34,8 @@ if ROOT not in sys.path:
 METRIC = "GPTQ layer quantize time (ms, incl. H+Cholesky) and % of roofline per kernel"
 L2_BYTES = 129 * 1024 * 1024
 FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x 2 flop x max SM clock
+# the Llama-3-8B-shaped decoder block (7 linears x bits 2, 3, 4 on 262144 calibration tokens)
+DEFAULT_CONFIG = 4
 
 
 def parse(argv=None):
@@ -41,7 +43,7 @@ def parse(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -298,8 +300,9 @@ def algorithmic(cfg_layers):
 
 
 # kernel class -> (bound, unit); "tensor-tf32x3" is the fp32-accurate 3xTF32 product whose
-# ceiling is the TF32 tensor peak / 3 (TF32 peak = measured bf16 peak x 1.1 / 2.25, the
-# nominal dense ratio); "alu" kernels are measured against the FP32 FFMA peak
+# ceiling is the TF32 tensor peak / 3 (the TF32 peak measured in this run with a cuBLAS TF32
+# GEMM, else GB300's nominal dense TF32:BF16 ratio of 1.1 : 2.25 times the measured bf16
+# peak); "alu" kernels are measured against the FP32 FFMA peak
 ROOF = {
     "hessian_tc_kernel": ("tensor", "TFLOP/s"),
     "tc_gemm_nt_kernel[prepare]": ("tensor-tf32x3", "TFLOP/s"),
@@ -329,13 +332,149 @@ def peak_for(bound, pk):
     if bound == "tensor":
         return pk["bf16_tflops"], "measured bf16 dense (cuBLAS burst)"
     if bound == "tensor-tf32x3":
-        return pk["bf16_tflops"] * (1.1 / 2.25) / 3.0, "measured bf16 x 1.1/2.25 (TF32 nominal ratio) / 3 passes"
+        if pk.get("tf32_tflops"):
+            return pk["tf32_tflops"] / 3.0, "measured TF32 dense (cuBLAS TF32 8192^3 burst, this run) / 3 passes"
+        return pk["bf16_tflops"] * (1.1 / 2.25) / 3.0, "measured bf16 x 1.1/2.25 (GB300 nominal dense TF32:BF16) / 3"
     if bound == "alu":
         return FFMA_PEAK_TFLOPS, "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz"
     return pk["hbm_gbs"], "measured HBM copy"
 
 
+def measure_tf32_peak(dev, n: int = 8192, reps: int = 10) -> float:
+    """Dense TF32 tensor-core throughput of a cuBLAS GEMM (fp32 in and out, TF32 products)
+    on this GPU: the best of `reps` CUDA-event-timed n^3 products, in TFLOP/s."""
+    import torch
+    prev = torch.get_float32_matmul_precision()
+    torch.set_float32_matmul_precision("high")   # fp32 matmuls on the TF32 tensor path
+    try:
+        a = torch.randn(n, n, device=dev)
+        b = torch.randn(n, n, device=dev)
+        c = torch.empty(n, n, device=dev)
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b, c
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    finally:
+        torch.set_float32_matmul_precision(prev)
+
+
 # ------------------------------------------------------------------------- CPU oracle
+#
+# The oracle (numpy fp64, test infrastructure) timed on this host's cores, for context:
+#   cpu_baseline (our arm, rank 0, N = 1): "one stated layer" timed whole - the whole
+#     layer pass for the tiny and OPT workloads, the one layer of the Llama-7B attention
+#     workload, and q_proj at 4 bits (H from the q/k/v input) for the decoder block; the
+#     MLP-down layer (d = 14336) is too large for a whole CPU pass and is sampled (stated).
+#     The column loop's rows are split over spawned processes (rows are independent given
+#     U); H and U use the threaded BLAS/LAPACK of numpy.
+#   reference arm: per step a bounded sample of the same stated layer (H on one 2048-token
+#     segment, U in full, the loop on a few rows), timed as it runs - no scaling.
+
+def stated_layer(cfg: int, wl):
+    """(layer index, weight index) of the layer the CPU oracle times, or None for the whole
+    layer pass (tiny and OPT workloads)."""
+    if cfg in (0, 1):
+        return None
+    if cfg == 4:
+        for li, L in enumerate(wl.layers):
+            if L.q.bits == 4 and L.weights[0].name == "q_proj":
+                return li, 0
+    return 0, 0
+
+
+def stated_desc(cfg: int, wl) -> str:
+    st = stated_layer(cfg, wl)
+    if st is None:
+        return f"the whole {wl.name} layer pass"
+    L = wl.layers[st[0]]
+    w = L.weights[st[1]]
+    return (f"{w.name} {w.out}x{w.inp} at {L.q.bits} bits (group {L.q.group}, "
+            f"{'sym' if L.q.sym else 'asym'}{', act_order' if L.q.act_order else ''}) with H from its "
+            f"{L.x.n}x{L.x.d} input")
+
+
+# the reference arm's per-step sample: (tokens for H, rows of the column loop); U in full
+REF_SAMPLE = {2: (2048, 8), 3: (2048, 4), 4: (2048, 8)}
+# the MLP-down layer's CPU baseline: token and row fractions (timed parts scaled up)
+CPU_SAMPLED = {3: (1.0 / 64, 1.0 / 256)}
+
+
+def _oracle_rows_job(job):
+    """Spawned worker: the oracle's quantisation of rows [r0, r1) of one weight given
+    (U, perm, dead) saved under `folder` (rows are independent given U). Returns seconds."""
+    folder, r0, r1, bits, group, sym = job
+    import numpy as np
+    import oracle as O
+    if r1 <= r0:
+        return 0.0
+    U = np.load(os.path.join(folder, "U.npy"), mmap_mode="r")
+    W = np.load(os.path.join(folder, "W.npy"), mmap_mode="r")
+    perm = np.load(os.path.join(folder, "perm.npy"))
+    dead = np.load(os.path.join(folder, "dead.npy"))
+    t0 = time.perf_counter()
+    O.gptq_quantize(np.array(W[r0:r1]), U, perm, dead, bits, group, sym)
+    return time.perf_counter() - t0
+
+
+def _noop_job(_):
+    import numpy  # noqa: F401
+    import oracle  # noqa: F401
+    return 0
+
+
+class RowPool:
+    """A pool of spawned single-threaded processes for the oracle's column loop (spawn, not
+    fork: the parent holds a CUDA context)."""
+
+    def __init__(self, procs: int):
+        import multiprocessing as mp
+        keys = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+        old = {k: os.environ.get(k) for k in keys}
+        for k in keys:
+            os.environ[k] = "1"
+        try:
+            self.pool = mp.get_context("spawn").Pool(procs)
+            self.pool.map(_noop_job, range(procs))   # start-up and imports, untimed
+        finally:
+            for k, v in old.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        self.procs = procs
+
+    def quantize(self, W, U, perm, dead, q) -> float:
+        """Wall seconds of the oracle's gptq_quantize over all rows of W, split by rows."""
+        import numpy as np
+        folder = tempfile.mkdtemp(prefix="oracle_rows_")
+        try:
+            t0 = time.perf_counter()
+            np.save(os.path.join(folder, "U.npy"), np.asarray(U, dtype=np.float64))
+            np.save(os.path.join(folder, "W.npy"), np.asarray(W, dtype=np.float64))
+            np.save(os.path.join(folder, "perm.npy"), np.asarray(perm))
+            np.save(os.path.join(folder, "dead.npy"), np.asarray(dead))
+            rows = W.shape[0]
+            cuts = [rows * i // self.procs for i in range(self.procs + 1)]
+            jobs = [(folder, cuts[i], cuts[i + 1], q.bits, q.group, q.sym) for i in range(self.procs)]
+            self.pool.map(_oracle_rows_job, jobs)
+            return time.perf_counter() - t0
+        finally:
+            for f in os.listdir(folder):
+                os.unlink(os.path.join(folder, f))
+            os.rmdir(folder)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
 
 def oracle_pass(cfg: int, layers_host):
     """One layer pass of the oracle (numpy fp64) over host copies of the inputs; returns
@@ -366,43 +505,95 @@ def oracle_pass(cfg: int, layers_host):
     return t_h, t_p, t_q
 
 
-def host_layers(cfg: int, layers, row_frac: float = 1.0, token_frac: float = 1.0):
+def host_layers(layers):
+    """Host fp64 copies of every layer's input and weights (one copy per distinct input)."""
     import synth
-    out = []
-    xs = {}
+    out, xs = [], {}
     for L in layers:
-        n = L.X.shape[0]
-        if id(L.X) not in xs:   # one host copy per distinct input
-            xs[id(L.X)] = synth.to_numpy_f64(L.X[: max(1, int(round(n * token_frac)))])
-        X = xs[id(L.X)]
-        Ws = [synth.to_numpy_f64(W[: max(1, int(round(W.shape[0] * row_frac)))]) for W in L.Ws]
-        out.append((X, n, Ws, L.spec.q))
+        if id(L.X) not in xs:
+            xs[id(L.X)] = synth.to_numpy_f64(L.X)
+        out.append((xs[id(L.X)], L.X.shape[0], [synth.to_numpy_f64(W) for W in L.Ws], L.spec.q))
     return out
 
 
-def cpu_sample_desc(cfg, row_frac, token_frac=1.0):
-    if row_frac >= 1.0 and token_frac >= 1.0:
-        return (f"the whole workload-{cfg} layer pass in the oracle (numpy fp64: H, inv+cholesky, column loop, "
-                "packing) on the host cores")
-    return (f"workload-{cfg} in the oracle (numpy fp64): H on the first {token_frac:.4g} of the tokens (time scaled "
-            f"by {1 / token_frac:.4g}), inv+cholesky in full, the column loop and packing on the first "
-            f"{row_frac:.4g} of each weight's rows (rows are independent given U; time scaled by {1 / row_frac:.4g})")
+def oracle_stated_layer(cfg: int, wl, X, W, q, pool: "RowPool", token_frac: float = 1.0, row_frac: float = 1.0):
+    """The oracle on one stated layer: S = sum over 2048-token segments of X_b^T X_b (each
+    segment copied from X, a device or host tensor, to host fp64), H = 2 S / n, U, perm, dead,
+    then the column loop over W's rows in the process pool. With token/row fractions below 1
+    only that share is run and its time scaled up (stated in the description).
+    Returns (total ms, {stage: ms})."""
+    import numpy as np
+    import oracle as O
+    import synth
+    n, d = X.shape
+    seg = 2048
+    n_s = max(1, int(round(n * token_frac)))
+    t0 = time.perf_counter()
+    S = None
+    for r in range(0, n_s, seg):
+        Xb = synth.to_numpy_f64(X[r:min(n_s, r + seg)])
+        S = O.xtx(Xb) if S is None else S + O.xtx(Xb)
+    S = S * (n / n_s)
+    H = O.hessian_from_sum(S, n)
+    t1 = time.perf_counter()
+    U, perm, dead = O.prepare(H, q.damp, q.act_order, np.diag(S))
+    t2 = time.perf_counter()
+    rows = W.shape[0]
+    r_s = max(pool.procs, int(round(rows * row_frac)))
+    Wh = synth.to_numpy_f64(W[:r_s])
+    tq = pool.quantize(Wh, U, perm, dead, q)
+    th, tp = (t1 - t0) / (n_s / n), t2 - t1
+    tq = tq * rows / r_s
+    comp = {"hessian": th * 1e3, "prepare": tp * 1e3, "quantize": tq * 1e3}
+    return (th + tp + tq) * 1e3, comp
 
 
-def time_oracle(cfg, layers, row_frac, reps=1, token_frac=1.0):
-    hl = host_layers(cfg, layers, row_frac, token_frac)
-    ts = []
-    for _ in range(reps):
-        t_h, t_p, t_q = oracle_pass(cfg, hl)
-        ts.append(t_h / token_frac + t_p + t_q / row_frac)
-    return ts
+def reference_sample(cfg: int, wl, device="cpu"):
+    """Host inputs of the reference arm's per-step sample (generated on `device` from the
+    workload's seeds; on the CPU the generator differs from the GPU's but the shapes and
+    distributions are the same): the whole pass for the tiny and OPT workloads, else the
+    stated layer's first 2048-token segment and its first few weight rows."""
+    import synth
+    if cfg in (0, 1):
+        _, layers = build_layers(cfg, device)
+        return {"kind": "whole", "layers": host_layers(layers),
+                "desc": f"the whole {wl.name} layer pass in the oracle (numpy fp64), timed per step"}
+    li, wi = stated_layer(cfg, wl)
+    L = wl.layers[li]
+    w = L.weights[wi]
+    n_s, r_s = REF_SAMPLE[cfg]
+    X = synth.make_x_rows(L.x, synth.x_seed(cfg, L.x), 0, n_s, device)
+    W = synth.make_weight(w.out, w.inp, w.std, synth.weight_seed(cfg, w.name), device=device)[:r_s]
+    return {"kind": "stated", "X": synth.to_numpy_f64(X), "n": L.x.n, "W": synth.to_numpy_f64(W), "q": L.q,
+            "rows": w.out,
+            "desc": (f"{stated_desc(cfg, wl)}: H on its first {n_s} tokens (S scaled to n = {L.x.n}), U in full, "
+                     f"the column loop and packing on its first {r_s} of {w.out} rows; timed per step as run, "
+                     "no scaling (one process, threaded BLAS)")}
 
 
-# oracle row fraction per workload: bounded CPU samples (roughly 3-30 s each on 8-16 cores)
-ORACLE_ROW_FRAC = {0: 1.0, 1: 0.125, 2: 1.0 / 256, 3: 1.0 / 1024, 4: 1.0 / 1024}
-CPU_BASELINE_ROW_FRAC = {0: 1.0, 1: 1.0, 2: 1.0 / 64, 3: 1.0 / 512, 4: 1.0 / 512}
-# token fraction for the oracle's H (X^T X is linear in the tokens)
-TOKEN_FRAC = {0: 1.0, 1: 1.0, 2: 1.0 / 16, 3: 1.0 / 64, 4: 1.0 / 64}
+def reference_step(sample):
+    """One step of the reference arm's sample; returns (ms, {stage: ms})."""
+    if sample["kind"] == "whole":
+        t_h, t_p, t_q = oracle_pass(0, sample["layers"])
+        return t_h + t_p + t_q, {"hessian": t_h, "prepare": t_p, "quantize": t_q}
+    t_h, t_p, t_q = oracle_pass(0, [(sample["X"], sample["n"], [sample["W"]], sample["q"])])
+    return t_h + t_p + t_q, {"hessian": t_h, "prepare": t_p, "quantize": t_q}
+
+
+def bench_config(cfg: int, wl, ws: int) -> dict:
+    """The `config` object of both arms' JSON lines (a function of the workload alone)."""
+    xs = {}
+    wbytes = 0
+    for li, L in enumerate(wl.layers):
+        xs[(L.x, li % 4 if cfg == 4 else li)] = L.x.n * L.x.d * (2 if L.x.dtype == "bf16" else 4)
+        wbytes += sum(w.out * w.inp * 4 for w in L.weights)
+    in_bytes = sum(xs.values()) + wbytes
+    flush = in_bytes < 2 * L2_BYTES
+    return {"workload": wl.name, "config_index": cfg,
+            "layers": [[[w.name for w in L.weights], [L.x.n, L.x.d], L.q.bits] for L in wl.layers],
+            "input_bytes": in_bytes,
+            "l2": ("flushed between steps (512 MiB write)" if flush else "inputs larger than L2"),
+            "parallelism": f"replicas x{ws}", "stated_layer": stated_desc(cfg, wl)}
 
 
 # ------------------------------------------------------------------------------ arms
@@ -410,21 +601,36 @@ TOKEN_FRAC = {0: 1.0, 1: 1.0, 2: 1.0 / 16, 3: 1.0 / 64, 4: 1.0 / 64}
 def run_reference(args, ws, rank):
     if rank != 0:
         return
-    import torch
+    import synth
     cores = len(os.sched_getaffinity(0))
-    wl, layers = build_layers(args.config, "cpu")
-    frac = ORACLE_ROW_FRAC[args.config]
-    tf = TOKEN_FRAC[args.config]
-    time_oracle(args.config, layers, frac, reps=min(args.warmup, 1), token_frac=tf)
-    v = statistics.mean(time_oracle(args.config, layers, frac, reps=args.steps, token_frac=tf))
+    wl = synth.workload(args.config)
+    sample = reference_sample(args.config, wl)
+    for _ in range(args.warmup):
+        reference_step(sample)
+    ts, comps = [], []
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        t, c = reference_step(sample)
+        ts.append(t)
+        comps.append(c)
+    wall = (time.perf_counter() - t_wall) * 1e3
+    v = statistics.mean(ts)
+    comp = {k: statistics.mean(c[k] for c in comps) for k in comps[0]}
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "ms", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": v, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic", "config": {"workload": wl.name, "config_index": args.config},
-        "cpu_baseline": {"value": v, "unit": "ms", "cores": cores, "kind": "oracle",
-                         "sample": cpu_sample_desc(args.config, frac, tf)},
+        "dtype": "f64", "data": "synthetic", "config": bench_config(args.config, wl, ws),
+        "sample": sample["desc"], "components_ms": comp, "wall_ms_timed_region": wall,
+        "cpu_baseline": {"value": v, "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample["desc"]},
         "e2e": {"value": v, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    if sample["kind"] == "stated":
+        n_s = sample["X"].shape[0]
+        r_s = sample["W"].shape[0]
+        line["extrapolated_stated_layer_ms"] = (comp["hessian"] * sample["n"] / n_s + comp["prepare"]
+                                                + comp["quantize"] * sample["rows"] / r_s)
+        line["extrapolation"] = ("not measured: the sample's H time x n/tokens + prepare + loop time x "
+                                 "rows/sampled rows, one process")
     print(json.dumps(line), flush=True)
 
 
@@ -458,14 +664,15 @@ def run_ours(args, ws, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pk = peaks()
+    pk["tf32_tflops"] = measure_tf32_peak(dev)
+    pk["tf32_source"] = "cuBLAS TF32 GEMM 8192^3, best of 10, CUDA events, this run"
 
     wl, layers = build_layers(args.config, dev)
     runner = Runner(lib, layers, dev)
     # deferred status reporting: the calls of a step only enqueue work (no host round trip
     # between them); device-side errors are checked once per step with status_sync
     lib.set_status_mode(True)
-    in_bytes = sum(L.X.numel() * L.X.element_size() + sum(W.numel() * 4 for W in L.Ws) for L in layers)
-    flush = in_bytes < 2 * L2_BYTES
+    flush = bench_config(args.config, wl, ws)["input_bytes"] < 2 * L2_BYTES
     fbuf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
 
     def barrier():
@@ -577,11 +784,13 @@ def run_ours(args, ws, rank, local):
         xs = {}
         for L in layers:
             if id(L.X) not in xs:
-                xs[id(L.X)] = (L.X.to("cpu").pin_memory(), torch.empty_like(L.X))
+                hx = torch.empty(L.X.shape, dtype=L.X.dtype, pin_memory=True)
+                hx.copy_(L.X)
+                xs[id(L.X)] = (hx, torch.empty_like(L.X))
         hX = [v[0] for v in xs.values()]
         dXu = [v[1] for v in xs.values()]
         dX = [xs[id(L.X)][1] for L in layers]
-        hW = [L.Wcat.to("cpu").pin_memory() for L in layers]
+        hW = [torch.empty(L.Wcat.shape, dtype=L.Wcat.dtype, pin_memory=True).copy_(L.Wcat) for L in layers]
         dW = [torch.empty_like(L.Wcat) for L in layers]
         h_out = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in o.items()
                   if k in ("packed", "scales", "zeros", "g_idx")} for o in runner.outs]
@@ -611,33 +820,105 @@ def run_ours(args, ws, rank, local):
             et.append((time.perf_counter() - t0) * 1e3)
         e2e = {"value": statistics.mean(et), "unit": "ms", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
 
+    # ---- the stated layer on the GPU (the layer the CPU oracle times whole) ----
+    stated = stated_layer(args.config, wl)
+    gpu_stated_ms = ms if stated is None else time_stated_layer_gpu(lib, runner, layers, stated, dev)
+
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and ws == 1:
-        frac = CPU_BASELINE_ROW_FRAC[args.config]
-        tf = TOKEN_FRAC[args.config]
-        t = time_oracle(args.config, layers, frac, reps=1, token_frac=tf)
-        cpu = {"value": statistics.mean(t), "unit": "ms", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-               "sample": cpu_sample_desc(args.config, frac, tf)}
+        cpu = cpu_baseline(args.config, wl, layers)
 
     if rank == 0:
         value = replica_value(ms, ws)
         line = {
             "metric": METRIC, "value": value, "unit": "ms", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16xbf16->f32 (Hessian), f32 (rest)", "data": "synthetic",
-            "config": {"workload": wl.name, "config_index": args.config,
-                       "layers": [[L.names, list(L.X.shape)] for L in layers],
-                       "l2": ("flushed between steps (512 MiB write)" if flush else "inputs larger than L2"),
-                       "parallelism": f"replicas x{ws}",
-                       "step": ("one CUDA graph of the step's library calls, replayed" if graph is not None
-                                else graph_note or "the library calls issued eagerly")},
+            "warmup": args.warmup, "ms_per_step": ms, "s_per_step": ms / 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16xbf16->f32 (Hessian), f32 (rest)",
+            "data": "synthetic", "config": bench_config(args.config, wl, ws),
+            "step": ("one CUDA graph of the step's library calls, replayed" if graph is not None
+                     else graph_note or "the library calls issued eagerly"),
             "clocks": ck, "gpu_launches": launches // max(1, args.steps) * args.steps,
             "gpu_launches_per_step": launches / max(1, args.steps), "wall_ms_timed_region": wall,
             "stages_ms": stages, "kernels": kernels, "roofline": roof, "e2e": e2e, "cpu_baseline": cpu,
+            "stated_layer": {"what": stated_desc(args.config, wl), "gpu_ms": gpu_stated_ms,
+                             "cpu_ms": cpu["value"] if cpu else None},
             "peaks": pk,
         }
         print(json.dumps(line), flush=True)
+
+
+def time_stated_layer_gpu(lib, runner, layers, stated, dev, reps: int = 5) -> float:
+    """Device time (CUDA events, mean of `reps` after one warm-up) of the stated layer alone:
+    one Hessian pass over its input, gptq_prepare, and gptq_quantize of that one weight."""
+    import torch
+    li, wi = stated
+    L = layers[li]
+    W = L.Ws[wi]
+    q = L.spec.q
+    h = runner.hess[L.X.shape[1]]
+    ws_q = torch.empty(lib.gptq_quantize_workspace_bytes(W.shape[0], W.shape[1], q.bits, q.group, q.sym),
+                       dtype=torch.uint8, device=dev)
+
+    def one():
+        h.reset()
+        h.accumulate(L.X)
+        H, diag, _ = h.finalize()
+        U, perm, dead = lib.gptq_prepare(H, diag, q.damp, act_order=q.act_order, ws=runner.prep_ws[L.X.shape[1]])
+        lib.gptq_quantize(W, U, perm, dead, q.bits, q.group, q.sym, ws=ws_q)
+
+    one()
+    lib.status_sync()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        one()
+        b.record()
+        lib.status_sync()
+        ts.append(a.elapsed_time(b))
+    return statistics.mean(ts)
+
+
+def cpu_baseline(cfg: int, wl, layers) -> dict:
+    """The oracle on this host's cores: the stated layer timed whole (sampled and scaled for
+    the MLP-down layer, which says so), plus one step of the reference arm's sample."""
+    cores = len(os.sched_getaffinity(0))
+    st = stated_layer(cfg, wl)
+    if st is None:
+        t_h, t_p, t_q = oracle_pass(cfg, host_layers(layers))
+        value, comp = t_h + t_p + t_q, {"hessian": t_h, "prepare": t_p, "quantize": t_q}
+        desc = (f"the whole {wl.name} layer pass in the oracle (numpy fp64: H, inv + cholesky, column loop, "
+                f"packing), one process with threaded BLAS/LAPACK on {cores} cores")
+        used = cores
+    else:
+        li, wi = st
+        L = layers[li]
+        pool = RowPool(cores)
+        try:
+            tf, rf = CPU_SAMPLED.get(cfg, (1.0, 1.0))
+            value, comp = oracle_stated_layer(cfg, wl, L.X, L.Ws[wi], L.spec.q, pool, tf, rf)
+        finally:
+            pool.close()
+        used = cores
+        if cfg in CPU_SAMPLED:
+            desc = (f"{stated_desc(cfg, wl)} in the oracle (numpy fp64): H on the first {tf:.4g} of the tokens "
+                    f"(time scaled by {1 / tf:.4g}), inv + cholesky in full, the column loop and packing on "
+                    f"the first {rf:.4g} of the rows split over {cores} processes (time scaled by {1 / rf:.4g}); "
+                    "a whole CPU pass of this layer takes tens of minutes")
+        else:
+            desc = (f"{stated_desc(cfg, wl)}, timed whole in the oracle (numpy fp64): H streamed over all "
+                    f"{L.X.shape[0]} tokens in 2048-token segments and inv + cholesky with threaded "
+                    f"BLAS/LAPACK on {cores} cores, the column loop and packing with the rows split over "
+                    f"{cores} single-threaded processes (rows are independent given U)")
+    out = {"value": value, "unit": "ms", "cores": used, "kind": "oracle", "sample": desc, "components_ms": comp}
+    if st is not None:
+        # one step of the reference arm's per-step sample, on the same host: the two arms'
+        # CPU numbers for the same sample
+        sample = reference_sample(cfg, wl)
+        out["reference_sample_ms"], _ = reference_step(sample)
+        out["reference_sample"] = sample["desc"]
+    return out
 
 
 def run_dequant_matmul(args):
