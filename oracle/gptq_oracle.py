@@ -532,43 +532,79 @@ def prune_saliency(W, U, j0: int, j1: int) -> np.ndarray:
     return (W[:, j0:j1] / u) ** 2
 
 
-def prune_loop(W, U, sparsity: float, block: int = 128) -> Dict[str, np.ndarray]:
+def _force_mask(own, forced, sal, k, tol, b0, log):
+    """Adopt the forced mask of one block where it differs from the oracle's own, if in every
+    such row it prunes exactly k weights and every weight it prunes that the oracle keeps has
+    a saliency within a relative `tol` of the smallest saliency among the weights the oracle
+    prunes instead (a near-tie of the ranking); otherwise raise."""
+    forced = np.asarray(forced, dtype=bool)
+    rows = np.nonzero(np.any(forced != own, axis=1))[0]
+    for i in rows:
+        extra = forced[i] & ~own[i]       # pruned by the forced mask only
+        instead = own[i] & ~forced[i]     # pruned by the oracle only
+        if forced[i].sum() != k or sal[i, extra].max() > (1.0 + tol) * sal[i, instead].min():
+            raise TieMismatch(f"mask mismatch at row {i}, block at column {b0}: forced prunes "
+                              f"{np.nonzero(extra)[0] + b0} (saliency {sal[i, extra]}), oracle "
+                              f"{np.nonzero(instead)[0] + b0} (saliency {sal[i, instead]})")
+        log.append((int(i), int(b0), "mask", float(sal[i, extra].max() / sal[i, instead].min() - 1.0)))
+    out = own.copy()
+    out[rows] = forced[rows]
+    return out
+
+
+def prune_loop(W, U, sparsity: float, block: int = 128, forced_mask=None,
+               tie_tol: float = 1e-4) -> Dict[str, np.ndarray]:
     """The column loop of [loop] with pruning in place of rounding, on an already dead-zeroed,
     already permuted W: per block of `block` columns, each row prunes its
     round(sparsity * width) lowest-saliency weights (stable order on ties); then for every
     column j: q = 0 where pruned, else w_j; err = (w_j - q) / U[j, j];
     W[:, j+1:] -= outer(err, U[j, j+1:]). Returns the pruned-and-compensated W, the mask and
-    per-row sum err^2."""
+    per-row sum err^2.
+
+    Teacher forcing (as gptq_loop's for codes): with `forced_mask`, a block whose forced
+    mask differs from the oracle's own is accepted only where the difference is a near-tie
+    of the saliency ranking (`_force_mask`); the forced mask is then adopted and the loop
+    continues. Accepted differences are returned in 'ties'."""
     W = np.array(W, dtype=F64, copy=True)
     U = np.asarray(U, dtype=F64)
     o, d = W.shape
     mask = np.zeros((o, d), dtype=bool)
     err_sq = np.zeros(o, dtype=F64)
+    ties = []
     for b0 in range(0, d, block):
         b1 = min(d, b0 + block)
         k = int(round(sparsity * (b1 - b0)))
         if k > 0:
-            idx = np.argsort(prune_saliency(W, U, b0, b1), axis=1, kind="stable")[:, :k]
+            sal = prune_saliency(W, U, b0, b1)
+            idx = np.argsort(sal, axis=1, kind="stable")[:, :k]
             np.put_along_axis(mask[:, b0:b1], idx, True, axis=1)
+            if forced_mask is not None:
+                mask[:, b0:b1] = _force_mask(mask[:, b0:b1], np.asarray(forced_mask)[:, b0:b1], sal, k, tie_tol,
+                                             b0, ties)
+        elif forced_mask is not None and np.any(np.asarray(forced_mask)[:, b0:b1]):
+            raise TieMismatch(f"mask mismatch: block at column {b0} prunes nothing")
         for j in range(b0, b1):
             q = np.where(mask[:, j], 0.0, W[:, j])
             err = (W[:, j] - q) / U[j, j]
             W[:, j] = q
             W[:, j + 1:] -= np.outer(err, U[j, j + 1:])
             err_sq += err * err
-    return {"W": W, "mask": mask, "err_sq": err_sq}
+    return {"W": W, "mask": mask, "err_sq": err_sq, "ties": ties}
 
 
-def prune_layer(W, U, perm, dead, sparsity: float, block: int = 128) -> Dict[str, np.ndarray]:
+def prune_layer(W, U, perm, dead, sparsity: float, block: int = 128, forced_mask=None,
+                tie_tol: float = 1e-4) -> Dict[str, np.ndarray]:
     """Pruning of one layer given (U, perm, dead) as `gptq_quantize` takes them: W[:, dead] = 0,
-    columns permuted, `prune_loop`, results back in the original column order."""
+    columns permuted, `prune_loop`, results back in the original column order
+    (`forced_mask`, if given, is in the original column order)."""
     W = np.array(W, dtype=F64, copy=True)
     o, d = W.shape
     W[:, np.asarray(dead, dtype=bool)] = 0.0
     perm = np.arange(d) if perm is None else np.asarray(perm)
-    r = prune_loop(W[:, perm], U, sparsity, block)
+    fm = None if forced_mask is None else np.asarray(forced_mask, dtype=bool)[:, perm]
+    r = prune_loop(W[:, perm], U, sparsity, block, fm, tie_tol)
     inv = np.argsort(perm)
-    return {"W": r["W"][:, inv], "mask": r["mask"][:, inv], "err_sq": r["err_sq"]}
+    return {"W": r["W"][:, inv], "mask": r["mask"][:, inv], "err_sq": r["err_sq"], "ties": r["ties"]}
 
 
 def obs_prune_bruteforce_row(w, H, mask):

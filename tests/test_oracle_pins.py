@@ -570,3 +570,37 @@ def test_prune_layer_permutation_and_dead():
     inv = np.argsort(perm)
     np.testing.assert_array_equal(r["W"], r2["W"][:, inv])
     assert np.all(r["W"][:, dead] == 0.0)
+
+
+def test_prune_forced_mask_accepts_only_near_ties():
+    """Teacher forcing of the pruning mask: the oracle's own mask forced back changes nothing;
+    a mask that swaps two weights of exactly equal saliency is adopted (and logged); a mask
+    that swaps a clearly smaller weight for a larger one is rejected."""
+    rng, X, H, W = _corr_layer(55, 16, 4)
+    U = O.upper_cholesky_of_inverse(H)
+    r = O.prune_loop(W, U, 0.5, 8)
+    same = O.prune_loop(W, U, 0.5, 8, forced_mask=r["mask"])
+    np.testing.assert_array_equal(same["W"], r["W"])
+    assert same["ties"] == []
+    # an exact tie in block 0 of row 0: give the largest pruned weight and the smallest kept
+    # weight of that block the same saliency, then force the other choice
+    W2 = W.copy()
+    sal = O.prune_saliency(W2, U, 0, 8)[0]
+    own = O.prune_loop(W2, U, 0.5, 8)["mask"][0, :8]
+    p_max = np.nonzero(own)[0][np.argmax(sal[own])]
+    k_min = np.nonzero(~own)[0][np.argmin(sal[~own])]
+    W2[0, k_min] = np.sign(W2[0, k_min]) * np.sqrt(sal[p_max]) * U[k_min, k_min]
+    base = O.prune_loop(W2, U, 0.5, 8)
+    fm = base["mask"].copy()
+    a, b = (p_max, k_min) if base["mask"][0, p_max] else (k_min, p_max)
+    fm[0, a], fm[0, b] = False, True
+    forced = O.prune_loop(W2, U, 0.5, 8, forced_mask=fm)
+    assert forced["mask"][0, b] and not forced["mask"][0, a]
+    assert [t[:3] for t in forced["ties"]] == [(0, 0, "mask")]
+    # a clear swap: keep the smallest-saliency weight, prune the largest
+    fm = r["mask"].copy()
+    sal = O.prune_saliency(W, U, 0, 8)[1]
+    lo_, hi_ = int(np.argmin(sal)), int(np.argmax(sal))
+    fm[1, lo_], fm[1, hi_] = False, True
+    with pytest.raises(O.TieMismatch):
+        O.prune_loop(W, U, 0.5, 8, forced_mask=fm)
