@@ -9,6 +9,7 @@
  *   gptq_prepare              dead fix, damping, act_order permutation, U = upper chol(H^-1)
  *   gptq_quantize             the fixed-order column loop -> codes, scales, zeros, g_idx,
  *                             dequantised W, packed codes
+ *   gptq_prune                the same loop pruning instead of rounding (SparseGPT-style)
  *   rtn_quantize              round-to-nearest on the same grid (the baseline)
  *   gptq_pack                 codes -> LSB-first bitstream of b-bit unsigned codes
  *   gptq_dequant_matmul       Y = X Wq^T read straight from the packed codes, scales,
@@ -46,7 +47,8 @@ typedef enum gptq_status {
     GPTQ_ERR_NOT_SPD = 3,       /* a Cholesky pivot was <= 0 or not finite */
     GPTQ_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
     GPTQ_ERR_TIMEOUT = 5,       /* a bounded on-device wait gave up; results are invalid */
-    GPTQ_ERR_WORKSPACE = 6      /* ws_bytes smaller than the matching *_workspace_bytes() */
+    GPTQ_ERR_WORKSPACE = 6,     /* ws_bytes smaller than the matching *_workspace_bytes() */
+    GPTQ_ERR_NONFINITE = 7      /* an input held a NaN or an infinity; results are invalid */
 } gptq_status;
 
 typedef enum gptq_dtype { GPTQ_F32 = 0, GPTQ_BF16 = 1 } gptq_dtype;
@@ -91,9 +93,10 @@ int gptq_hessian_accumulate(gptq_hessian* h, const void* X, int dtype, int64_t n
 
 /* H = 2 S / n written to H (device, d*d fp32, both triangles), diag_xtx[j] = S[j][j]
  * (device, d fp32, the raw diag(X^T X) act_order sorts on; may be NULL), *n_tokens = n
- * (host; may be NULL). Synchronises `stream` to report a device-side timeout (not in the
- * deferred status mode, below).
- * Errors: INVALID_ARG (n == 0), TIMEOUT, CUDA. */
+ * (host; may be NULL). Synchronises `stream` to report a device-side error (not in the
+ * deferred status mode, below). A NaN or infinity anywhere in the accumulated X makes its
+ * channel's S[j][j] non-finite, which is reported as NONFINITE (kept until the next reset).
+ * Errors: INVALID_ARG (n == 0), TIMEOUT, NONFINITE, CUDA. */
 int gptq_hessian_finalize(gptq_hessian* h, float* H, float* diag_xtx, int64_t* n_tokens,
                           void* stream);
 
@@ -114,8 +117,9 @@ int gptq_hessian_destroy(gptq_hessian* h);
  * dead (d uint8, original column order).
  * ws: device workspace of at least gptq_prepare_workspace_bytes(d, act_order) bytes.
  * Synchronises `stream` at the end to report a failed factorisation (not in the deferred
- * status mode, below: the status is then kept for gptq_status_sync).
- * Errors: INVALID_ARG, WORKSPACE, NOT_SPD, CUDA. */
+ * status mode, below: the status is then kept for gptq_status_sync). An entry of H's upper
+ * triangle that is NaN or infinite is reported as NONFINITE (before any pivot check).
+ * Errors: INVALID_ARG, WORKSPACE, NONFINITE, NOT_SPD, CUDA. */
 size_t gptq_prepare_workspace_bytes(int64_t d, int act_order);
 int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, float damp, int act_order,
                  float* U, int32_t* perm, uint8_t* dead, void* ws, size_t ws_bytes, void* stream);
@@ -127,10 +131,11 @@ int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, float damp, i
  * The scratch is a fixed array compiled into the library (about 14 MiB, held on every
  * GPU that loads the library until the process exits), so d is limited to 1024:
  * d > 1024 returns GPTQ_ERR_UNSUPPORTED. Allocates nothing (no cudaMalloc/cudaFree).
- * The first call on a device looks up that device's copy of the array
+ * The first call in each CUDA context (one per device for the runtime's primary contexts;
+ * again after a device reset) looks up that context's copy of the array
  * (cudaGetSymbolAddress); make that first call before any stream capture. All calls share
  * the one array, so calls that overlap on the GPU (other streams, other threads) race;
- * serialise them. Errors: INVALID_ARG, UNSUPPORTED, NOT_SPD, CUDA. */
+ * serialise them. Errors: INVALID_ARG, UNSUPPORTED, NONFINITE, NOT_SPD, CUDA. */
 int gptq_prepare_noalloc(const float* H, const float* diag_xtx, int64_t d, float damp,
                          int act_order, float* U, int32_t* perm, uint8_t* dead, void* stream);
 
@@ -153,9 +158,10 @@ int gptq_prepare_noalloc(const float* H, const float* diag_xtx, int64_t d, float
  *           LSB-first bitstream of unsigned codes u (sym u = code + 2^(bits-1))
  *   row_loss rows fp32 (may be NULL): sum_k err_k^2 per row
  * ws: device workspace of at least gptq_quantize_workspace_bytes(rows, cols, q) bytes.
- * Synchronises `stream` at the end to report a device-side timeout (not in the deferred
- * status mode, below).
- * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, TIMEOUT, CUDA. */
+ * Synchronises `stream` at the end to report a device-side error (not in the deferred
+ * status mode, below). A NaN or infinity in W (outside dead columns, which are not read) or
+ * on U's diagonal is reported as NONFINITE.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, TIMEOUT, NONFINITE, CUDA. */
 size_t gptq_quantize_workspace_bytes(int64_t rows, int64_t cols, gptq_qconfig q);
 int gptq_quantize(const float* W, int64_t rows, int64_t cols, const float* U,
                   const int32_t* perm, const uint8_t* dead, gptq_qconfig q,
@@ -163,10 +169,39 @@ int gptq_quantize(const float* W, int64_t rows, int64_t cols, const float* U,
                   uint32_t* packed, float* row_loss, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Pruning with GPTQ's update.  GPTQ guide page, "Going further" (SparseGPT reuses the same
+ * error-compensation update for pruning); the loop is the one above with the rounding
+ * replaced by pruning. The pages give the update, not the mask rule; the rule here:
+ * at the start of each 128-column block of loop positions, each row prunes the
+ * round(sparsity * width) weights (ties to even, computed in double from the float
+ * sparsity) of smallest saliency (w_k / U[k][k])^2 of its updated weights (the loss the
+ * guide page's "How it works" assigns to removing w_k alone, e^2 / (2 H_F^-1[k][k]) with
+ * H_F^-1[k][k] = U[k][k]^2, factor 1/2 dropped), ties broken by the lower loop position;
+ * then for every k: q = 0 where pruned, q = w_k elsewhere, err = (w_k - q) / U[k][k],
+ * W[:, k+1:] -= err * U[k][k+1:].
+ * Inputs as gptq_quantize (W read only; dead columns zeroed; perm NULL = identity);
+ * sparsity in [0, 1].
+ * Outputs (device, original column order): Wp rows*cols fp32, the pruned and compensated
+ * weights (exactly 0 where pruned); mask rows*cols uint8 (may be NULL), 1 where pruned;
+ * row_loss rows fp32 (may be NULL), sum_k err_k^2 per row.
+ * ws: device workspace of at least gptq_prune_workspace_bytes(rows, cols) bytes.
+ * Synchronises `stream` at the end to report a device-side error (not in the deferred
+ * status mode, below).
+ * Errors: INVALID_ARG (sizes, NULL, sparsity outside [0, 1]), WORKSPACE, TIMEOUT, NONFINITE,
+ * CUDA. */
+size_t gptq_prune_workspace_bytes(int64_t rows, int64_t cols);
+int gptq_prune(const float* W, int64_t rows, int64_t cols, const float* U, const int32_t* perm,
+               const uint8_t* dead, float sparsity, float* Wp, uint8_t* mask, float* row_loss,
+               void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Round-to-nearest baseline (GPTQ's error-compensation loop page, first paragraph; guide
  * page, "The idea"): the same grid with scales from W itself, no error feedback.
  * Same output conventions as gptq_quantize (contiguous groups, no permutation); dead may
- * be NULL. Asynchronous. Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+ * be NULL. Synchronises `stream` at the end to report a NaN or infinity in W (outside dead
+ * columns) as NONFINITE (not in the deferred status mode, below). Allocates nothing (the
+ * call's status word is one of a ring of words in static device memory).
+ * Errors: INVALID_ARG, UNSUPPORTED, NONFINITE, CUDA. */
 int rtn_quantize(const float* W, int64_t rows, int64_t cols, const uint8_t* dead,
                  gptq_qconfig q, int8_t* codes, float* scales, uint8_t* zeros, float* Wq,
                  uint32_t* packed, void* stream);
@@ -200,9 +235,11 @@ int gptq_pack(const int8_t* codes, int64_t rows, int64_t cols, int bits, int sym
  *           GPTQ_DQ_BF16_OUT: Y is bf16 (rounded to nearest even), else fp32
  *   Y       device, (T, N) row-major, row stride ldy elements
  * The weights are expanded to bf16 on chip (rounding each to 8 significant bits) and
- * multiplied on the tensor cores with fp32 accumulation. Synchronises the stream and
- * returns the device status (in the deferred status mode, below, neither). Errors: INVALID_ARG, UNSUPPORTED (bits not 2-4, K % 64,
- * alignment, K or G too large for the shared-memory plan), TIMEOUT, CUDA. */
+ * multiplied on the tensor cores with fp32 accumulation. Allocates nothing (the call's
+ * status word is one of a ring of words in static device memory). Synchronises the stream
+ * and returns the device status (in the deferred status mode, below, neither).
+ * Errors: INVALID_ARG, UNSUPPORTED (bits not 2-4, K % 64, alignment, K or G too large for
+ * the shared-memory plan), TIMEOUT, CUDA. */
 enum { GPTQ_DQ_RELU = 1, GPTQ_DQ_BF16_OUT = 2 };
 int gptq_dequant_matmul(const void* X, int64_t T, int64_t K, int64_t ldx, const uint32_t* packed,
                         const float* scales, const uint8_t* zeros, const int32_t* g_idx, int64_t N,

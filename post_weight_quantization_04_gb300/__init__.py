@@ -23,7 +23,7 @@ GPTQ_BF16 = 1
 
 STATUS = {
     0: "GPTQ_OK", 1: "GPTQ_ERR_INVALID_ARG", 2: "GPTQ_ERR_UNSUPPORTED", 3: "GPTQ_ERR_NOT_SPD",
-    4: "GPTQ_ERR_CUDA", 5: "GPTQ_ERR_TIMEOUT", 6: "GPTQ_ERR_WORKSPACE",
+    4: "GPTQ_ERR_CUDA", 5: "GPTQ_ERR_TIMEOUT", 6: "GPTQ_ERR_WORKSPACE", 7: "GPTQ_ERR_NONFINITE",
 }
 
 # every symbol include/gptq.h declares
@@ -31,7 +31,7 @@ EXPORTS = [
     "gptq_hessian_create", "gptq_hessian_reset", "gptq_hessian_accumulate", "gptq_hessian_finalize",
     "gptq_hessian_destroy", "gptq_prepare_workspace_bytes", "gptq_prepare", "gptq_prepare_noalloc",
     "gptq_quantize_workspace_bytes",
-    "gptq_quantize", "rtn_quantize", "gptq_packed_words_per_row", "gptq_pack", "gptq_dequant_matmul",
+    "gptq_quantize", "gptq_prune_workspace_bytes", "gptq_prune", "rtn_quantize", "gptq_packed_words_per_row", "gptq_pack", "gptq_dequant_matmul",
     "gptq_status_string", "gptq_set_status_mode", "gptq_status_mode", "gptq_status_sync",
     "gptq_launch_count", "gptq_profile_enable", "gptq_profile_read", "gptq_profile_kernel_count",
     "gptq_profile_kernel_name",
@@ -71,6 +71,8 @@ def _declare(lib: ctypes.CDLL) -> None:
         "gptq_quantize_workspace_bytes": (_SZ, [_I64, _I64, QConfig]),
         "gptq_quantize": (_I, [_P, _I64, _I64, _P, _P, _P, QConfig, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
         "rtn_quantize": (_I, [_P, _I64, _I64, _P, QConfig, _P, _P, _P, _P, _P, _P]),
+        "gptq_prune_workspace_bytes": (_SZ, [_I64, _I64]),
+        "gptq_prune": (_I, [_P, _I64, _I64, _P, _P, _P, _F, _P, _P, _P, _P, _SZ, _P]),
         "gptq_packed_words_per_row": (_I64, [_I64, _I]),
         "gptq_pack": (_I, [_P, _I64, _I64, _I, _I, _P, _P]),
         "gptq_dequant_matmul": (_I, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _I64, _I64, _I, _I, _P, _I64, _P]),
@@ -83,6 +85,8 @@ def _declare(lib: ctypes.CDLL) -> None:
         "gptq_profile_read": (_I, [_P, _P, _I]),
         "gptq_profile_kernel_count": (_I, []),
         "gptq_profile_kernel_name": (ctypes.c_char_p, [_I]),
+        # test hook (exported, deliberately not declared in gptq.h)
+        "gptq_test_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -272,6 +276,37 @@ def gptq_quantize(W: torch.Tensor, U: torch.Tensor, perm: Optional[torch.Tensor]
         _ptr(W), rows, cols, _ptr(U), _ptr(perm), _ptr(dead), qconfig(bits, group, sym, zero_in_range),
         _ptr(o["codes"]), _ptr(o["scales"]), _ptr(o["zeros"]), _ptr(o["g_idx"]), _ptr(o.get("Wq")),
         _ptr(o.get("packed")), _ptr(o["row_loss"]), _ptr(ws), ws.numel(), _stream(stream)))
+    return o
+
+
+def gptq_prune_workspace_bytes(rows: int, cols: int) -> int:
+    return int(load().gptq_prune_workspace_bytes(rows, cols))
+
+
+def gptq_prune(W: torch.Tensor, U: torch.Tensor, perm: Optional[torch.Tensor] = None,
+               dead: Optional[torch.Tensor] = None, sparsity: float = 0.5, ws: Optional[torch.Tensor] = None,
+               out: Optional[Dict[str, torch.Tensor]] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """Pruning with GPTQ's update: Wp (pruned and compensated, 0 where pruned), mask (uint8,
+    1 where pruned) and row_loss, all in the original column order."""
+    rows, cols = W.shape
+    _dev(W, torch.float32, "W")
+    _dev(U, torch.float32, "U", (cols, cols))
+    if perm is not None:
+        _dev(perm, torch.int32, "perm", (cols,))
+    if dead is not None:
+        _dev(dead, torch.uint8, "dead", (cols,))
+    dev = W.device
+    nb = gptq_prune_workspace_bytes(rows, cols)
+    if ws is None:
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    o = out if out is not None else {
+        "Wp": torch.empty(rows, cols, dtype=torch.float32, device=dev),
+        "mask": torch.empty(rows, cols, dtype=torch.uint8, device=dev),
+        "row_loss": torch.empty(rows, dtype=torch.float32, device=dev),
+    }
+    _check("gptq_prune", load().gptq_prune(
+        _ptr(W), rows, cols, _ptr(U), _ptr(perm), _ptr(dead), float(sparsity), _ptr(o["Wp"]), _ptr(o.get("mask")),
+        _ptr(o.get("row_loss")), _ptr(ws), ws.numel(), _stream(stream)))
     return o
 
 

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "gptq.h"
 
@@ -50,6 +51,48 @@ int device_sm_count();
 // The end of an entry point: report the call's device status word at once (synchronising
 // the stream) or, in deferred mode, fold it into the device's sticky status and return OK.
 int finish_call(const int* status, cudaStream_t s);
+
+// The unique id of the CUDA context current on this thread (cuCtxGetId: never reused in
+// the life of the process, so an address cached under it cannot outlive a device reset or
+// belong to another context); 0 when no context is current or the driver lacks the call.
+unsigned long long current_context_id();
+
+// A device pointer per CUDA context (the address of a file-scope __device__ array in that
+// context), looked up once per context by its owner and kept for the life of the process.
+struct ContextPtrCache {
+    static constexpr int kEntries = 16;
+    std::mutex mu;
+    unsigned long long id[kEntries] = {};
+    void* ptr[kEntries] = {};
+    int n = 0;
+    void* find(unsigned long long cid) {
+        if (!cid) return nullptr;
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < n && i < kEntries; ++i)
+            if (id[i] == cid) return ptr[i];
+        return nullptr;
+    }
+    void put(unsigned long long cid, void* p) {
+        if (!cid) return;
+        std::lock_guard<std::mutex> lk(mu);
+        const int i = n % kEntries;   // the oldest entry goes first once all are used
+        id[i] = cid;
+        ptr[i] = p;
+        ++n;
+    }
+};
+
+// A device status word for one call of an entry point that has no workspace (the consumer
+// of the stored form, round-to-nearest): one of a ring of words in static device memory
+// (nothing is allocated), cleared on `s`. Calls in flight at the same time get different
+// words unless a few hundred calls are issued while one is still running.
+cudaError_t call_status_word(cudaStream_t s, int** out);
+
+// Test hook support: sets this library's limit on pipeline mbarrier waits (mbar_wait) in
+// every translation unit that has such waits; the drain waits keep kWaitLimitNs.
+cudaError_t hessian_set_wait_limit(unsigned long long ns);
+cudaError_t tc_gemm_set_wait_limit(unsigned long long ns);
+cudaError_t dequant_set_wait_limit(unsigned long long ns);
 
 static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -98,6 +141,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // lets the kernel unwind (no kernel waits on another launch or another device).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// The limit of the pipeline waits (mbar_wait) of this translation unit, kWaitLimitNs unless a
+// test lowers it through the library's test hook (a limit of 0 gives up at the first wait
+// that is not already complete). The drain waits, which let in-flight copies and MMAs land
+// before a CTA exits, always use kWaitLimitNs.
+static __device__ unsigned long long g_pipeline_wait_limit_ns = kWaitLimitNs;
+
+static inline cudaError_t set_pipeline_wait_limit_this_unit(unsigned long long ns) {
+    return cudaMemcpyToSymbol(g_pipeline_wait_limit_ns, &ns, sizeof(ns));
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -137,11 +190,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                                           int* status) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const uint64_t limit = *static_cast<volatile unsigned long long*>(&g_pipeline_wait_limit_ns);
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0) {
+        if ((it & 255u) == 0 || limit == 0) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 >= limit) {
                 *abort_flag = 1;
                 set_status(status, GPTQ_ERR_TIMEOUT);
                 return false;

@@ -67,14 +67,34 @@ struct DParams {
     // odd and zp / 4 odd so the 32 rows a warp reads hit 32 different banks
     int tab, sp, zp;
     int g_off, s_off, z_off;
-    int gs;           // group size in columns (the grouped kernel)
-    const int* contig;  // device word: 1 when g_idx[k] == k / gs for every k (set by g_contig_kernel)
+    int gs;           // the grouped kernel's group size in columns; for the general kernel the
+                      // group size of the grouped kernel launched with it, 0 if none was
 };
 
-// contig = 1 unless some column's group differs from k / gs (contig preset to 1)
-__global__ void g_contig_kernel(const int32_t* __restrict__ g_idx, int K, int gs, int* contig) {
-    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < K; k += gridDim.x * blockDim.x)
-        if (g_idx[k] != k / gs) *contig = 0;
+// Whether every column's group is g_idx[k] == k / gs (contiguous groups of gs columns), as
+// the whole CTA sees it. Both kernels of a call decide with the same test, so exactly one
+// of them does the work; the other returns before touching shared memory or TMEM.
+__device__ __forceinline__ bool cta_groups_contiguous(const int32_t* __restrict__ g_idx, int K, int gs) {
+    int bad = 0;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) bad |= (g_idx[k] != k / gs) ? 1 : 0;
+    return __syncthreads_or(bad) == 0;
+}
+
+// Named barrier ID over N threads that also ANDs a predicate across them: a group of warps
+// that shares a named barrier inside its tile loop leaves the loop together (a warp whose
+// bounded wait gave up must not leave the others waiting at that barrier).
+template <int ID, int N>
+__device__ __forceinline__ bool bar_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %1, 0;\n\t"
+        "barrier.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)(v ? 1 : 0)), "n"(ID), "n"(N)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ uint32_t bf16x2(float a, float b) {
@@ -97,7 +117,7 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity, int* status
 template <int BITS, bool TAB>
 __global__ void __launch_bounds__(D_THREADS, 1) dequant_matmul_kernel(const __grid_constant__ CUtensorMap tX,
                                                                      const DParams p) {
-    if (p.contig && *p.contig) return;   // the grouped kernel of the same call does the work
+    if (p.gs > 0 && cta_groups_contiguous(p.g_idx, p.K, p.gs)) return;   // the grouped kernel does the work
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + D_RING);
@@ -355,7 +375,10 @@ __global__ void __launch_bounds__(D_THREADS, 1) dequant_matmul_kernel(const __gr
         int ws = 0, ps = 0, tab_tn = -1;
         uint32_t wph = 0, pph = 0;
         bool ok = true;
-        for (int t = t_begin; t < t_end && ok; ++t) {
+        for (int t = t_begin; t < t_end; ++t) {
+            // all expansion warps leave together if any of them gave up a wait; this barrier
+            // also means every thread is done with the previous tile's table
+            if (!bar_all<2, 32 * D_DQ_WARPS>(ok)) break;
             const int tn = t / tiles_m;
             const float* srow[4];
             const uint8_t* zrow[4];
@@ -371,7 +394,6 @@ __global__ void __launch_bounds__(D_THREADS, 1) dequant_matmul_kernel(const __gr
             if (TAB && tn != tab_tn) {
                 // this tile's scales and zero points, read once, coalesced
                 tab_tn = tn;
-                dq_sync();  // every thread is done with the previous tile's table
                 const int64_t n = (int64_t)D_BN * p.G;
                 for (int64_t idx = i; idx < n; idx += NDQ) {
                     const int rr = (int)(idx / p.G), g = (int)(idx - (int64_t)rr * p.G);
@@ -498,7 +520,7 @@ constexpr uint32_t G_TMEM_COLS = 512;  // three partials, then the running total
 template <int BITS>
 __global__ void __launch_bounds__(GQ_THREADS, 1) dequant_matmul_grouped_kernel(const __grid_constant__ CUtensorMap tX,
                                                                              const DParams p) {
-    if (!*p.contig) return;   // scattered groups: the general kernel of the same call does the work
+    if (!cta_groups_contiguous(p.g_idx, p.K, p.gs)) return;   // scattered groups: the general kernel's work
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + D_RING);
@@ -645,12 +667,14 @@ __global__ void __launch_bounds__(GQ_THREADS, 1) dequant_matmul_grouped_kernel(c
         bool ok = true;
         const bool vec = ((p.ldy & 7) == 0) && ((reinterpret_cast<uintptr_t>(p.Y) & 15) == 0);
         const uint32_t lanes = (uint32_t)(32 * q) << 16;
-        for (int t = t_begin; t < t_end && ok; ++t) {
+        for (int t = t_begin; t < t_end; ++t) {
+            // all epilogue warps leave together if any of them gave up a wait; this barrier
+            // also means every thread is done with the previous tile's table
+            if (!bar_all<3, 32 * GQ_EPI_WARPS>(ok)) break;
             const int tm = t % tiles_m, tn = t / tiles_m;
             if (tn != tab_tn) {
                 // this tile's scales, [output][group], read once, coalesced
                 tab_tn = tn;
-                asm volatile("bar.sync 3, %0;" ::"n"(32 * GQ_EPI_WARPS) : "memory");
                 if (et < D_BN) {
                     const int o = tn * D_BN + et;   // thread et fills output et's column of the table
                     for (int g = 0; g < ngroups; ++g)
@@ -784,14 +808,16 @@ __global__ void __launch_bounds__(GQ_THREADS, 1) dequant_matmul_grouped_kernel(c
         int ws = 0, ps = 0, tab_tn = -1;
         uint32_t wph = 0, pph = 0;
         bool ok = true;
-        for (int t = t_begin; t < t_end && ok; ++t) {
+        for (int t = t_begin; t < t_end; ++t) {
+            // all expansion warps leave together if any of them gave up a wait; this barrier
+            // also means every thread is done with the previous tile's table
+            if (!bar_all<2, 32 * GQ_DQ_WARPS>(ok)) break;
             const int tn = t / tiles_m;
             bool live[GQ_ITEMS];
 #pragma unroll
             for (int it = 0; it < GQ_ITEMS; ++it) live[it] = tn * D_BN + rb + RS * it < p.N;
             if (tn != tab_tn) {
                 tab_tn = tn;
-                dq_sync();
                 const int64_t n = (int64_t)D_BN * p.G;
                 for (int64_t idx = i; idx < n; idx += NDQ) {
                     const int rr = (int)(idx / p.G), g = (int)(idx - (int64_t)rr * p.G);
@@ -910,9 +936,9 @@ extern "C" int gptq_dequant_matmul(const void* X, int64_t T, int64_t K, int64_t 
     const int smem = (int)(p.tab ? with_tab : up16(p.g_off + 2 * K) + 1024);
     if (smem > D_SMEM_MAX) return GPTQ_ERR_UNSUPPORTED;
     // Contiguous groups whose size is a multiple of the K step (no act_order) go to the exact
-    // grouped kernel, the rest to the general one. Contiguity is checked on the device
-    // (g_contig_kernel); both kernels are launched and the one that does not apply returns
-    // at once.
+    // grouped kernel, the rest to the general one. Contiguity is checked on the device by
+    // every CTA of both kernels (cta_groups_contiguous); both kernels are launched and the one
+    // that does not apply returns at once.
     // (the grouped kernel has its own shared-memory layout: a copy of the parameters)
     const bool maybe_grouped = K % G == 0 && (K / G) % D_BK == 0;
     DParams pg = p;
@@ -925,20 +951,14 @@ extern "C" int gptq_dequant_matmul(const void* X, int64_t T, int64_t K, int64_t 
         if (need <= D_SMEM_MAX) gsmem = (int)need;
     }
     const bool grouped = gsmem > 0;
-    int* words2 = nullptr;   // status, contiguity flag
-    GPTQ_CUDA_TRY(cudaMallocAsync(reinterpret_cast<void**>(&words2), 2 * sizeof(int), s));
-    int* status = words2;
+    p.gs = grouped ? pg.gs : 0;   // the general kernel steps aside when the grouped one applies
+    // the call's status word: static device memory, cleared on the stream (no allocation)
+    int* status = nullptr;
+    GPTQ_CUDA_TRY(call_status_word(s, &status));
     p.status = status;
-    p.contig = grouped ? words2 + 1 : nullptr;
     pg.status = status;
-    pg.contig = words2 + 1;
-    const int init[2] = {0, 1};
-    GPTQ_CUDA_TRY(cudaMemcpyAsync(words2, init, sizeof(init), cudaMemcpyHostToDevice, s));
     const int grid = std::min(p.ntiles, device_sm_count());
     if (grouped) {
-        GPTQ_LAUNCH(K_DEQUANT_MM, s, g_contig_kernel<<<(unsigned)std::min<int64_t>(ceil_div(K, 256), 64), 256, 0, s>>>(
-                                         g_idx, (int)K, pg.gs, words2 + 1));
-        GPTQ_LAUNCH_CHECK();
         auto gk = bits == 2 ? dequant_matmul_grouped_kernel<2>
                 : bits == 3 ? dequant_matmul_grouped_kernel<3> : dequant_matmul_grouped_kernel<4>;
         GPTQ_CUDA_TRY(cudaFuncSetAttribute(gk, cudaFuncAttributeMaxDynamicSharedMemorySize, gsmem));
@@ -952,7 +972,10 @@ extern "C" int gptq_dequant_matmul(const void* X, int64_t T, int64_t K, int64_t 
     GPTQ_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
     GPTQ_LAUNCH(K_DEQUANT_MM, s, kern<<<grid, D_THREADS, smem, s>>>(tx, p));
     GPTQ_LAUNCH_CHECK();
-    const int rc = finish_call(status, s);   // reads the status word before it is freed
-    GPTQ_CUDA_TRY(cudaFreeAsync(words2, s));
-    return rc;
+    return finish_call(status, s);
 }
+
+namespace gptq {
+// this file's copy of the pipeline-wait limit (the library's test hook sets every copy)
+cudaError_t dequant_set_wait_limit(unsigned long long ns) { return set_pipeline_wait_limit_this_unit(ns); }
+}  // namespace gptq

@@ -361,8 +361,12 @@ __global__ void __launch_bounds__(256) hessian_simt_kernel(const T* __restrict__
 }
 
 // H[i][j] = scale * S[min(i,j)][max(i,j)], diag_xtx[j] = S[j][j]
+// H = scale * S (both triangles from S's upper one), diag = diag(S). A diagonal entry that
+// is not finite (a NaN or an infinity anywhere in the accumulated X makes its channel's
+// S[j][j] one) records GPTQ_ERR_NONFINITE.
 __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ S, int64_t d, float scale,
-                                                      float* __restrict__ H, float* __restrict__ diag) {
+                                                      float* __restrict__ H, float* __restrict__ diag,
+                                                      int* __restrict__ status) {
     __shared__ float T[32][33];
     const int ti = blockIdx.y, tj = blockIdx.x;
     const int lo = min(ti, tj), hi = max(ti, tj);
@@ -380,7 +384,10 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__
         else if (ti > tj) v = T[tx][r];
         else v = (r <= tx) ? T[r][tx] : T[tx][r];
         H[gi * d + gj] = scale * v;
-        if (diag && gi == gj) diag[gi] = v;
+        if (gi == gj) {
+            if (diag) diag[gi] = v;
+            if (!isfinite(v)) set_status(status, GPTQ_ERR_NONFINITE);
+        }
     }
 }
 
@@ -530,7 +537,8 @@ extern "C" int gptq_hessian_finalize(gptq_hessian* h, float* H, float* diag_xtx,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const float scale = (float)(2.0 / (double)h->n);
     const unsigned nt = (unsigned)ceil_div(h->d, 32);
-    GPTQ_LAUNCH(K_FINALIZE, s, finalize_kernel<<<dim3(nt, nt), 256, 0, s>>>(h->S, h->d, scale, H, diag_xtx));
+    GPTQ_LAUNCH(K_FINALIZE, s, finalize_kernel<<<dim3(nt, nt), 256, 0, s>>>(h->S, h->d, scale, H, diag_xtx,
+                                                                                   h->status));
     GPTQ_LAUNCH_CHECK();
     if (n_tokens) *n_tokens = h->n;
     return finish_call(h->status, s);
@@ -550,3 +558,8 @@ extern "C" int gptq_hessian_destroy(gptq_hessian* h) {
     delete h;
     return GPTQ_OK;
 }
+
+namespace gptq {
+// this file's copy of the pipeline-wait limit (the library's test hook sets every copy)
+cudaError_t hessian_set_wait_limit(unsigned long long ns) { return set_pipeline_wait_limit_this_unit(ns); }
+}  // namespace gptq

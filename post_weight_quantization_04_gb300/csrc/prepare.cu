@@ -98,14 +98,16 @@ PrepWs carve(void* base, int64_t d) {
 }
 
 // dead[j] = (H[j][j] == 0); the dead diagonal becomes 1; mean of the fixed diagonal in
-// fp64; damped diagonal (rounded to fp32) and its inverse square root in fp32.
+// fp64; damped diagonal (rounded to fp32) and its inverse square root in fp32. A diagonal
+// entry that is not finite records GPTQ_ERR_NONFINITE.
 __global__ void __launch_bounds__(1024) prep_diag_kernel(const float* __restrict__ H, int64_t d, float damp,
                                                         uint8_t* __restrict__ dead, float* __restrict__ ddiag,
-                                                        float* __restrict__ rr) {
+                                                        float* __restrict__ rr, int* __restrict__ status) {
     __shared__ double part[32];
     double s = 0.0;
     for (int64_t j = threadIdx.x; j < d; j += blockDim.x) {
         const float h = H[j * d + j];
+        if (!isfinite(h)) set_status(status, GPTQ_ERR_NONFINITE);
         const bool dj = (h == 0.0f);
         dead[j] = dj ? 1 : 0;
         s += dj ? 1.0 : (double)h;
@@ -156,10 +158,12 @@ __global__ void iota_kernel(int32_t* __restrict__ perm, int64_t d) {
 }
 
 // A[i][j] (j <= i) = Hh[d-1-i][d-1-j], Hh = D^-1/2 Hp D^-1/2, Hp = H[perm][:, perm]
-// (fixed, damped diagonal; H read from its upper triangle).
+// (fixed, damped diagonal; H read from its upper triangle). An off-diagonal entry that is not
+// finite records GPTQ_ERR_NONFINITE.
 __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restrict__ H, int64_t d,
                                                          const int32_t* __restrict__ perm,
-                                                         const float* __restrict__ rr, float* __restrict__ A) {
+                                                         const float* __restrict__ rr, float* __restrict__ A,
+                                                         int* __restrict__ status) {
     const int64_t i = (int64_t)blockIdx.y * 8 + (threadIdx.x >> 5);
     const int64_t jb = (int64_t)blockIdx.x * 32;
     if (i >= d || jb > i) return;
@@ -172,7 +176,9 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
         v = 1.0f;
     } else {
         const int32_t lo = a < b ? a : b, hi = a < b ? b : a;
-        v = H[(int64_t)lo * d + hi] * rr[a] * rr[b];
+        const float h = H[(int64_t)lo * d + hi];
+        if (!isfinite(h)) set_status(status, GPTQ_ERR_NONFINITE);
+        v = h * rr[a] * rr[b];
     }
     A[i * d + j] = v;
 }
@@ -626,7 +632,7 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
     cudaStream_t s = static_cast<cudaStream_t>(stream_);
 
     GPTQ_CUDA_TRY(cudaMemsetAsync(w.status, 0, sizeof(int), s));
-    GPTQ_LAUNCH(K_PREP_DIAG, s, prep_diag_kernel<<<1, 1024, 0, s>>>(H, d, damp, dead, w.ddiag, w.rr));
+    GPTQ_LAUNCH(K_PREP_DIAG, s, prep_diag_kernel<<<1, 1024, 0, s>>>(H, d, damp, dead, w.ddiag, w.rr, w.status));
     GPTQ_LAUNCH_CHECK();
     const unsigned g1 = (unsigned)ceil_div(d, 256);
     if (act_order)
@@ -636,7 +642,7 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
     GPTQ_LAUNCH_CHECK();
     {
         dim3 grid((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 8));
-        GPTQ_LAUNCH(K_PREP_GATHER, s, prep_gather_kernel<<<grid, 256, 0, s>>>(H, d, perm, w.rr, w.A));
+        GPTQ_LAUNCH(K_PREP_GATHER, s, prep_gather_kernel<<<grid, 256, 0, s>>>(H, d, perm, w.rr, w.A, w.status));
         GPTQ_LAUNCH_CHECK();
     }
 
@@ -919,8 +925,6 @@ extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, fl
 // exits. The entry point itself allocates nothing: no cudaMalloc, cudaFree or allocating
 // library routine.
 // ------------------------------------------------------------------------------------
-#include <mutex>
-
 namespace gptq {
 namespace {
 
@@ -928,14 +932,15 @@ constexpr int64_t kNoAllocMaxD = 1024;
 
 // the workspace gptq_prepare carves for d = kNoAllocMaxD
 constexpr size_t kNoAllocBytes = prep_ws_bytes(kNoAllocMaxD);
-constexpr int kMaxDevices = 64;
 
 // Host code must not use this name as an address: on the host it is only a stand-in for
-// the device symbol. The device address comes from cudaGetSymbolAddress, per device.
+// the device symbol. The device address comes from cudaGetSymbolAddress, per CUDA context.
 static __device__ __align__(256) unsigned char g_prepare_scratch[kNoAllocBytes];
 
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices] = {};
+// the array's address in each CUDA context that has called the entry point (keyed by the
+// context's unique id: a device reset or another context on the same device gets its own
+// lookup, never a stale address)
+ContextPtrCache g_noalloc_addr;
 
 }  // namespace
 }  // namespace gptq
@@ -947,23 +952,15 @@ extern "C" int gptq_prepare_noalloc(const float* H, const float* diag_xtx, int64
     if (d > kNoAllocMaxD) return GPTQ_ERR_UNSUPPORTED;
     const size_t need = gptq_prepare_workspace_bytes(d, act_order);
     if (need > kNoAllocBytes) return GPTQ_ERR_UNSUPPORTED;
-    int dev = 0;
-    GPTQ_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= kMaxDevices) return GPTQ_ERR_UNSUPPORTED;
-    void* scratch = nullptr;
-    {
-        // first call on a device: look up this device's copy of the array (once)
-        std::lock_guard<std::mutex> lk(g_noalloc_mu);
-        if (!g_noalloc_ptr[dev]) {
-            void* p = nullptr;
-            const cudaError_t e = cudaGetSymbolAddress(&p, g_prepare_scratch);
-            if (e != cudaSuccess || p == nullptr) {
-                (void)cudaGetLastError();
-                return GPTQ_ERR_CUDA;
-            }
-            g_noalloc_ptr[dev] = p;
+    void* scratch = g_noalloc_addr.find(current_context_id());
+    if (!scratch) {
+        // first call in this context: look up this context's copy of the array (once)
+        const cudaError_t e = cudaGetSymbolAddress(&scratch, g_prepare_scratch);
+        if (e != cudaSuccess || scratch == nullptr) {
+            (void)cudaGetLastError();
+            return GPTQ_ERR_CUDA;
         }
-        scratch = g_noalloc_ptr[dev];
+        g_noalloc_addr.put(current_context_id(), scratch);   // the lookup made the context current
     }
     // every slab gptq_prepare reads is written by it first (its status word is cleared),
     // so the previous call's contents need no clearing here

@@ -24,6 +24,8 @@
 // The working copy of W lives in the caller's workspace, permuted into loop order with
 // dead columns zeroed (guide page, "Source code": W[:, dead] = 0, W = W[:, perm]).
 // Outputs go straight to the original column order.
+#include <math.h>
+
 #include <algorithm>
 
 #include "common.cuh"
@@ -81,11 +83,14 @@ bool group_ok(int group) { return group == 0 || (group > 0 && (group % QB == 0 |
 
 // Wk[r][k] = dead[perm[k]] ? 0 : W[r][perm[k]]
 // Four consecutive loop columns per thread (one 16-byte store when cols % 4 == 0), IW_ROWS
-// rows per CTA so the permutation and dead flags are read once for several rows.
+// rows per CTA so the permutation and dead flags are read once for several rows. A weight
+// that is not finite (outside a dead column, which is never read) records
+// GPTQ_ERR_NONFINITE.
 constexpr int IW_ROWS = 4;
 __global__ void __launch_bounds__(256) init_work_kernel(const float* __restrict__ W, int64_t rows, int64_t cols,
                                                         const int32_t* __restrict__ perm,
-                                                        const uint8_t* __restrict__ dead, float* __restrict__ Wk) {
+                                                        const uint8_t* __restrict__ dead, float* __restrict__ Wk,
+                                                        int* __restrict__ status) {
     const int64_t k0 = 4 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x);
     if (k0 >= cols) return;
     const int nk = cols - k0 < 4 ? (int)(cols - k0) : 4;
@@ -106,7 +111,13 @@ __global__ void __launch_bounds__(256) init_work_kernel(const float* __restrict_
         const float* src = W + r * cols;
         float v[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = z[e] ? 0.0f : src[c[e]];
+        bool bad = false;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            v[e] = z[e] ? 0.0f : src[c[e]];
+            bad |= !isfinite(v[e]);
+        }
+        if (bad) set_status(status, GPTQ_ERR_NONFINITE);
         float* dst = Wk + r * cols + k0;
         if (vec) {
             *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
@@ -168,6 +179,9 @@ struct BlockArgs {
     uint8_t* zeros;
     int64_t G;
     float* loss;
+    int* status;
+    int prune_k;        // pruning: weights pruned per row in this block
+    uint8_t* mask;      // pruning: optional rows x cols mask output (original column order)
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -184,7 +198,13 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // and of the next one (`nxt`), updated with the same operations as the owner's, so the
 // column-to-column dependency never goes through a shuffle: the next chunk is fetched
 // from its owner one chunk ahead.
-template <int TPR, bool SMALL_GROUPS>
+//
+// PRUNE: the same loop with pruning in place of rounding (the GPTQ guide page's "Going
+// further": SparseGPT reuses this update). At the block start each row ranks its block's
+// saliencies (w_j / U[j][j])^2 of the updated weights (stable: ties by column) and prunes
+// the a.prune_k smallest; then for every column q = 0 where pruned and q = w_j elsewhere
+// (err = 0 there, so kept weights are left to the compensation of later columns).
+template <int TPR, bool SMALL_GROUPS, bool PRUNE = false>
 __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
     constexpr int CPT = QB / TPR;   // columns per thread
     constexpr int NCH = CPT / 4;    // 4-column chunks per thread
@@ -219,10 +239,18 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
         }
     }
     __syncthreads();
-    invd[threadIdx.x] = (threadIdx.x < bw) ? 1.0f / us[threadIdx.x * QB + threadIdx.x] : 0.0f;
+    bool u_bad = false;   // a diagonal entry of U that is not finite (reported after the wait)
+    if (threadIdx.x < bw) {
+        const float ujj = us[threadIdx.x * QB + threadIdx.x];
+        u_bad = !isfinite(ujj);
+        invd[threadIdx.x] = 1.0f / ujj;
+    } else {
+        invd[threadIdx.x] = 0.0f;
+    }
     __syncthreads();
     pdl_wait();
     pdl_trigger();
+    if (u_bad && blockIdx.x == 0) set_status(a.status, GPTQ_ERR_NONFINITE);
 
     const int sub = threadIdx.x % TPR;
     const int64_t row = (int64_t)blockIdx.x * RPC + threadIdx.x / TPR;
@@ -289,8 +317,75 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
         return gg;
     };
 
+    // pruning: the row's mask over the block's 128 columns (bit c % 32 of word c / 32), the
+    // same in every lane of the row
+    uint32_t pm0 = 0u, pm1 = 0u, pm2 = 0u, pm3 = 0u;
+    if constexpr (PRUNE) {
+        float sal[CPT];
+        int rank[CPT];
+#pragma unroll
+        for (int m = 0; m < NCH; ++m)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c = col_of(m, e);
+                const float t = w[4 * m + e] * (c < bw ? invd[c] : 0.0f);
+                sal[4 * m + e] = c < bw ? t * t : INFINITY;
+                rank[4 * m + e] = 0;
+            }
+        // rank of each own weight: how many of the block's weights come before it in the
+        // stable ascending order of saliency (smaller, or equal at a lower column)
+#pragma unroll
+        for (int m = 0; m < NCH; ++m) {
+#pragma unroll 1
+            for (int o = 0; o < TPR; ++o) {
+                if (4 * (m * TPR + o) >= bw) break;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = 4 * (m * TPR + o) + e;
+                    const float v = __shfl_sync(0xffffffffu, sal[4 * m + e], o, TPR);
+                    if (c >= bw) continue;
+#pragma unroll
+                    for (int mm = 0; mm < NCH; ++mm)
+#pragma unroll
+                        for (int ee = 0; ee < 4; ++ee) {
+                            const float sv = sal[4 * mm + ee];
+                            rank[4 * mm + ee] += (v < sv || (v == sv && c < col_of(mm, ee))) ? 1 : 0;
+                        }
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < NCH; ++m)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c = col_of(m, e);
+                if (c < bw && rank[4 * m + e] < a.prune_k) {
+                    const uint32_t bit = 1u << (c & 31);
+                    const int wd = c >> 5;
+                    pm0 |= wd == 0 ? bit : 0u;
+                    pm1 |= wd == 1 ? bit : 0u;
+                    pm2 |= wd == 2 ? bit : 0u;
+                    pm3 |= wd == 3 ? bit : 0u;
+                }
+            }
+#pragma unroll
+        for (int off = TPR / 2; off > 0; off >>= 1) {
+            pm0 |= __shfl_xor_sync(0xffffffffu, pm0, off, TPR);
+            pm1 |= __shfl_xor_sync(0xffffffffu, pm1, off, TPR);
+            pm2 |= __shfl_xor_sync(0xffffffffu, pm2, off, TPR);
+            pm3 |= __shfl_xor_sync(0xffffffffu, pm3, off, TPR);
+        }
+    }
+    auto pruned = [&](int jj) -> bool {
+        const int wd = jj >> 5;
+        const uint32_t word = wd == 0 ? pm0 : wd == 1 ? pm1 : wd == 2 ? pm2 : pm3;
+        return (word >> (jj & 31)) & 1u;
+    };
+
     Grid g{1.0f, 1.0f, 0.0f};
-    if (!inblock_groups) {
+    if (PRUNE) {
+        // no grid
+    } else if (!inblock_groups) {
         if (active) {
             g.s = a.cur_s[row];
             g.inv_s = 1.0f / g.s;
@@ -327,8 +422,13 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
         for (int mm = 0; mm < NCH; ++mm)
             if (mm >= m) uo[mm] = *reinterpret_cast<const float4*>(ur + col_of(mm, 0));
         const float wj = cur[e];
-        const float cf = grid_code_f(wj, g, sym, flo, fhi);
-        const float q = grid_dequant_f(cf, g, sym);
+        float cf = 0.0f, q;
+        if constexpr (PRUNE) {
+            q = pruned(jj) ? 0.0f : wj;
+        } else {
+            cf = grid_code_f(wj, g, sym, flo, fhi);
+            q = grid_dequant_f(cf, g, sym);
+        }
         const float err = (wj - q) * id;
         if (sub == o) {
             cr[4 * m + e] = (int8_t)(int)cf;
@@ -372,7 +472,7 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
             for (int e = 0; e < 4; ++e) {
                 const int jj = 4 * cc + e;
                 if (jj >= bw) break;
-                if (SMALL_GROUPS && jj == next_gs) {
+                if (!PRUNE && SMALL_GROUPS && jj == next_gs) {
                     next_gs += a.group;
                     g = group_grid(jj, min(jj + a.group, bw));
                 }
@@ -408,7 +508,11 @@ __global__ void __launch_bounds__(128) gptq_block_kernel(const BlockArgs a) {
             const int lc = c0 + e;
             if (lc < bw) {
                 const int64_t oc = a.perm ? (int64_t)a.perm[a.j0 + lc] : a.j0 + lc;
-                a.codes[row * a.cols + oc] = cr[4 * m + e];
+                if constexpr (PRUNE) {
+                    if (a.mask) a.mask[row * a.cols + oc] = pruned(lc) ? 1 : 0;
+                } else {
+                    a.codes[row * a.cols + oc] = cr[4 * m + e];
+                }
                 if (a.Wq) a.Wq[row * a.cols + oc] = qr[4 * m + e];
             }
         }
@@ -424,7 +528,46 @@ __global__ void g_idx_kernel(const int32_t* __restrict__ perm, int64_t cols, int
 }
 
 
-// One thread per output word: bits [32w, 32w+32) of the row's LSB-first b-bit stream.
+// Rows whose length is a multiple of 32 codes: 32 codes fill exactly BITS words, so chunk c
+// of the flat code array (codes 32c .. 32c+31, two 16-byte loads) becomes words
+// BITS*c .. BITS*c+BITS-1 of the flat packed array (one 16- or 8-byte store for 4 and 2
+// bits, three 4-byte stores for 3). Grid-stride over the chunks; each byte is read once and
+// each word written once, with streaming cache hints.
+template <int BITS>
+__global__ void __launch_bounds__(256) pack32_kernel(const int8_t* __restrict__ codes, int64_t chunks, int offset,
+                                                     uint32_t* __restrict__ packed) {
+    constexpr uint32_t mask = (1u << BITS) - 1u;
+    for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < chunks;
+         c += (int64_t)gridDim.x * blockDim.x) {
+        const int4* src = reinterpret_cast<const int4*>(codes) + 2 * c;
+        const int4 v0 = __ldcs(src), v1 = __ldcs(src + 1);
+        const uint32_t b[8] = {(uint32_t)v0.x, (uint32_t)v0.y, (uint32_t)v0.z, (uint32_t)v0.w,
+                               (uint32_t)v1.x, (uint32_t)v1.y, (uint32_t)v1.z, (uint32_t)v1.w};
+        uint32_t w[BITS];
+#pragma unroll
+        for (int k = 0; k < BITS; ++k) w[k] = 0u;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            // the low BITS bits of (code byte + offset): carries out of the byte are masked off
+            const uint32_t u = ((b[i >> 2] >> (8 * (i & 3))) + (uint32_t)offset) & mask;
+            const int pos = i * BITS;
+            w[pos >> 5] |= u << (pos & 31);
+            if ((pos & 31) + BITS > 32) w[(pos >> 5) + 1] |= u >> (32 - (pos & 31));
+        }
+        uint32_t* dst = packed + (int64_t)BITS * c;
+        if constexpr (BITS == 4) {
+            __stcs(reinterpret_cast<uint4*>(dst), make_uint4(w[0], w[1], w[2], w[3]));
+        } else if constexpr (BITS == 2) {
+            __stcs(reinterpret_cast<uint2*>(dst), make_uint2(w[0], w[1]));
+        } else {
+#pragma unroll
+            for (int k = 0; k < BITS; ++k) __stcs(dst + k, w[k]);
+        }
+    }
+}
+
+// One thread per output word: bits [32w, 32w+32) of the row's LSB-first b-bit stream (any
+// row length and alignment).
 __global__ void pack_kernel(const int8_t* __restrict__ codes, int64_t rows, int64_t cols, int bits, int offset,
                             int64_t words, uint32_t* __restrict__ packed) {
     const int64_t r = blockIdx.y;
@@ -444,9 +587,11 @@ __global__ void pack_kernel(const int8_t* __restrict__ codes, int64_t rows, int6
 }
 
 // Round-to-nearest: one warp per (row, group) (group > 0) or one CTA per row (group == 0).
+// A weight that is not finite (outside a dead column) records GPTQ_ERR_NONFINITE.
 __global__ void rtn_group_kernel(const float* __restrict__ W, int64_t rows, int64_t cols, const uint8_t* __restrict__ dead,
                                  int bits, int sym, int zr, int group, int64_t G, int8_t* __restrict__ codes,
-                                 float* __restrict__ scales, uint8_t* __restrict__ zeros, float* __restrict__ Wq) {
+                                 float* __restrict__ scales, uint8_t* __restrict__ zeros, float* __restrict__ Wq,
+                                 int* __restrict__ status) {
     const int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (task >= rows * G) return;
@@ -454,12 +599,15 @@ __global__ void rtn_group_kernel(const float* __restrict__ W, int64_t rows, int6
     const int64_t c0 = gi * group, c1 = std::min<int64_t>(cols, c0 + group);
     const float* row = W + r * cols;
     float mx = -INFINITY, mn = INFINITY, am = 0.0f;
+    bool bad = false;
     for (int64_t c = c0 + lane; c < c1; c += 32) {
         const float v = (dead && dead[c]) ? 0.0f : row[c];
+        bad |= !isfinite(v);
         mx = fmaxf(mx, v);
         mn = fminf(mn, v);
         am = fmaxf(am, fabsf(v));
     }
+    if (bad) set_status(status, GPTQ_ERR_NONFINITE);
     const int qmax = sym ? (1 << (bits - 1)) - 1 : (1 << bits) - 1;
     const Grid g = sym ? sym_grid(warp_max(am), qmax) : asym_grid(warp_min(mn), warp_max(mx), qmax, zr != 0);
     if (lane == 0) {
@@ -478,17 +626,21 @@ __global__ void rtn_group_kernel(const float* __restrict__ W, int64_t rows, int6
 __global__ void __launch_bounds__(256) rtn_row_kernel(const float* __restrict__ W, int64_t rows, int64_t cols,
                                                      const uint8_t* __restrict__ dead, int bits, int sym, int zr,
                                                      int8_t* __restrict__ codes, float* __restrict__ scales,
-                                                     uint8_t* __restrict__ zeros, float* __restrict__ Wq) {
+                                                     uint8_t* __restrict__ zeros, float* __restrict__ Wq,
+                                                     int* __restrict__ status) {
     const int64_t r = blockIdx.x;
     const float* row = W + r * cols;
     __shared__ float red[3][8];
     float mx = -INFINITY, mn = INFINITY, am = 0.0f;
+    bool bad = false;
     for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) {
         const float v = (dead && dead[c]) ? 0.0f : row[c];
+        bad |= !isfinite(v);
         mx = fmaxf(mx, v);
         mn = fminf(mn, v);
         am = fmaxf(am, fabsf(v));
     }
+    if (bad) set_status(status, GPTQ_ERR_NONFINITE);
     mx = warp_max(mx);
     mn = warp_min(mn);
     am = warp_max(am);
@@ -523,6 +675,19 @@ __global__ void __launch_bounds__(256) rtn_row_kernel(const float* __restrict__ 
 }
 
 int launch_pack(const int8_t* codes, int64_t rows, int64_t cols, int bits, int sym, uint32_t* packed, cudaStream_t s) {
+    const int offset = sym ? (1 << (bits - 1)) : 0;
+    if (cols % 32 == 0 && (reinterpret_cast<uintptr_t>(codes) & 15) == 0 &&
+        (reinterpret_cast<uintptr_t>(packed) & 15) == 0) {
+        const int64_t chunks = rows * (cols / 32);
+        const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(chunks, 256), (int64_t)device_sm_count() * 8);
+        switch (bits) {
+            case 2: GPTQ_LAUNCH(K_PACK, s, pack32_kernel<2><<<grid, 256, 0, s>>>(codes, chunks, offset, packed)); break;
+            case 3: GPTQ_LAUNCH(K_PACK, s, pack32_kernel<3><<<grid, 256, 0, s>>>(codes, chunks, offset, packed)); break;
+            default: GPTQ_LAUNCH(K_PACK, s, pack32_kernel<4><<<grid, 256, 0, s>>>(codes, chunks, offset, packed)); break;
+        }
+        GPTQ_LAUNCH_CHECK();
+        return GPTQ_OK;
+    }
     const int64_t words = gptq_packed_words_per_row(cols, bits);
     const unsigned gx = (unsigned)std::min<int64_t>(ceil_div(words, 256), 1024);
     dim3 grid(gx, (unsigned)rows);
@@ -556,19 +721,19 @@ extern "C" int gptq_pack(const int8_t* codes, int64_t rows, int64_t cols, int bi
     return launch_pack(codes, rows, cols, bits, sym, packed, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const float* U, const int32_t* perm,
-                             const uint8_t* dead, gptq_qconfig q, int8_t* codes, float* scales, uint8_t* zeros,
-                             int32_t* g_idx, float* Wq, uint32_t* packed, float* row_loss, void* ws, size_t ws_bytes,
-                             void* stream) {
-    if (rows < 0 || cols < 0) return GPTQ_ERR_INVALID_ARG;
-    if (q.bits < 2 || q.bits > 4 || !group_ok(q.group)) return GPTQ_ERR_UNSUPPORTED;
-    if (rows == 0 || cols == 0) return GPTQ_OK;
-    if (!W || !U || !codes || !scales || !zeros || !ws || rows > 65535) return GPTQ_ERR_INVALID_ARG;
+namespace gptq {
+namespace {
+
+// The column loop shared by gptq_quantize and gptq_prune (prune_sparsity < 0: quantize).
+int column_loop(const float* W, int64_t rows, int64_t cols, const float* U, const int32_t* perm,
+                const uint8_t* dead, gptq_qconfig q, int8_t* codes, float* scales, uint8_t* zeros, int32_t* g_idx,
+                float* Wq, uint32_t* packed, float* row_loss, void* ws, size_t ws_bytes, void* stream,
+                double prune_sparsity, uint8_t* mask) {
+    const bool prune = prune_sparsity >= 0.0;
     QuantWs w = carve(ws, rows, cols);
     if (ws_bytes < w.bytes) return GPTQ_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool sym = q.sym != 0;
-    const int64_t G = q.group ? ceil_div(cols, q.group) : 1;
+    const int64_t G = (!prune && q.group) ? ceil_div(cols, q.group) : 1;
 
     // (the memsets first: every later item in the stream is one of this call's kernels, so
     // the block and trailing kernels may be launched as programmatic dependents)
@@ -578,14 +743,14 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
     GPTQ_CUDA_TRY(cudaMemsetAsync(w.status, 0, sizeof(int), s));
     {
         dim3 grid((unsigned)ceil_div(cols, 4 * 256), (unsigned)ceil_div(rows, IW_ROWS));
-        GPTQ_LAUNCH(K_INIT_WORK, s, init_work_kernel<<<grid, 256, 0, s>>>(W, rows, cols, perm, dead, w.W));
+        GPTQ_LAUNCH(K_INIT_WORK, s, init_work_kernel<<<grid, 256, 0, s>>>(W, rows, cols, perm, dead, w.W, w.status));
         GPTQ_LAUNCH_CHECK();
     }
     // tensor-core trailing update when every row of W and U is 16-byte aligned
     const bool tc = (cols % 4 == 0) && tc_gemm_nt_ok(w.W, cols);
     if (tc) GPTQ_CUDA_TRY(split_cols(K_SPLIT, U, cols, (int)cols, (int)cols, w.uhi, w.ulo, (int)cols, s));
     const unsigned pgrid = (unsigned)ceil_div(rows, 8);
-    if (q.group == 0) {
+    if (!prune && q.group == 0) {
         GPTQ_LAUNCH(K_ROW_PARAMS, s, row_params_kernel<<<pgrid, 256, 0, s>>>(w.W, rows, cols, 0, cols, q.bits, q.sym, q.zero_in_range,
                                                                              w.cur_s, w.cur_z, scales, zeros, G, 0));
         GPTQ_LAUNCH_CHECK();
@@ -602,8 +767,16 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         }
     }
     const size_t smem = sizeof(float) * QB * QB;
-    const bool small_groups = q.group > 0 && q.group < QB;
+    const bool small_groups = !prune && q.group > 0 && q.group < QB;
     auto block_fn = [&](int t) -> void (*)(BlockArgs) {
+        if (prune) {
+            switch (t) {
+                case 32: return gptq_block_kernel<32, false, true>;
+                case 16: return gptq_block_kernel<16, false, true>;
+                case 8: return gptq_block_kernel<8, false, true>;
+                default: return gptq_block_kernel<4, false, true>;
+            }
+        }
         switch (t) {
             case 32: return small_groups ? gptq_block_kernel<32, true> : gptq_block_kernel<32, false>;
             case 16: return small_groups ? gptq_block_kernel<16, true> : gptq_block_kernel<16, false>;
@@ -621,7 +794,7 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
     a.bits = q.bits;
     a.sym = q.sym;
     a.zr = q.zero_in_range;
-    a.group = q.group;
+    a.group = prune ? 0 : q.group;
     a.cur_s = w.cur_s;
     a.cur_z = w.cur_z;
     a.Err = w.Err;
@@ -633,10 +806,12 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
     a.zeros = zeros;
     a.G = G;
     a.loss = loss;
+    a.status = w.status;
+    a.mask = mask;
     const unsigned bgrid = (unsigned)ceil_div(rows, 128 / tpr);
     for (int64_t j0 = 0; j0 < cols; j0 += QB) {
         const int bw = (int)std::min<int64_t>(QB, cols - j0);
-        if (q.group > QB && j0 % q.group == 0) {
+        if (!prune && q.group > QB && j0 % q.group == 0) {
             GPTQ_LAUNCH(K_ROW_PARAMS, s,
                         row_params_kernel<<<pgrid, 256, 0, s>>>(w.W, rows, cols, j0,
                                                                 std::min<int64_t>(cols, j0 + q.group), q.bits, q.sym,
@@ -646,6 +821,8 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
         }
         a.j0 = j0;
         a.bw = bw;
+        // pruning: round(sparsity * width), ties to even, in double
+        a.prune_k = prune ? (int)std::nearbyint(prune_sparsity * (double)bw) : 0;
         // this block's errors go to its slot of the super-block's split
         const int64_t sb0 = j0 / (SB * QB) * (SB * QB), sb_end = std::min<int64_t>(cols, sb0 + SB * QB);
         a.ehi = tc ? w.ehi + (j0 - sb0) : nullptr;
@@ -680,9 +857,7 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
                                     U + j0 * cols + e, cols, 1.0f, w.W + e, cols, false, s));
             }
         }
-
     }
-    (void)sym;
 
     if (g_idx) {
         GPTQ_LAUNCH(K_G_IDX, s, g_idx_kernel<<<(unsigned)ceil_div(cols, 256), 256, 0, s>>>(perm, cols, q.group, g_idx));
@@ -695,6 +870,38 @@ extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const f
     return finish_call(w.status, s);
 }
 
+}  // namespace
+}  // namespace gptq
+
+extern "C" int gptq_quantize(const float* W, int64_t rows, int64_t cols, const float* U, const int32_t* perm,
+                             const uint8_t* dead, gptq_qconfig q, int8_t* codes, float* scales, uint8_t* zeros,
+                             int32_t* g_idx, float* Wq, uint32_t* packed, float* row_loss, void* ws, size_t ws_bytes,
+                             void* stream) {
+    if (rows < 0 || cols < 0) return GPTQ_ERR_INVALID_ARG;
+    if (q.bits < 2 || q.bits > 4 || !group_ok(q.group)) return GPTQ_ERR_UNSUPPORTED;
+    if (rows == 0 || cols == 0) return GPTQ_OK;
+    if (!W || !U || !codes || !scales || !zeros || !ws || rows > 65535) return GPTQ_ERR_INVALID_ARG;
+    return column_loop(W, rows, cols, U, perm, dead, q, codes, scales, zeros, g_idx, Wq, packed, row_loss, ws,
+                       ws_bytes, stream, -1.0, nullptr);
+}
+
+extern "C" size_t gptq_prune_workspace_bytes(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return carve(nullptr, rows, cols).bytes;
+}
+
+extern "C" int gptq_prune(const float* W, int64_t rows, int64_t cols, const float* U, const int32_t* perm,
+                          const uint8_t* dead, float sparsity, float* Wp, uint8_t* mask, float* row_loss, void* ws,
+                          size_t ws_bytes, void* stream) {
+    if (rows < 0 || cols < 0) return GPTQ_ERR_INVALID_ARG;
+    if (!(sparsity >= 0.0f && sparsity <= 1.0f)) return GPTQ_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return GPTQ_OK;
+    if (!W || !U || !Wp || !ws || rows > 65535) return GPTQ_ERR_INVALID_ARG;
+    gptq_qconfig q{4, 0, 1, 0};   // unused by the pruning loop
+    return column_loop(W, rows, cols, U, perm, dead, q, nullptr, nullptr, nullptr, nullptr, Wp, nullptr, row_loss,
+                       ws, ws_bytes, stream, (double)sparsity, mask);
+}
+
 extern "C" int rtn_quantize(const float* W, int64_t rows, int64_t cols, const uint8_t* dead, gptq_qconfig q,
                             int8_t* codes, float* scales, uint8_t* zeros, float* Wq, uint32_t* packed, void* stream) {
     if (rows < 0 || cols < 0) return GPTQ_ERR_INVALID_ARG;
@@ -702,18 +909,27 @@ extern "C" int rtn_quantize(const float* W, int64_t rows, int64_t cols, const ui
     if (rows == 0 || cols == 0) return GPTQ_OK;
     if (!W || !codes || !scales || !zeros || rows > 65535) return GPTQ_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the call's status word (static device memory, cleared on the stream: no allocation)
+    int* status = nullptr;
+    GPTQ_CUDA_TRY(call_status_word(s, &status));
     if (q.group == 0) {
-        GPTQ_LAUNCH(K_RTN, s, rtn_row_kernel<<<(unsigned)rows, 256, 0, s>>>(W, rows, cols, dead, q.bits, q.sym, q.zero_in_range, codes, scales, zeros, Wq));
+        GPTQ_LAUNCH(K_RTN, s, rtn_row_kernel<<<(unsigned)rows, 256, 0, s>>>(W, rows, cols, dead, q.bits, q.sym,
+                                                                             q.zero_in_range, codes, scales, zeros,
+                                                                             Wq, status));
     } else {
         const int64_t G = ceil_div(cols, q.group);
         const int64_t tasks = rows * G;
         GPTQ_LAUNCH(K_RTN, s,
-                    rtn_group_kernel<<<(unsigned)ceil_div(tasks, 8), 256, 0, s>>>(W, rows, cols, dead, q.bits, q.sym, q.zero_in_range,
-                                                                                  q.group, G, codes, scales, zeros, Wq));
+                    rtn_group_kernel<<<(unsigned)ceil_div(tasks, 8), 256, 0, s>>>(W, rows, cols, dead, q.bits, q.sym,
+                                                                                  q.zero_in_range, q.group, G, codes,
+                                                                                  scales, zeros, Wq, status));
     }
     GPTQ_LAUNCH_CHECK();
-    if (packed) return launch_pack(codes, rows, cols, q.bits, q.sym, packed, s);
-    return GPTQ_OK;
+    if (packed) {
+        const int rc = launch_pack(codes, rows, cols, q.bits, q.sym, packed, s);
+        if (rc != GPTQ_OK) return rc;
+    }
+    return finish_call(status, s);
 }
 
 extern "C" const char* gptq_status_string(int status) {
@@ -725,6 +941,7 @@ extern "C" const char* gptq_status_string(int status) {
         case GPTQ_ERR_CUDA: return "CUDA error";
         case GPTQ_ERR_TIMEOUT: return "on-device wait timed out";
         case GPTQ_ERR_WORKSPACE: return "workspace too small";
+        case GPTQ_ERR_NONFINITE: return "input not finite (NaN or infinity)";
         default: return "unknown status";
     }
 }

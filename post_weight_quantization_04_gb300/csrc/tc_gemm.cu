@@ -804,3 +804,8 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
 }
 
 }  // namespace gptq
+
+namespace gptq {
+// this file's copy of the pipeline-wait limit (the library's test hook sets every copy)
+cudaError_t tc_gemm_set_wait_limit(unsigned long long ns) { return set_pipeline_wait_limit_this_unit(ns); }
+}  // namespace gptq

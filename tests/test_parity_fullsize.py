@@ -98,6 +98,41 @@ def test_llama7b_attention_projection(lib):
     _layer(lib, layers[0], rng, row_sample=256)
 
 
+def test_llama7b_attention_end_to_end_from_oracle_chain(lib):
+    """One comparison over the whole chain at full size: the oracle's own fp64 H (streamed
+    over all 262144 tokens from the same bf16 bits), its own inv + Cholesky U, and its
+    free-running loop on a sample of rows, against the GPU's Hessian -> prepare -> quantize
+    of the same layer; the sampled rows' relative output error (through the oracle's S)
+    within 2%."""
+    wl, layers = bench.build_layers(2, "cuda")
+    L = layers[0]
+    q = L.spec.q
+    X, W = L.X, L.Ws[0]
+    n, d = X.shape
+    S = None
+    for r in range(0, n, 8192):
+        Xb = synth.to_numpy_f64(X[r:r + 8192])
+        S = O.xtx(Xb) if S is None else S + O.xtx(Xb)
+    Href = O.hessian_from_sum(S, n)
+    Uref, pref, dref = O.prepare(Href, q.damp, q.act_order, np.diag(S))
+    h = lib.Hessian(d)
+    h.accumulate(X)
+    H, diag, _ = h.finalize()
+    U, perm, dead = lib.gptq_prepare(H, diag, q.damp, act_order=q.act_order)
+    out = lib.gptq_quantize(W, U, perm, dead, q.bits, q.group, q.sym)
+    rng = np.random.default_rng(22)
+    rows = np.sort(rng.choice(W.shape[0], 128, replace=False))
+    ri = torch.as_tensor(rows, device=W.device)
+    Wr = synth.to_numpy_f64(W[ri])
+    ref = O.gptq_quantize(Wr, Uref, pref, dref, q.bits, q.group, q.sym)
+    e_gpu = O.rel_output_error_from_xtx(S, Wr, npy(out["Wq"][ri]))
+    e_ref = O.rel_output_error_from_xtx(S, Wr, ref["Wq"])
+    print(f"end to end from the oracle's H and U: gpu {e_gpu:.6f} oracle {e_ref:.6f}")
+    assert abs(e_gpu - e_ref) <= 0.02 * e_ref, (e_gpu, e_ref)
+    np.testing.assert_array_equal(npy(perm), pref)
+    np.testing.assert_array_equal(npy(dead).astype(bool), dref)
+
+
 def test_mlp_down_projection_act_order(lib):
     wl, layers = bench.build_layers(3, "cuda")
     rng = np.random.default_rng(3)

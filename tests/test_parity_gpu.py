@@ -138,6 +138,9 @@ QCASES = [
     (50, 384, 3, 32, False, True),
     # several super-blocks of the deferred trailing update, ragged last block
     (64, 1100, 4, 128, False, True),
+    # cols % 4 != 0: the FFMA trailing update (TMA needs 16-byte rows) and the any-length packer
+    (130, 301, 4, 128, False, True),
+    (70, 458, 3, 0, True, False),
 ]
 
 
@@ -280,13 +283,30 @@ def test_rtn_exact_at_half_points(lib, bits, group, sym):
     np.testing.assert_array_equal(npy(out["codes"]).astype(np.int64), ref["codes"])
 
 
-@pytest.mark.parametrize("bits,sym,cols", [(2, True, 64), (3, True, 96), (3, False, 100), (4, False, 33)])
-def test_pack_bit_exact(lib, bits, sym, cols):
+@pytest.mark.parametrize("bits,sym,cols,rows", [(2, True, 64, 11), (3, True, 96, 11), (3, False, 100, 11),
+                                                (4, False, 33, 11), (4, True, 4096, 301), (3, True, 3072, 97),
+                                                (2, False, 1024, 257), (4, False, 14336, 5)])
+def test_pack_bit_exact(lib, bits, sym, cols, rows):
+    """Rows of a multiple of 32 codes take the 32-codes-per-thread packer, others the
+    one-word-per-thread packer; both bit-exact against the oracle's bitstream."""
     rng = np.random.default_rng(bits * 100 + cols)
     lo, hi = (-(2 ** (bits - 1) - 1), 2 ** (bits - 1) - 1) if sym else (0, 2 ** bits - 1)
-    codes = rng.integers(lo, hi + 1, size=(11, cols))
+    codes = rng.integers(lo, hi + 1, size=(rows, cols))
     p = lib.gptq_pack(torch.tensor(codes.astype(np.int8), device=DEV), bits, sym)
     np.testing.assert_array_equal(npy(p).view(np.uint32), O.pack_rows(O.unsigned_codes(codes, bits, sym), bits))
+
+
+def test_pack_misaligned_codes_take_the_general_packer(lib):
+    """Codes that do not start on a 16-byte boundary (a view one byte into a buffer) are packed
+    by the general kernel, with the same result."""
+    rng = np.random.default_rng(5)
+    codes = rng.integers(-7, 8, size=(40, 256)).astype(np.int8)
+    buf = torch.zeros(codes.size + 1, dtype=torch.int8, device=DEV)
+    buf[1:] = torch.tensor(codes.reshape(-1), device=DEV)
+    view = buf[1:].view(40, 256)
+    assert view.data_ptr() % 16 != 0
+    p = lib.gptq_pack(view, 4, True)
+    np.testing.assert_array_equal(npy(p).view(np.uint32), O.pack_rows(O.unsigned_codes(codes, 4, True), 4))
 
 
 # ---------------------------------------------------------------------------- end to end
