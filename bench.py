@@ -52,7 +52,27 @@ def parse(argv=None):
     ap.add_argument("--op", choices=["layer", "dequant_matmul", "layerwise"], default="layer")
     ap.add_argument("--mlp", default="mlp4096")
     ap.add_argument("--tokens", type=int, default=8192)
+    # smaller cases of the same shapes (profiler captures that must stay within a few GB):
+    # fewer calibration tokens per layer input, or one bit width of the decoder block's sweep
+    ap.add_argument("--x-tokens", type=int, default=0, help="calibration tokens per input (default: the workload's)")
+    ap.add_argument("--bits", type=int, default=0, help="keep only the layers of this bit width")
     return ap.parse_args(argv)
+
+
+def workload_for(args):
+    """The workload recipe, reduced by --x-tokens / --bits when given (the name says so)."""
+    import dataclasses
+    import synth
+    wl = synth.workload(args.config)
+    if not args.x_tokens and not args.bits:
+        return wl
+    layers = [L for L in wl.layers if not args.bits or L.q.bits == args.bits]
+    if not layers:
+        raise SystemExit(f"no layer of {args.bits} bits in workload {args.config}")
+    if args.x_tokens:
+        layers = [dataclasses.replace(L, x=dataclasses.replace(L.x, n=args.x_tokens)) for L in layers]
+    name = wl.name + (f"-x{args.x_tokens}" if args.x_tokens else "") + (f"-only{args.bits}b" if args.bits else "")
+    return dataclasses.replace(wl, name=name, layers=layers)
 
 
 def dist_info():
@@ -141,14 +161,22 @@ class Layer:
         self.names = names
 
 
-def build_layers(cfg: int, device, host: bool = False):
+def x_group(cfg: int, wl, li: int) -> int:
+    """Which distinct input layer li of the workload reads: the decoder block's four inputs
+    (q/k/v, o, gate/up, down) repeat across its bit widths; elsewhere one input per layer."""
+    if cfg != 4:
+        return li
+    return ("q_proj", "o_proj", "gate_proj", "down_proj").index(wl.layers[li].weights[0].name)
+
+
+def build_layers(cfg: int, device, host: bool = False, wl=None):
     import torch
     import synth
-    wl = synth.workload(cfg)
+    wl = wl or synth.workload(cfg)
     layers = []
     xcache = {}
     for li, L in enumerate(wl.layers):
-        key = (L.x, li % 4 if cfg == 4 else li)
+        key = (L.x, x_group(cfg, wl, li))
         if key not in xcache:
             seed = synth.x_seed(cfg, L.x) + (key[1] if cfg == 4 else 0)
             xcache[key] = synth.make_x(L.x, seed, device=device)
@@ -585,7 +613,7 @@ def bench_config(cfg: int, wl, ws: int) -> dict:
     xs = {}
     wbytes = 0
     for li, L in enumerate(wl.layers):
-        xs[(L.x, li % 4 if cfg == 4 else li)] = L.x.n * L.x.d * (2 if L.x.dtype == "bf16" else 4)
+        xs[(L.x, x_group(cfg, wl, li))] = L.x.n * L.x.d * (2 if L.x.dtype == "bf16" else 4)
         wbytes += sum(w.out * w.inp * 4 for w in L.weights)
     in_bytes = sum(xs.values()) + wbytes
     flush = in_bytes < 2 * L2_BYTES
@@ -603,7 +631,7 @@ def run_reference(args, ws, rank):
         return
     import synth
     cores = len(os.sched_getaffinity(0))
-    wl = synth.workload(args.config)
+    wl = workload_for(args)
     sample = reference_sample(args.config, wl)
     for _ in range(args.warmup):
         reference_step(sample)
@@ -667,7 +695,7 @@ def run_ours(args, ws, rank, local):
     pk["tf32_tflops"] = measure_tf32_peak(dev)
     pk["tf32_source"] = "cuBLAS TF32 GEMM 8192^3, best of 10, CUDA events, this run"
 
-    wl, layers = build_layers(args.config, dev)
+    wl, layers = build_layers(args.config, dev, wl=workload_for(args))
     runner = Runner(lib, layers, dev)
     # deferred status reporting: the calls of a step only enqueue work (no host round trip
     # between them); device-side errors are checked once per step with status_sync
