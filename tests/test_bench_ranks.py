@@ -73,3 +73,27 @@ def test_reference_arm_json_contract():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    # the same config object our arm prints (built from the workload alone)
+    args = bench.parse(["--config", "0"])
+    assert line["config"] == json.loads(json.dumps(bench.bench_config(0, bench.workload_for(args), 1)))
+    # what was timed is stated, and the timed region fits the steps it claims
+    assert "whole" in line["sample"]
+    assert line["wall_ms_timed_region"] >= line["value"] * line["steps"] * 0.99
+
+
+def test_reference_arm_decoder_block_sample_is_bounded():
+    """The default workload's reference arm times a bounded sample of the stated layer per step
+    (seconds, not minutes) and reports any whole-layer estimate apart from `value`."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0"],
+                         cwd=root, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["config"]["workload"].startswith("llama3-8b-block")
+    assert "q_proj" in line["config"]["stated_layer"] and "first 8 of 4096 rows" in line["sample"]
+    assert line["value"] < 60_000
+    assert line["extrapolated_stated_layer_ms"] > line["value"]
+    assert "not measured" in line["extrapolation"]
