@@ -356,13 +356,21 @@ TRAFFIC = {
 }
 
 
-def peak_for(bound, pk):
+def peak_for(bound, pk, sustained: bool = False):
+    """The roofline denominator of a kernel class. Tensor peaks are the burst figures for a
+    short timed region and the sustained ones (seconds of back-to-back GEMMs under the power
+    cap) for a timed region of a second or more; the TF32 sustained figure is the measured
+    TF32 burst scaled by the measured bf16 sustained/burst ratio."""
+    ratio = (pk["bf16_tflops_sustained"] / pk["bf16_tflops"]) if (sustained and pk.get("bf16_tflops_sustained")) else 1.0
+    kind = "sustained" if ratio != 1.0 else "burst"
     if bound == "tensor":
-        return pk["bf16_tflops"], "measured bf16 dense (cuBLAS burst)"
+        return pk["bf16_tflops"] * ratio, f"measured bf16 dense (cuBLAS {kind})"
     if bound == "tensor-tf32x3":
         if pk.get("tf32_tflops"):
-            return pk["tf32_tflops"] / 3.0, "measured TF32 dense (cuBLAS TF32 8192^3 burst, this run) / 3 passes"
-        return pk["bf16_tflops"] * (1.1 / 2.25) / 3.0, "measured bf16 x 1.1/2.25 (GB300 nominal dense TF32:BF16) / 3"
+            return (pk["tf32_tflops"] * ratio / 3.0,
+                    f"measured TF32 dense (cuBLAS TF32 8192^3, this run; {kind}) / 3 passes")
+        return (pk["bf16_tflops"] * ratio * (1.1 / 2.25) / 3.0,
+                f"measured bf16 {kind} x 1.1/2.25 (GB300 nominal dense TF32:BF16) / 3")
     if bound == "alu":
         return FFMA_PEAK_TFLOPS, "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz"
     return pk["hbm_gbs"], "measured HBM copy"
@@ -767,6 +775,9 @@ def run_ours(args, ws, rank, local):
     ms = max_over_ranks(statistics.mean(times), ws, dev)
 
     # ---- profiled pass: per-stage and per-kernel CUDA events over the same steps ----
+    # a timed region of a second or more keeps the tensor cores loaded long enough for the
+    # power cap to act: its kernels are measured against the sustained tensor peaks
+    long_region = sum(times) >= 1000.0
     stages, kernels, roof = {}, {}, None
     if not args.no_profile:
         lib.gptq_profile_enable(True)
@@ -790,7 +801,7 @@ def run_ours(args, ws, rank, local):
             if name in work and name in ROOF:
                 bound, unit = ROOF[name]
                 sec = t / args.steps / 1e3
-                peak, src = peak_for(bound, pk)
+                peak, src = peak_for(bound, pk, sustained=long_region)
                 ach = work[name] / sec / (1e12 if unit == "TFLOP/s" else 1e9)
                 kernels[name].update({"bound": bound, "achieved": ach, "peak": peak, "unit": unit,
                                       "frac": ach / peak, "peak_source": src})
@@ -804,6 +815,8 @@ def run_ours(args, ws, rank, local):
                     "avg_launch_ms": per_launch}
         if "hessian_tc_kernel" in kernels:
             stages["hessian_tc_frac_of_bf16_peak"] = kernels["hessian_tc_kernel"].get("frac")
+            k = kernels["hessian_tc_kernel"]
+            stages["hessian_tc_frac_of_bf16_burst_peak"] = k.get("achieved", 0.0) / pk["bf16_tflops"]
 
     # ---- e2e: pinned host inputs -> device -> same pass -> quantised artefacts back ----
     e2e = None

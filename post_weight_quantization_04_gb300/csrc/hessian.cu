@@ -11,7 +11,12 @@
 //     (one tcgen05.mma 128x256x16 per 16 tokens), listed once per accumulator.
 //   - Work units are (tile, token split); a persistent grid of one CTA per SM walks them
 //     split-major so concurrently running CTAs stream the same token range (X is re-read
-//     from L2, not HBM).
+//     from L2, not HBM). The tiles are listed in 2D blocks of kWaveRows x kWaveCols tiles,
+//     so the tiles of one wave of CTAs read only ~kWaveRows*128 + kWaveCols*256 channels
+//     of each token (on a 14336-wide input X is read from HBM ~1.6x less than with the
+//     tiles listed column by column; 1-2.5% faster). Splits short enough for a split's X
+//     slab to stay in L2 were measured slower: their extra atomic flushes into S cost more
+//     than the re-reads they save.
 //   - Warp roles: warp 0 issues TMA, warp 1 issues MMA (one thread), warps 2..9 drain the
 //     accumulator. TMEM holds two 128x256 fp32 accumulators (all 512 columns); every
 //     1024 tokens the MMA warp switches buffers and the epilogue warps add the finished
@@ -68,6 +73,8 @@ constexpr int TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;   // 48 KB
 constexpr int TC_SMEM = TC_STAGES * TC_STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr uint32_t TC_IDESC = idesc_bf16_f32_mn_mn(TC_BM, TC_BN);
 constexpr uint32_t TC_TMEM_COLS = 512;
+// the tile order's 2D blocks: about one wave of 152 CTAs (19 x 128 + 8 x 256 channels)
+constexpr int64_t kWaveRows = 19, kWaveCols = 8;
 
 struct TcParams {
     int64_t d;
@@ -391,6 +398,56 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__
     }
 }
 
+// The same on 64 x 64 tiles with 16-byte accesses (d % 4 == 0, 16-byte aligned S and H):
+// upper tiles are scaled copies; a lower or diagonal tile stages its mirror tile of S
+// (rows j, columns i: S's upper triangle) in shared memory and writes it transposed.
+__global__ void __launch_bounds__(256) finalize4_kernel(const float* __restrict__ S, int64_t d, float scale,
+                                                       float* __restrict__ H, float* __restrict__ diag,
+                                                       int* __restrict__ status) {
+    __shared__ float T[64][65];
+    const int ti = blockIdx.y, tj = blockIdx.x;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;   // 16 groups of four per row, 16 rows per pass
+    const int64_t i0 = (int64_t)ti * 64, j0 = (int64_t)tj * 64;
+    if (ti < tj) {
+        for (int r = ty; r < 64; r += 16) {
+            const int64_t gi = i0 + r, gj = j0 + 4 * tx;
+            if (gi >= d || gj >= d) continue;
+            const float4 v = *reinterpret_cast<const float4*>(S + gi * d + gj);
+            *reinterpret_cast<float4*>(H + gi * d + gj) = make_float4(scale * v.x, scale * v.y, scale * v.z, scale * v.w);
+        }
+        return;
+    }
+    // T[r][c] = S[j0 + r][i0 + c]
+    for (int r = ty; r < 64; r += 16) {
+        const int64_t gr = j0 + r, gc = i0 + 4 * tx;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (gr < d && gc < d) v = *reinterpret_cast<const float4*>(S + gr * d + gc);
+        T[r][4 * tx] = v.x;
+        T[r][4 * tx + 1] = v.y;
+        T[r][4 * tx + 2] = v.z;
+        T[r][4 * tx + 3] = v.w;
+    }
+    __syncthreads();
+    for (int r = ty; r < 64; r += 16) {
+        const int64_t gi = i0 + r, gj = j0 + 4 * tx;
+        if (gi >= d || gj >= d) continue;
+        float o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = 4 * tx + e;
+            // below the diagonal: S[gj + e][gi] = T[c][r]; on a diagonal tile at or above it:
+            // S[gi][gj + e] = T[r][c]
+            o[e] = (ti > tj || c < r) ? T[c][r] : T[r][c];
+            if (ti == tj && c == r) {
+                const float v = T[r][r];
+                if (diag) diag[gi] = v;
+                if (!isfinite(v)) set_status(status, GPTQ_ERR_NONFINITE);
+            }
+        }
+        *reinterpret_cast<float4*>(H + gi * d + gj) = make_float4(scale * o[0], scale * o[1], scale * o[2], scale * o[3]);
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -479,11 +536,16 @@ extern "C" int gptq_hessian_create(int64_t d, gptq_hessian** out) {
     h->n = 0;
     GPTQ_CUDA_TRY(cudaGetDevice(&h->device));
     h->sms = device_sm_count();
+    // the upper tiles in 2D blocks of kWaveRows x kWaveCols tiles (block rows of a block
+    // column first), so that consecutive units - the ones a wave of CTAs runs together -
+    // share their channel panels
     std::vector<int2> tiles;
     const int64_t nbi = ceil_div(d, TC_BM), nbj = ceil_div(d, TC_BN);
-    for (int64_t bj = 0; bj < nbj; ++bj)
-        for (int64_t bi = 0; bi < nbi; ++bi)
-            if (bj * TC_BN + TC_BN - 1 >= bi * TC_BM) tiles.push_back(make_int2((int)bi, (int)bj));
+    for (int64_t BJ = 0; BJ < nbj; BJ += kWaveCols)
+        for (int64_t BI = 0; BI < nbi; BI += kWaveRows)
+            for (int64_t bj = BJ; bj < std::min(nbj, BJ + kWaveCols); ++bj)
+                for (int64_t bi = BI; bi < std::min(nbi, BI + kWaveRows); ++bi)
+                    if (bj * TC_BN + TC_BN - 1 >= bi * TC_BM) tiles.push_back(make_int2((int)bi, (int)bj));
     h->ntiles = (int)tiles.size();
     cudaError_t e = cudaMalloc(&h->S, sizeof(float) * d * d);
     if (e == cudaSuccess) e = cudaMalloc(&h->status, sizeof(int));
@@ -536,9 +598,15 @@ extern "C" int gptq_hessian_finalize(gptq_hessian* h, float* H, float* diag_xtx,
     if (h->n <= 0) return GPTQ_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const float scale = (float)(2.0 / (double)h->n);
-    const unsigned nt = (unsigned)ceil_div(h->d, 32);
-    GPTQ_LAUNCH(K_FINALIZE, s, finalize_kernel<<<dim3(nt, nt), 256, 0, s>>>(h->S, h->d, scale, H, diag_xtx,
-                                                                                   h->status));
+    if (h->d % 4 == 0 && ((reinterpret_cast<uintptr_t>(H) | reinterpret_cast<uintptr_t>(h->S)) % 16 == 0)) {
+        const unsigned nt = (unsigned)ceil_div(h->d, 64);
+        GPTQ_LAUNCH(K_FINALIZE, s, finalize4_kernel<<<dim3(nt, nt), 256, 0, s>>>(h->S, h->d, scale, H, diag_xtx,
+                                                                                     h->status));
+    } else {
+        const unsigned nt = (unsigned)ceil_div(h->d, 32);
+        GPTQ_LAUNCH(K_FINALIZE, s, finalize_kernel<<<dim3(nt, nt), 256, 0, s>>>(h->S, h->d, scale, H, diag_xtx,
+                                                                                    h->status));
+    }
     GPTQ_LAUNCH_CHECK();
     if (n_tokens) *n_tokens = h->n;
     return finish_call(h->status, s);

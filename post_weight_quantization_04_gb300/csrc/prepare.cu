@@ -183,6 +183,47 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
     A[i * d + j] = v;
 }
 
+// The same without a permutation (perm = identity), four columns per thread with 16-byte
+// loads and stores (d % 4 == 0, 16-byte aligned H, A and rr): A[i][j..j+3] comes from the
+// group d-4-j .. d-1-j of H's row d-1-i, reversed; only entries on or above H's diagonal
+// are read (j + e < i), the diagonal is 1, and the group's entries past A's diagonal
+// (never read) are 0. GTH_ROWS rows per CTA.
+constexpr int GTH_ROWS = 4;
+__global__ void __launch_bounds__(256) prep_gather4_kernel(const float* __restrict__ H, int64_t d,
+                                                          const float* __restrict__ rr, float* __restrict__ A,
+                                                          int* __restrict__ status) {
+    for (int u = 0; u < GTH_ROWS; ++u) {
+        const int64_t i = (int64_t)blockIdx.x * GTH_ROWS + u;
+        if (i >= d) return;
+        const int64_t a = d - 1 - i;
+        const float ra = rr[a];
+        const float* src = H + a * d;
+        float4* dst = reinterpret_cast<float4*>(A + i * d);
+        bool bad = false;
+        for (int64_t g = threadIdx.x; 4 * g <= i; g += blockDim.x) {
+            const int64_t j = 4 * g, c = d - 4 - j;   // H columns c .. c+3 hold A columns j+3 .. j
+            float4 h = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (j + 3 <= i) {
+                h = *reinterpret_cast<const float4*>(src + c);
+            } else {
+                if (j + 2 < i) h.y = src[c + 1];
+                if (j + 1 < i) h.z = src[c + 2];
+                if (j < i) h.w = src[c + 3];
+            }
+            const float4 r4 = *reinterpret_cast<const float4*>(rr + c);
+            float4 o;
+            o.x = (j == i) ? 1.0f : h.w * ra * r4.w;
+            o.y = (j + 1 == i) ? 1.0f : (j + 1 < i ? h.z * ra * r4.z : 0.0f);
+            o.z = (j + 2 == i) ? 1.0f : (j + 2 < i ? h.y * ra * r4.y : 0.0f);
+            o.w = (j + 3 == i) ? 1.0f : (j + 3 < i ? h.x * ra * r4.x : 0.0f);
+            bad |= (j < i && !isfinite(h.w)) || (j + 1 < i && !isfinite(h.z)) || (j + 2 < i && !isfinite(h.y)) ||
+                   (j + 3 < i && !isfinite(h.x));
+            dst[g] = o;
+        }
+        if (bad) set_status(status, GPTQ_ERR_NONFINITE);
+    }
+}
+
 // Warp-level Cholesky + inverse of a (nb <= 32)-square block held in shared memory. Lane
 // r keeps row r of the block (row stride LDS_) in registers. Step k publishes column k of
 // the partly reduced block as row k of `lt` (32 x LT_LD floats, 16-byte aligned rows):
@@ -562,7 +603,55 @@ __global__ void eye_kernel(float* __restrict__ B, int64_t d) {
     if (idx < d * d) B[idx] = (idx / d == idx % d) ? 1.0f : 0.0f;
 }
 
-// U[i][j] = (i <= j) ? Linv[d-1-i][d-1-j] * rr[perm[j]] : 0
+// The identity with 16-byte stores (d % 4 == 0, B 16-byte aligned): grid-stride over the
+// d*d/4 groups of four, one row per block of d/4 groups.
+__global__ void __launch_bounds__(256) eye4_kernel(float* __restrict__ B, int64_t d) {
+    const int64_t q = d >> 2, total = d * q;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = g / q, c = (g - i * q) << 2;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (i >= c && i < c + 4) {
+            const int e = (int)(i - c);
+            v.x = e == 0 ? 1.0f : 0.0f;
+            v.y = e == 1 ? 1.0f : 0.0f;
+            v.z = e == 2 ? 1.0f : 0.0f;
+            v.w = e == 3 ? 1.0f : 0.0f;
+        }
+        reinterpret_cast<float4*>(B)[g] = v;
+    }
+}
+
+// U[i][j] = (i <= j) ? Linv[d-1-i][d-1-j] * rr[perm[j]] : 0, four columns per thread with
+// 16-byte loads and stores (d % 4 == 0, 16-byte aligned bases): the four columns j..j+3 of
+// U's row i are the 16-byte group d-4-j .. d-1-j of Linv's row d-1-i, reversed. SCR_ROWS
+// rows per CTA; the groups left of the diagonal are zeros and read nothing.
+constexpr int SCR_ROWS = 4;
+__global__ void __launch_bounds__(256) prep_scatter4_kernel(const float* __restrict__ Binv, int64_t d,
+                                                           const int32_t* __restrict__ perm,
+                                                           const float* __restrict__ rr, float* __restrict__ U) {
+    const int64_t q = d >> 2;
+    for (int u = 0; u < SCR_ROWS; ++u) {
+        const int64_t i = (int64_t)blockIdx.x * SCR_ROWS + u;
+        if (i >= d) return;
+        const float* src = Binv + (d - 1 - i) * d;
+        float4* dst = reinterpret_cast<float4*>(U + i * d);
+        for (int64_t g = threadIdx.x; g < q; g += blockDim.x) {
+            const int64_t j = g << 2;
+            float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (j + 3 >= i) {
+                const float4 b = *reinterpret_cast<const float4*>(src + (d - 4 - j));
+                const int4 p = *reinterpret_cast<const int4*>(perm + j);
+                o.x = (j + 0 >= i) ? b.w * rr[p.x] : 0.0f;
+                o.y = (j + 1 >= i) ? b.z * rr[p.y] : 0.0f;
+                o.z = (j + 2 >= i) ? b.y * rr[p.z] : 0.0f;
+                o.w = (j + 3 >= i) ? b.x * rr[p.w] : 0.0f;
+            }
+            dst[g] = o;
+        }
+    }
+}
+
+// U[i][j] = (i <= j) ? Linv[d-1-i][d-1-j] * rr[perm[j]] : 0 (any d)
 __global__ void __launch_bounds__(256) prep_scatter_kernel(const float* __restrict__ Binv, int64_t d,
                                                           const int32_t* __restrict__ perm,
                                                           const float* __restrict__ rr, float* __restrict__ U) {
@@ -640,7 +729,11 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
     else
         GPTQ_LAUNCH(K_PREP_PERM, s, iota_kernel<<<g1, 256, 0, s>>>(perm, d));
     GPTQ_LAUNCH_CHECK();
-    {
+    if (!act_order && d % 4 == 0 && ((reinterpret_cast<uintptr_t>(H) | reinterpret_cast<uintptr_t>(w.A)) % 16 == 0)) {
+        GPTQ_LAUNCH(K_PREP_GATHER, s, prep_gather4_kernel<<<(unsigned)ceil_div(d, GTH_ROWS), 256, 0, s>>>(
+                                          H, d, w.rr, w.A, w.status));
+        GPTQ_LAUNCH_CHECK();
+    } else {
         dim3 grid((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 8));
         GPTQ_LAUNCH(K_PREP_GATHER, s, prep_gather_kernel<<<grid, 256, 0, s>>>(H, d, perm, w.rr, w.A, w.status));
         GPTQ_LAUNCH_CHECK();
@@ -655,9 +748,21 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
     const bool tc = (d % 4 == 0) && tc_gemm_nt_ok(w.A, d);
 
     const int64_t nblk = ceil_div(d, NB);
-    if (!tc || !conc) {
-        GPTQ_LAUNCH(K_EYE, s, eye_kernel<<<(unsigned)ceil_div(d * d, 256), 256, 0, s>>>(w.Binv, d));
+    const bool vec4 = (d % 4 == 0) && ((reinterpret_cast<uintptr_t>(w.Binv) | reinterpret_cast<uintptr_t>(U) |
+                                        reinterpret_cast<uintptr_t>(perm)) % 16 == 0);
+    auto launch_eye = [&](cudaStream_t st) -> int {
+        if (vec4) {
+            const unsigned g = (unsigned)std::min<int64_t>(ceil_div(d * d / 4, 256), (int64_t)device_sm_count() * 8);
+            GPTQ_LAUNCH(K_EYE, st, eye4_kernel<<<g, 256, 0, st>>>(w.Binv, d));
+        } else {
+            GPTQ_LAUNCH(K_EYE, st, eye_kernel<<<(unsigned)ceil_div(d * d, 256), 256, 0, st>>>(w.Binv, d));
+        }
         GPTQ_LAUNCH_CHECK();
+        return GPTQ_OK;
+    };
+    if (!tc || !conc) {
+        const int rc = launch_eye(s);
+        if (rc != GPTQ_OK) return rc;
     }
     if (tc) {
         // Blocked right-looking Cholesky of A (lower) with the block-row inverse step of
@@ -682,8 +787,8 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
             GPTQ_CUDA_TRY(wait(cs, conc->fork));
             GPTQ_CUDA_TRY(wait(ss, conc->fork));
             // B = I (the right-hand side of L X = I) is first read by the side stream
-            GPTQ_LAUNCH(K_EYE, ss, eye_kernel<<<(unsigned)ceil_div(d * d, 256), 256, 0, ss>>>(w.Binv, d));
-            GPTQ_LAUNCH_CHECK();
+            const int rc = launch_eye(ss);
+            if (rc != GPTQ_OK) return rc;
         }
         // the SMs are split between the streams: persistent CTAs of one stream would
         // otherwise hold SMs that the other's next kernel waits for
@@ -884,7 +989,11 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
         }
     }
 
-    {
+    if (vec4) {
+        GPTQ_LAUNCH(K_SCATTER, s, prep_scatter4_kernel<<<(unsigned)ceil_div(d, SCR_ROWS), 256, 0, s>>>(w.Binv, d, perm,
+                                                                                                       w.rr, U));
+        GPTQ_LAUNCH_CHECK();
+    } else {
         dim3 grid((unsigned)std::min<int64_t>(ceil_div(d, 256), 64), (unsigned)d);
         GPTQ_LAUNCH(K_SCATTER, s, prep_scatter_kernel<<<grid, 256, 0, s>>>(w.Binv, d, perm, w.rr, U));
         GPTQ_LAUNCH_CHECK();

@@ -748,7 +748,9 @@ int column_loop(const float* W, int64_t rows, int64_t cols, const float* U, cons
     }
     // tensor-core trailing update when every row of W and U is 16-byte aligned
     const bool tc = (cols % 4 == 0) && tc_gemm_nt_ok(w.W, cols);
-    if (tc) GPTQ_CUDA_TRY(split_cols(K_SPLIT, U, cols, (int)cols, (int)cols, w.uhi, w.ulo, (int)cols, s));
+    // U^T's split: the trailing updates read it strictly below the diagonal only (rows past
+    // the block, the block's columns), so the tiles with nothing there are skipped
+    if (tc) GPTQ_CUDA_TRY(split_cols(K_SPLIT, U, cols, (int)cols, (int)cols, w.uhi, w.ulo, (int)cols, s, false, true));
     const unsigned pgrid = (unsigned)ceil_div(rows, 8);
     if (!prune && q.group == 0) {
         GPTQ_LAUNCH(K_ROW_PARAMS, s, row_params_kernel<<<pgrid, 256, 0, s>>>(w.W, rows, cols, 0, cols, q.bits, q.sym, q.zero_in_range,

@@ -605,11 +605,13 @@ __global__ void __launch_bounds__(256) split_cols_kernel(const float* __restrict
 // aligned bases): a 64 x 64 tile per CTA, read as rows of B, written as rows of hi/lo.
 constexpr int SC_T = 64;
 __global__ void __launch_bounds__(256) split_cols4_kernel(const float* __restrict__ B, int64_t ld, int K, int N,
-                                                         float* __restrict__ hi, float* __restrict__ lo, int ldk) {
+                                                         float* __restrict__ hi, float* __restrict__ lo, int ldk,
+                                                         int strict_lower) {
     __shared__ float tile[SC_T][SC_T + 1];
     pdl_wait();
     pdl_trigger();
     const int k0 = blockIdx.y * SC_T, n0 = blockIdx.x * SC_T;
+    if (strict_lower && n0 + SC_T <= k0) return;   // every output n < k: never read
     const int c4 = (threadIdx.x & 15) * 4, r = threadIdx.x >> 4;   // 16 float4 per row, 16 rows per pass
 #pragma unroll
     for (int rr = 0; rr < SC_T; rr += 16) {
@@ -700,7 +702,7 @@ cudaError_t split_rows(int id, const float* A, int64_t lda, int rows, int K, flo
 }
 
 cudaError_t split_cols(int id, const float* B, int64_t ld, int K, int N, float* hi, float* lo, int ldk,
-                       cudaStream_t s, bool pdl) {
+                       cudaStream_t s, bool pdl, bool strict_lower) {
     if (K <= 0 || N <= 0) return cudaSuccess;
     cudaError_t e = cudaSuccess;
     const bool vec = (N % 4 == 0) && (ld % 4 == 0) && (ldk % 4 == 0) &&
@@ -709,9 +711,10 @@ cudaError_t split_cols(int id, const float* B, int64_t ld, int K, int N, float* 
     if (vec) {
         dim3 grid((unsigned)((N + SC_T - 1) / SC_T), (unsigned)((K + SC_T - 1) / SC_T));
         if (pdl)
-            GPTQ_LAUNCH(id, s, e = launch_pdl(split_cols4_kernel, grid, dim3(256), 0, s, B, ld, K, N, hi, lo, ldk));
+            GPTQ_LAUNCH(id, s, e = launch_pdl(split_cols4_kernel, grid, dim3(256), 0, s, B, ld, K, N, hi, lo, ldk,
+                                              (int)strict_lower));
         else
-            GPTQ_LAUNCH(id, s, split_cols4_kernel<<<grid, 256, 0, s>>>(B, ld, K, N, hi, lo, ldk));
+            GPTQ_LAUNCH(id, s, split_cols4_kernel<<<grid, 256, 0, s>>>(B, ld, K, N, hi, lo, ldk, (int)strict_lower));
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }

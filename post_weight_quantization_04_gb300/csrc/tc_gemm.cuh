@@ -20,9 +20,11 @@ cudaError_t split_rows(int id, const float* A, int64_t lda, int rows, int K, flo
                        cudaStream_t s, bool pdl = false);
 
 // The same for the transpose of a (K x N, row stride ld) block: hi/lo are (N x ldk) with
-// hi[n][k] = split(B[k][n]).
+// hi[n][k] = split(B[k][n]). strict_lower: only the entries n > k are needed (the reader
+// takes hi/lo strictly below the diagonal only), so 64 x 64 tiles with every n < k are
+// skipped and left unwritten.
 cudaError_t split_cols(int id, const float* B, int64_t ld, int K, int N, float* hi, float* lo, int ldk,
-                       cudaStream_t s, bool pdl = false);
+                       cudaStream_t s, bool pdl = false, bool strict_lower = false);
 
 // C[M x N] (ldc) = beta * C + alpha * (A * B^T) with A given as (Ahi, Alo) M x K and B as
 // (Bhi, Blo) N x K, both K-major with row stride ldk (ldk % 4 == 0, 16-byte aligned).
