@@ -95,9 +95,11 @@ def _declare(lib: ctypes.CDLL) -> None:
 
 
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libgptq.so (built in-tree by ``build.py``); raises if it is missing."""
+    """Load libgptq.so (built in-tree by ``build.py``; the environment variable GPTQ_LIB names
+    another build of the same library instead); raises if it is missing."""
     global _lib
     if _lib is None:
+        path = os.environ.get("GPTQ_LIB", path)
         if not os.path.exists(path):
             raise RuntimeError(f"libgptq.so not built ({path}); run post_weight_quantization_04_gb300.build")
         lib = ctypes.CDLL(path)

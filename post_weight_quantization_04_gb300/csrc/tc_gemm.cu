@@ -41,29 +41,43 @@ namespace {
 // Output tiles are 128 rows x BN columns, BN = 128, or 64 for launches too small to fill
 // their SMs with 128-wide tiles (twice the CTAs, each with half the MMAs and epilogue).
 constexpr int G_BM = 128, G_BK = 32, G_THREADS = 192;
-constexpr int G_BOX = G_BM * G_BK * 4;         // 16 KB: one 128 x 32 fp32 box (A, and a C chunk)
-template <int BN, bool DEEP = false>
+// K step of the 128 x 256 variant's operand ring (16: four 48 KB stages; 32: two 96 KB)
+#ifndef GPTQ_GEMM_WIDE_KB
+#define GPTQ_GEMM_WIDE_KB 16
+#endif
+constexpr int kWideKB = GPTQ_GEMM_WIDE_KB;
+constexpr int G_BOX = G_BM * G_BK * 4;         // 16 KB: one 128 x 32 fp32 box (a C chunk)
+// KB: the K step of the operand ring in fp32 columns. 32 (128-byte rows, 128-byte swizzle);
+// or 16 (64-byte rows, 64-byte swizzle), which halves a stage so twice as many stages fit
+// in the same shared memory and a stage's load has more K steps of MMAs to hide behind.
+template <int BN, bool DEEP = false, int KB = G_BK>
 struct GTile {
-    static constexpr int BBOX = BN * G_BK * 4;                      // one BN x 32 fp32 box of B
-    static constexpr int STAGE = 2 * G_BOX + 2 * BBOX;              // Ahi, Alo, Bhi, Blo
-    // ring depth: 3 for the deep variant (large launches with long K: a stage arrives
-    // ~1.1-1.2k cycles after its TMA issue under full load, more than one K step of MMAs),
-    // whose C tile then streams through two rotating 32-column chunk buffers; else 2
-    static constexpr int STAGES = (DEEP && BN == 128) ? 3 : 2;
+    static constexpr int ABOX = G_BM * KB * 4;                      // one 128 x KB fp32 box of A
+    static constexpr int BBOX = BN * KB * 4;                        // one BN x KB fp32 box of B
+    static constexpr int STAGE = 2 * ABOX + 2 * BBOX;               // Ahi, Alo, Bhi, Blo
+    // ring depth: 3 for the deep 128-wide variant (large launches with long K: a stage
+    // arrives ~1.1-1.2k cycles after its TMA issue under full load, more than one K step of
+    // MMAs), whose C tile then streams through two rotating 32-column chunk buffers; 4 for
+    // the deep 256-wide variant with 16-wide K steps; else 2
+    static constexpr int STAGES = (DEEP && BN == 128 && KB == 32) ? 3 : (DEEP && KB == 16) ? 4 : 2;
     static constexpr int CB = DEEP ? 2 : BN / 32;                   // C chunk buffers
     static constexpr int NCH = BN / 32;                             // 32-column C chunks
     static constexpr int CBUF = CB * G_BOX;                         // C chunk buffers
     static constexpr int SMEM = STAGES * STAGE + CBUF + 1024 + 256;
     static constexpr uint32_t TMEM_COLS = 2 * BN;                   // two accumulators
+    // operand layout: 8-row core-matrix groups KB * 4 * 8 bytes apart; swizzle mode of the
+    // shared-memory descriptor (2 = 128-byte, 4 = 64-byte)
+    static constexpr uint32_t SBO = KB * 4 * 8;
+    static constexpr uint64_t SWZ = KB == 32 ? 2 : 4;
     // kind::tf32: D fp32 (bits 4-5 = 1), A/B TF32 (2), both K-major, N >> 3, M >> 4
     static constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
                                       ((uint32_t)(G_BM >> 4) << 24);
 };
 
 static_assert(GTile<64>::SMEM <= 232448 && GTile<128>::SMEM <= 232448 && GTile<128, true>::SMEM <= 232448 &&
-                  GTile<256, true>::SMEM <= 232448,
+                  GTile<256, true>::SMEM <= 232448 && GTile<256, true, 16>::SMEM <= 232448,
               "shared memory per CTA");
-static_assert(2 * GTile<128, true>::STAGES + 12 < 30, "barrier slots");
+static_assert(2 * GTile<256, true, 16>::STAGES + 12 < 30, "barrier slots");
 
 struct GParams {
     int M, N, K;
@@ -155,7 +169,7 @@ __device__ __forceinline__ void tile_of(const GParams& p, int t, int& tm, int& t
 // The C tile moves through shared memory by TMA in both directions: the producer loads it
 // (when beta != 0) while the MMAs of the tile run, the epilogue combines it with the
 // accumulator in place and stores it back with TMA, so no thread waits on a global load.
-template <int BN, bool DEEP>
+template <int BN, bool DEEP, int KB = G_BK>
 __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_constant__ CUtensorMap tAh,
                                                                   const __grid_constant__ CUtensorMap tAl,
                                                                   const __grid_constant__ CUtensorMap tBh,
@@ -164,7 +178,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                                                                   const GParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    using T = GTile<BN, DEEP>;
+    using T = GTile<BN, DEEP, KB>;
     constexpr int G_STAGES = T::STAGES;
     uint8_t* cbuf = smem + G_STAGES * T::STAGE;
     uint64_t* bars = reinterpret_cast<uint64_t*>(cbuf + T::CBUF);
@@ -217,7 +231,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int ktiles = (p.K + G_BK - 1) / G_BK;
+    const int ktiles = (p.K + KB - 1) / KB;
     pdl_wait();      // operands and C may be the previous kernel's output
     pdl_trigger();
 
@@ -237,11 +251,11 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                     }
                     mbar_expect_tx(full_bar(stage), T::STAGE);
                     const uint32_t sa = sbase + stage * T::STAGE;
-                    const int x = kt * G_BK;
+                    const int x = kt * KB;
                     tma_load_2d(sa, &tAh, full_bar(stage), x, tm * G_BM);
-                    tma_load_2d(sa + G_BOX, &tAl, full_bar(stage), x, tm * G_BM);
-                    tma_load_2d(sa + 2 * G_BOX, &tBh, full_bar(stage), x, tn * BN);
-                    tma_load_2d(sa + 2 * G_BOX + T::BBOX, &tBl, full_bar(stage), x, tn * BN);
+                    tma_load_2d(sa + T::ABOX, &tAl, full_bar(stage), x, tm * G_BM);
+                    tma_load_2d(sa + 2 * T::ABOX, &tBh, full_bar(stage), x, tn * BN);
+                    tma_load_2d(sa + 2 * T::ABOX + T::BBOX, &tBl, full_bar(stage), x, tn * BN);
                     issued |= 1u << stage;
                     issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == G_STAGES) {
@@ -290,13 +304,13 @@ __global__ void __launch_bounds__(G_THREADS, 1) tc_gemm_nt_kernel(const __grid_c
                     tc_fence_after();
                     const uint32_t sa = sbase + stage * T::STAGE;
 #pragma unroll
-                    for (int kk = 0; kk < G_BK / 8; ++kk) {
-                        // 8 TF32 = 32 bytes along K inside the 128-byte swizzle row
+                    for (int kk = 0; kk < KB / 8; ++kk) {
+                        // 8 TF32 = 32 bytes along K inside the swizzled row
                         const uint32_t off = kk * 32;
-                        const uint64_t ah = smem_desc(sa + off, 16, 1024, kSwizzle128B);
-                        const uint64_t al = smem_desc(sa + G_BOX + off, 16, 1024, kSwizzle128B);
-                        const uint64_t bh = smem_desc(sa + 2 * G_BOX + off, 16, 1024, kSwizzle128B);
-                        const uint64_t bl = smem_desc(sa + 2 * G_BOX + T::BBOX + off, 16, 1024, kSwizzle128B);
+                        const uint64_t ah = smem_desc(sa + off, 16, T::SBO, T::SWZ);
+                        const uint64_t al = smem_desc(sa + T::ABOX + off, 16, T::SBO, T::SWZ);
+                        const uint64_t bh = smem_desc(sa + 2 * T::ABOX + off, 16, T::SBO, T::SWZ);
+                        const uint64_t bl = smem_desc(sa + 2 * T::ABOX + T::BBOX + off, 16, T::SBO, T::SWZ);
                         umma_tf32(dt, ah, bh, T::IDESC, (kt > 0 || kk > 0) ? 1u : 0u);
                         umma_tf32(dt, ah, bl, T::IDESC, 1u);
                         umma_tf32(dt, al, bh, T::IDESC, 1u);
@@ -650,16 +664,17 @@ __global__ void __launch_bounds__(256) split_cols4_kernel(const float* __restric
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() { return tma_encoder(); }
 
-bool make_map(CUtensorMap* m, const float* base, int rows, int K, int64_t ldk, int box_rows = G_BM) {
+// box of box_rows rows x kb fp32 columns: kb = 32 (128-byte swizzle) or 16 (64-byte swizzle)
+bool make_map(CUtensorMap* m, const float* base, int rows, int K, int64_t ldk, int box_rows = G_BM, int kb = G_BK) {
     auto enc = encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ldk * 4};
-    cuuint32_t box[2] = {(cuuint32_t)G_BK, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)kb, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, kb == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -760,9 +775,10 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
     const bool deep = bn == 128 && nt128 >= 2 * cap && K >= 8 * G_BK;
     const bool wide = deep && N >= 1024 && nt256 >= cap;
     const int tw = wide ? 256 : bn;   // the launch's tile width
+    const int kb = wide ? kWideKB : G_BK;   // the operand ring's K step
     CUtensorMap tah, tal, tbh, tbl, tcm;
-    if (!make_map(&tah, Ahi, M, K, ldk) || !make_map(&tal, Alo, M, K, ldk) ||
-        !make_map(&tbh, Bhi, N, K, out.ldb, tw) || !make_map(&tbl, Blo, N, K, out.ldb, tw) ||
+    if (!make_map(&tah, Ahi, M, K, ldk, G_BM, kb) || !make_map(&tal, Alo, M, K, ldk, G_BM, kb) ||
+        !make_map(&tbh, Bhi, N, K, out.ldb, tw, kb) || !make_map(&tbl, Blo, N, K, out.ldb, tw, kb) ||
         !make_map(&tcm, C, M, N, ldc))
         return cudaErrorInvalidValue;
     GParams p;
@@ -787,11 +803,11 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
     if (p.ntiles == 0) return cudaSuccess;
     const int grid = std::min(p.ntiles, cap);
     auto kern = bn == 64 ? tc_gemm_nt_kernel<64, false>
-              : wide    ? tc_gemm_nt_kernel<256, true>
+              : wide    ? (kWideKB == 16 ? tc_gemm_nt_kernel<256, true, 16> : tc_gemm_nt_kernel<256, true, 32>)
               : deep    ? tc_gemm_nt_kernel<128, true>
                         : tc_gemm_nt_kernel<128, false>;
     const int smem = bn == 64 ? GTile<64>::SMEM
-                   : wide    ? GTile<256, true>::SMEM
+                   : wide    ? (kWideKB == 16 ? GTile<256, true, 16>::SMEM : GTile<256, true, 32>::SMEM)
                    : deep    ? GTile<128, true>::SMEM
                              : GTile<128>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
