@@ -56,6 +56,10 @@ def parse(argv=None):
     # fewer calibration tokens per layer input, or one bit width of the decoder block's sweep
     ap.add_argument("--x-tokens", type=int, default=0, help="calibration tokens per input (default: the workload's)")
     ap.add_argument("--bits", type=int, default=0, help="keep only the layers of this bit width")
+    # the timed step's schedule: serial (group after group), prepare (all Hessians, then the
+    # groups' gptq_prepare calls side by side, then the quantizations), groups (all
+    # Hessians, then each group's prepare and quantizations on its own stream)
+    ap.add_argument("--schedule", choices=["serial", "prepare", "groups"], default="groups")
     return ap.parse_args(argv)
 
 
@@ -221,13 +225,8 @@ class Runner:
             d = L.X.shape[1]
             if d not in self.hess:
                 self.hess[d] = lib.Hessian(d, device)
-                self.prep_ws[d] = torch.empty(lib.gptq_prepare_workspace_bytes(d, True), dtype=torch.uint8,
-                                              device=device)
             q = L.spec.q
             r, c = L.Wcat.shape
-            nb = lib.gptq_quantize_workspace_bytes(r, c, q.bits, q.group, q.sym)
-            if (r, c) not in self.q_ws or self.q_ws[(r, c)].numel() < nb:
-                self.q_ws[(r, c)] = torch.empty(nb, dtype=torch.uint8, device=device)
             G = -(-c // q.group) if q.group else 1
             self.outs.append({
                 "codes": torch.empty(r, c, dtype=torch.int8, device=device),
@@ -239,6 +238,82 @@ class Runner:
                                       device=device),
                 "row_loss": torch.empty(r, dtype=torch.float32, device=device),
             })
+
+        # one prepare workspace and one quantize workspace per group (the concurrent schedule
+        # runs groups side by side; a group's calls share them in turn), and one stream per
+        # group for it
+        for g in self.groups:
+            d = layers[g[0]].X.shape[1]
+            self.prep_ws[id(g)] = torch.empty(lib.gptq_prepare_workspace_bytes(d, True), dtype=torch.uint8,
+                                              device=device)
+            nb = 0
+            for li in g:
+                q = layers[li].spec.q
+                r, c = layers[li].Wcat.shape
+                nb = max(nb, lib.gptq_quantize_workspace_bytes(r, c, q.bits, q.group, q.sym))
+            self.q_ws[id(g)] = torch.empty(nb, dtype=torch.uint8, device=device)
+        self.gstreams = [torch.cuda.Stream(device=device) for _ in self.groups]
+
+    def step_concurrent(self, quantize_in_group: bool = True, Xs=None, Wcats=None, x_chunks=None, w_ready=None,
+                        layer_done=None, order=None):
+        """One pass with the groups side by side: every group's Hessian on the current stream
+        (each is a full-GPU kernel), then per group on its own stream, as soon as that group's
+        Hessian is final (an event, not the whole Hessian queue), its gptq_prepare - the
+        small groups' latency-bound factorisations overlap the large group's - followed, with
+        quantize_in_group, by its gptq_quantize calls (else those run after all prepares, on
+        the current stream). The same calls and results as step(); Xs, Wcats, x_chunks,
+        w_ready, layer_done and order as there."""
+        import torch
+        lib = self.lib
+        main = torch.cuda.current_stream()
+        order = list(order) if order is not None else list(range(len(self.groups)))
+        Hs = {}
+        for gi in order:
+            g = self.groups[gi]
+            X = self.layers[g[0]].X if Xs is None else Xs[g[0]]
+            h = self.hess[X.shape[1]]
+            h.reset()
+            if x_chunks is None:
+                h.accumulate(X)
+            else:
+                for rows, ev, _ in x_chunks[gi]:
+                    main.wait_event(ev)
+                    h.accumulate(rows)
+            Hs[gi] = h.finalize()[:2]
+            ev = torch.cuda.Event()
+            ev.record(main)
+            Hs[gi] = (Hs[gi], ev)
+        preps = {}
+        for gi in order:
+            g = self.groups[gi]
+            st = self.gstreams[gi]
+            (H, diag), ev = Hs[gi]
+            st.wait_event(ev)
+            with torch.cuda.stream(st):
+                q0 = self.layers[g[0]].spec.q
+                U, perm, dead = lib.gptq_prepare(H, diag, q0.damp, act_order=q0.act_order, ws=self.prep_ws[id(g)])
+                preps[gi] = (U, perm, dead)
+                if quantize_in_group:
+                    self._quantize_group(g, U, perm, dead, Wcats, w_ready, layer_done)
+        for st in self.gstreams:
+            main.wait_stream(st)
+        if not quantize_in_group:
+            for gi in order:
+                self._quantize_group(self.groups[gi], *preps[gi], Wcats, w_ready, layer_done)
+        return self.outs
+
+    def _quantize_group(self, g, U, perm, dead, Wcats=None, w_ready=None, layer_done=None):
+        import torch
+        for li in g:
+            L = self.layers[li]
+            Wcat = L.Wcat if Wcats is None else Wcats[li]
+            q = L.spec.q
+            if w_ready is not None:
+                torch.cuda.current_stream().wait_event(w_ready[li])
+            self.lib.gptq_quantize(Wcat, U, perm, dead, q.bits, q.group, q.sym, ws=self.q_ws[id(g)],
+                                   out=self.outs[li])
+            if layer_done is not None:
+                layer_done[li].record()
 
     def weight_outputs(self, li):
         """The outputs of layer li split per weight (row blocks of the stacked outputs)."""
@@ -278,7 +353,7 @@ class Runner:
             H, diag, _ = h.finalize()
             if e:
                 e[1].record()
-            U, perm, dead = lib.gptq_prepare(H, diag, q0.damp, act_order=q0.act_order, ws=self.prep_ws[X.shape[1]])
+            U, perm, dead = lib.gptq_prepare(H, diag, q0.damp, act_order=q0.act_order, ws=self.prep_ws[id(g)])
             if e:
                 e[2].record()
             for li in g:
@@ -287,7 +362,7 @@ class Runner:
                 q = L.spec.q
                 if w_ready is not None:
                     torch.cuda.current_stream().wait_event(w_ready[li])
-                lib.gptq_quantize(Wcat, U, perm, dead, q.bits, q.group, q.sym, ws=self.q_ws[tuple(Wcat.shape)],
+                lib.gptq_quantize(Wcat, U, perm, dead, q.bits, q.group, q.sym, ws=self.q_ws[id(g)],
                                   out=self.outs[li])
                 if layer_done is not None:
                     layer_done[li].record()
@@ -358,15 +433,18 @@ ROOF = {
     "init_work_kernel": ("hbm", "GB/s"),
 }
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures
-# (summaries under profiles/): one --set full launch per kernel class, or, for a class
-# launched with many shapes per step, the average over one whole step's launches; a
-# kernel changed since its capture has no entry here.
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the current kernels
+# from the ncu captures summarised under profiles/ (hessian_tc_kernel_d4096_x262144.md,
+# hessian_tc_kernel_d14336_x16384.md); a kernel changed since its capture has no entry here.
+# The d = 14336 launch of the decoder block is estimated from its 16384-token capture: its
+# reads (X re-streamed by each wave of tiles) scale with the tokens (x16), its writes (the
+# accumulator flushes into S, one per tile) do not. Per launch, as `achieved` is.
+_H4096 = 4.635595e9 + 160.0128e6
+_H14336 = 4.726530e9 * 16 + 409.165056e6
 TRAFFIC = {
-    (1, "tc_gemm_nt_kernel[prepare]"): 768972.8,
-    (1, "tc_gemm_nt_kernel[trailing]"): 10273228.8,
-    (2, "hessian_tc_kernel"): 4.827069e9 + 159.446272e6,
-    (2, "pack_kernel"): 16.788224e6,
+    (2, "hessian_tc_kernel"): _H4096,
+    (3, "hessian_tc_kernel"): _H14336,
+    (4, "hessian_tc_kernel"): (3 * _H4096 + _H14336) / 4,
 }
 
 
@@ -731,10 +809,15 @@ def run_ours(args, ws, rank, local):
 
     # clocks are sampled every 200 ms from before the warm-up to the end of the timed
     # region (at the small workloads the timed region itself is a few milliseconds)
+    def run_step():
+        if args.schedule == "serial":
+            return runner.step()
+        return runner.step_concurrent(quantize_in_group=(args.schedule == "groups"))
+
     clocks = Clocks(local)
     clocks.start()
     for _ in range(args.warmup):
-        runner.step()
+        run_step()
     lib.status_sync()
     torch.cuda.synchronize()
 
@@ -747,13 +830,13 @@ def run_ours(args, ws, rank, local):
             gs = torch.cuda.Stream()
             gs.wait_stream(torch.cuda.current_stream())
             with torch.cuda.stream(gs):
-                runner.step()
+                run_step()
                 lib.status_sync(gs)
             torch.cuda.current_stream().wait_stream(gs)
             graph = torch.cuda.CUDAGraph()
             c0 = lib.gptq_launch_count()
             with torch.cuda.graph(graph, stream=gs):
-                runner.step()
+                run_step()
             graph_launches = lib.gptq_launch_count() - c0
             graph.replay()
             lib.status_sync()
@@ -776,7 +859,7 @@ def run_ours(args, ws, rank, local):
         if graph is not None:
             graph.replay()
         else:
-            runner.step()
+            run_step()
         b.record()
         lib.status_sync()   # synchronises the stream: the step's errors, after its end event
         times.append(a.elapsed_time(b))
@@ -897,8 +980,9 @@ def run_ours(args, ws, rank, local):
                     for li in g:
                         dW[li].copy_(hW[li], non_blocking=True)
                         w_ready[li].record()
-            outs = runner.step(Xs=dX, Wcats=dW, x_chunks=x_chunks, w_ready=w_ready, layer_done=layer_done,
-                               order=gorder)
+            kw = dict(Xs=dX, Wcats=dW, x_chunks=x_chunks, w_ready=w_ready, layer_done=layer_done, order=gorder)
+            outs = (runner.step(**kw) if args.schedule == "serial"
+                    else runner.step_concurrent(quantize_in_group=(args.schedule == "groups"), **kw))
             with torch.cuda.stream(d2h):
                 for gi in gorder:
                     for li in runner.groups[gi]:
@@ -918,7 +1002,19 @@ def run_ours(args, ws, rank, local):
             t0 = time.perf_counter()
             e2e_step()
             et.append((time.perf_counter() - t0) * 1e3)
+        # the step's host-to-device copies alone (the floor the host link sets on e2e)
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(h2d):
+            c0.record()
+            for hx, dx in xs.values():
+                dx.copy_(hx, non_blocking=True)
+            for li in range(len(layers)):
+                dW[li].copy_(hW[li], non_blocking=True)
+            c1.record()
+        torch.cuda.synchronize()
         e2e = {"value": statistics.mean(et), "unit": "ms", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+               "h2d_alone_ms": c0.elapsed_time(c1),
                "copies": "pinned host buffers; the inputs go in on a copy stream in token chunks (one per 256 MB, at "
                          "most 8), largest input first, each chunk accumulated into its Hessian once landed; weights "
                          "follow their group's input; each layer's stored form goes back on another stream once the "
@@ -942,6 +1038,11 @@ def run_ours(args, ws, rank, local):
             "data": "synthetic", "config": bench_config(args.config, wl, ws),
             "step": ("one CUDA graph of the step's library calls, replayed" if graph is not None
                      else graph_note or "the library calls issued eagerly"),
+            "schedule": {"serial": "group after group",
+                         "prepare": "all Hessians, then every group's gptq_prepare side by side on its own stream, "
+                                    "then the quantizations",
+                         "groups": "all Hessians, then per group on its own stream its gptq_prepare and its "
+                                   "gptq_quantize calls, the groups side by side"}[args.schedule],
             "clocks": ck, "gpu_launches": launches // max(1, args.steps) * args.steps,
             "gpu_launches_per_step": launches / max(1, args.steps), "wall_ms_timed_region": wall,
             "stages_ms": stages, "kernels": kernels, "roofline": roof, "e2e": e2e, "cpu_baseline": cpu,
@@ -959,6 +1060,7 @@ def time_stated_layer_gpu(lib, runner, layers, stated, dev, reps: int = 5) -> fl
     li, wi = stated
     L = layers[li]
     W = L.Ws[wi]
+    grp = next(g for g in runner.groups if li in g)
     q = L.spec.q
     h = runner.hess[L.X.shape[1]]
     ws_q = torch.empty(lib.gptq_quantize_workspace_bytes(W.shape[0], W.shape[1], q.bits, q.group, q.sym),
@@ -968,7 +1070,7 @@ def time_stated_layer_gpu(lib, runner, layers, stated, dev, reps: int = 5) -> fl
         h.reset()
         h.accumulate(L.X)
         H, diag, _ = h.finalize()
-        U, perm, dead = lib.gptq_prepare(H, diag, q.damp, act_order=q.act_order, ws=runner.prep_ws[L.X.shape[1]])
+        U, perm, dead = lib.gptq_prepare(H, diag, q.damp, act_order=q.act_order, ws=runner.prep_ws[id(grp)])
         lib.gptq_quantize(W, U, perm, dead, q.bits, q.group, q.sym, ws=ws_q)
 
     one()

@@ -119,6 +119,9 @@ int gptq_hessian_destroy(gptq_hessian* h);
  * Synchronises `stream` at the end to report a failed factorisation (not in the deferred
  * status mode, below: the status is then kept for gptq_status_sync). An entry of H's upper
  * triangle that is NaN or infinite is reported as NONFINITE (before any pivot check).
+ * For d > 128 the factorisation runs on two library-owned streams forked from and joined
+ * back to `stream`: one set per caller stream (up to 8 per device), so calls on different
+ * caller streams, with different workspaces, can run side by side on the GPU.
  * Errors: INVALID_ARG, WORKSPACE, NONFINITE, NOT_SPD, CUDA. */
 size_t gptq_prepare_workspace_bytes(int64_t d, int act_order);
 int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, float damp, int act_order,
@@ -259,7 +262,7 @@ const char* gptq_status_string(int status);
  * gptq_status_sync then reports it. The mode is process-wide. In deferred mode the
  * calls only enqueue work, so a sequence of them can be captured into a CUDA graph and
  * replayed (make one call of each kind before capturing: the first gptq_prepare on a
- * device creates the streams and events its two-stream schedule uses).
+ * caller stream creates the streams and events its two-stream schedule uses).
  * ------------------------------------------------------------------------------------ */
 enum { GPTQ_STATUS_SYNC = 0, GPTQ_STATUS_DEFERRED = 1 };
 /* Errors: INVALID_ARG (unknown mode). Host only. */

@@ -676,19 +676,42 @@ extern "C" size_t gptq_prepare_workspace_bytes(int64_t d, int act_order) {
 namespace gptq {
 namespace {
 
-// Streams and events for the two-stream factorisation, one set per device, created on
-// first use and kept for the life of the process. The mutex is held for the whole call, so
-// calls from several host threads on one device take the streams in turn.
+// Streams and events for the two-stream factorisation: one set per (device, caller stream)
+// (up to kSetsPerDevice per device; beyond that, caller streams share sets), created on
+// first use and kept for the life of the process. Calls on different caller streams run on
+// different sets, so their factorisations can overlap on the GPU; a set's mutex is held for
+// the whole call, so calls that share a set take its streams in turn (their work is then
+// ordered on the set's streams, which is still correct).
 constexpr int kChainSMs = 32;
 constexpr int kMaxPrepDevices = 64;
+constexpr int kSetsPerDevice = 8;
 struct PrepConcurrency {
     std::mutex mu;
+    cudaStream_t owner = nullptr;   // the caller stream this set serves
+    bool used = false;
     bool ready = false;
     cudaStream_t crit = nullptr, side = nullptr;
     cudaEvent_t fork = nullptr, trsm = nullptr, rest = nullptr, rest_far = nullptr, side_done[2] = {nullptr, nullptr},
                 far_done[2] = {nullptr, nullptr}, join_side = nullptr, join_crit = nullptr;
 };
-PrepConcurrency g_conc[kMaxPrepDevices];
+PrepConcurrency g_conc[kMaxPrepDevices][kSetsPerDevice];
+std::mutex g_conc_mu;   // guards the owner assignment of the sets
+
+// The set for caller stream s on device dev: the one it used before, else a free one, else
+// one shared by hash.
+PrepConcurrency& conc_for(int dev, cudaStream_t s) {
+    std::lock_guard<std::mutex> lk(g_conc_mu);
+    PrepConcurrency* sets = g_conc[dev];
+    for (int i = 0; i < kSetsPerDevice; ++i)
+        if (sets[i].used && sets[i].owner == s) return sets[i];
+    for (int i = 0; i < kSetsPerDevice; ++i)
+        if (!sets[i].used) {
+            sets[i].used = true;
+            sets[i].owner = s;
+            return sets[i];
+        }
+    return sets[(reinterpret_cast<uintptr_t>(s) >> 4) % kSetsPerDevice];
+}
 
 cudaError_t conc_init(PrepConcurrency& c) {
     if (c.ready) return cudaSuccess;
@@ -1013,7 +1036,7 @@ extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, fl
     GPTQ_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxPrepDevices || d <= NB)
         return prepare_impl(H, diag_xtx, d, damp, act_order, U, perm, dead, ws, ws_bytes, stream, nullptr);
-    PrepConcurrency& c = g_conc[dev];
+    PrepConcurrency& c = conc_for(dev, static_cast<cudaStream_t>(stream));
     std::lock_guard<std::mutex> lk(c.mu);
     if (conc_init(c) != cudaSuccess) {
         (void)cudaGetLastError();

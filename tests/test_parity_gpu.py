@@ -405,3 +405,35 @@ def test_stacked_weights_equal_per_weight_calls(lib):
     parts = runner.weight_outputs(0)
     assert [p["codes"].shape[0] for p in parts] == [W.shape[0] for W in L.Ws]
     assert all(bool(torch.isfinite(p["Wq"]).all()) for p in parts)
+
+
+def test_prepare_on_concurrent_streams_equals_sequential(lib):
+    """gptq_prepare calls on different caller streams get their own library stream sets and
+    run side by side on the GPU; each gives the result it gives alone, bit for bit (two
+    super-panel sizes and one small one, all three in flight at once)."""
+    cases = [(2176, True, 601), (2304, False, 602), (768, False, 603)]
+    inputs = []
+    for d, act, seed in cases:
+        H32, diag32, _ = _h_for(d, seed)
+        inputs.append((torch.tensor(H32, device=DEV), torch.tensor(diag32, device=DEV), act,
+                       torch.empty(lib.gptq_prepare_workspace_bytes(d, True), dtype=torch.uint8, device=DEV)))
+    ref = []
+    for H, diag, act, ws in inputs:
+        U, perm, dead = lib.gptq_prepare(H, diag, 0.01, act_order=act, ws=ws)
+        torch.cuda.synchronize()
+        ref.append((npy(U), npy(perm), npy(dead)))
+    streams = [torch.cuda.Stream() for _ in inputs]
+    outs = []
+    with lib.deferred_status():
+        for st, (H, diag, act, ws) in zip(streams, inputs):
+            st.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(st):
+                outs.append(lib.gptq_prepare(H, diag, 0.01, act_order=act, ws=ws))
+        for st in streams:
+            torch.cuda.current_stream().wait_stream(st)
+        lib.status_sync()
+    torch.cuda.synchronize()
+    for (U, perm, dead), (Ur, pr, dr) in zip(outs, ref):
+        np.testing.assert_array_equal(npy(U), Ur)
+        np.testing.assert_array_equal(npy(perm), pr)
+        np.testing.assert_array_equal(npy(dead), dr)
