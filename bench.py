@@ -58,8 +58,9 @@ def parse(argv=None):
     ap.add_argument("--bits", type=int, default=0, help="keep only the layers of this bit width")
     # the timed step's schedule: serial (group after group), prepare (all Hessians, then the
     # groups' gptq_prepare calls side by side, then the quantizations), groups (all
-    # Hessians, then each group's prepare and quantizations on its own stream)
-    ap.add_argument("--schedule", choices=["serial", "prepare", "groups"], default="groups")
+    # Hessians, then each group's prepare and quantizations on its own stream), layers (as
+    # groups, with each layer of a group quantised on a stream of its own)
+    ap.add_argument("--schedule", choices=["serial", "prepare", "groups", "layers"], default="layers")
     return ap.parse_args(argv)
 
 
@@ -253,16 +254,33 @@ class Runner:
                 nb = max(nb, lib.gptq_quantize_workspace_bytes(r, c, q.bits, q.group, q.sym))
             self.q_ws[id(g)] = torch.empty(nb, dtype=torch.uint8, device=device)
         self.gstreams = [torch.cuda.Stream(device=device) for _ in self.groups]
+        # per layer (made on first use by the layers schedule): a stream and a quantize
+        # workspace, so the layers of a group (the bit widths of one input) quantise side by side
+        self.lstreams = {}
+        self.q_ws_layer = {}
+
+    def _layer_res(self, li):
+        import torch
+        if li not in self.lstreams:
+            L = self.layers[li]
+            q = L.spec.q
+            r, c = L.Wcat.shape
+            self.q_ws_layer[li] = torch.empty(self.lib.gptq_quantize_workspace_bytes(r, c, q.bits, q.group, q.sym),
+                                              dtype=torch.uint8, device=self.dev)
+            self.lstreams[li] = torch.cuda.Stream(device=self.dev)
+        return self.lstreams[li], self.q_ws_layer[li]
 
     def step_concurrent(self, quantize_in_group: bool = True, Xs=None, Wcats=None, x_chunks=None, w_ready=None,
-                        layer_done=None, order=None):
+                        layer_done=None, order=None, fork_layers: bool = False):
         """One pass with the groups side by side: every group's Hessian on the current stream
         (each is a full-GPU kernel), then per group on its own stream, as soon as that group's
         Hessian is final (an event, not the whole Hessian queue), its gptq_prepare - the
         small groups' latency-bound factorisations overlap the large group's - followed, with
         quantize_in_group, by its gptq_quantize calls (else those run after all prepares, on
-        the current stream). The same calls and results as step(); Xs, Wcats, x_chunks,
-        w_ready, layer_done and order as there."""
+        the current stream). With fork_layers each layer of a group then quantises on a
+        stream and workspace of its own, forked from the group's stream after its prepare.
+        The same calls and results as step(); Xs, Wcats, x_chunks, w_ready, layer_done and
+        order as there."""
         import torch
         lib = self.lib
         main = torch.cuda.current_stream()
@@ -294,7 +312,7 @@ class Runner:
                 U, perm, dead = lib.gptq_prepare(H, diag, q0.damp, act_order=q0.act_order, ws=self.prep_ws[id(g)])
                 preps[gi] = (U, perm, dead)
                 if quantize_in_group:
-                    self._quantize_group(g, U, perm, dead, Wcats, w_ready, layer_done)
+                    self._quantize_group(g, U, perm, dead, Wcats, w_ready, layer_done, fork_layers)
         for st in self.gstreams:
             main.wait_stream(st)
         if not quantize_in_group:
@@ -302,18 +320,25 @@ class Runner:
                 self._quantize_group(self.groups[gi], *preps[gi], Wcats, w_ready, layer_done)
         return self.outs
 
-    def _quantize_group(self, g, U, perm, dead, Wcats=None, w_ready=None, layer_done=None):
+    def _quantize_group(self, g, U, perm, dead, Wcats=None, w_ready=None, layer_done=None, fork_layers=False):
         import torch
+        gst = torch.cuda.current_stream()
         for li in g:
             L = self.layers[li]
             Wcat = L.Wcat if Wcats is None else Wcats[li]
             q = L.spec.q
-            if w_ready is not None:
-                torch.cuda.current_stream().wait_event(w_ready[li])
-            self.lib.gptq_quantize(Wcat, U, perm, dead, q.bits, q.group, q.sym, ws=self.q_ws[id(g)],
-                                   out=self.outs[li])
-            if layer_done is not None:
-                layer_done[li].record()
+            st, ws = (self._layer_res(li) if fork_layers else (gst, self.q_ws[id(g)]))
+            if st is not gst:
+                st.wait_stream(gst)
+            with torch.cuda.stream(st):
+                if w_ready is not None:
+                    st.wait_event(w_ready[li])
+                self.lib.gptq_quantize(Wcat, U, perm, dead, q.bits, q.group, q.sym, ws=ws, out=self.outs[li])
+                if layer_done is not None:
+                    layer_done[li].record(st)
+        if fork_layers:
+            for li in g:
+                gst.wait_stream(self.lstreams[li])
 
     def weight_outputs(self, li):
         """The outputs of layer li split per weight (row blocks of the stacked outputs)."""
@@ -812,7 +837,8 @@ def run_ours(args, ws, rank, local):
     def run_step():
         if args.schedule == "serial":
             return runner.step()
-        return runner.step_concurrent(quantize_in_group=(args.schedule == "groups"))
+        return runner.step_concurrent(quantize_in_group=(args.schedule in ("groups", "layers")),
+                                      fork_layers=(args.schedule == "layers"))
 
     clocks = Clocks(local)
     clocks.start()
@@ -982,7 +1008,8 @@ def run_ours(args, ws, rank, local):
                         w_ready[li].record()
             kw = dict(Xs=dX, Wcats=dW, x_chunks=x_chunks, w_ready=w_ready, layer_done=layer_done, order=gorder)
             outs = (runner.step(**kw) if args.schedule == "serial"
-                    else runner.step_concurrent(quantize_in_group=(args.schedule == "groups"), **kw))
+                    else runner.step_concurrent(quantize_in_group=(args.schedule in ("groups", "layers")),
+                                                fork_layers=(args.schedule == "layers"), **kw))
             with torch.cuda.stream(d2h):
                 for gi in gorder:
                     for li in runner.groups[gi]:
@@ -1042,7 +1069,10 @@ def run_ours(args, ws, rank, local):
                          "prepare": "all Hessians, then every group's gptq_prepare side by side on its own stream, "
                                     "then the quantizations",
                          "groups": "all Hessians, then per group on its own stream its gptq_prepare and its "
-                                   "gptq_quantize calls, the groups side by side"}[args.schedule],
+                                   "gptq_quantize calls, the groups side by side",
+                         "layers": "all Hessians, then per group on its own stream its gptq_prepare, then each "
+                                   "of its layers' gptq_quantize on a stream of its own, all side by side"
+                         }[args.schedule],
             "clocks": ck, "gpu_launches": launches // max(1, args.steps) * args.steps,
             "gpu_launches_per_step": launches / max(1, args.steps), "wall_ms_timed_region": wall,
             "stages_ms": stages, "kernels": kernels, "roofline": roof, "e2e": e2e, "cpu_baseline": cpu,

@@ -21,13 +21,30 @@ def test_concurrent_schedules_equal_serial(lib):
     wl, layers = bench.build_layers(4, "cuda", wl=bench.workload_for(args))
     runner = bench.Runner(lib, layers, torch.device("cuda"))
     ref = _snap(runner.step())
-    for in_group in (False, True):
+    for in_group, fork in ((False, False), (True, False), (True, True)):
         with lib.deferred_status():
-            got = _snap(runner.step_concurrent(quantize_in_group=in_group))
+            got = _snap(runner.step_concurrent(quantize_in_group=in_group, fork_layers=fork))
             lib.status_sync()
         for li, (a, b) in enumerate(zip(got, ref)):
             for k in b:
-                np.testing.assert_array_equal(a[k], b[k], err_msg=f"layer {li} {k} (quantize_in_group={in_group})")
+                np.testing.assert_array_equal(a[k], b[k], err_msg=f"layer {li} {k} (in_group={in_group}, fork={fork})")
+
+
+def test_layer_fork_with_shared_input_equals_serial(lib):
+    """Two bit widths on each input: the layers of a group quantise on their own streams and
+    workspaces at the same time, against the same U; each gives its serial result."""
+    args = bench.parse(["--config", "4", "--x-tokens", "2048"])
+    wl, layers = bench.build_layers(4, "cuda", wl=bench.workload_for(args))
+    layers = [L for L in layers if L.spec.q.bits in (2, 4) and L.X.shape[1] == 4096]
+    runner = bench.Runner(lib, layers, torch.device("cuda"))
+    assert max(len(g) for g in runner.groups) == 2
+    ref = _snap(runner.step())
+    with lib.deferred_status():
+        got = _snap(runner.step_concurrent(quantize_in_group=True, fork_layers=True))
+        lib.status_sync()
+    for li, (a, b) in enumerate(zip(got, ref)):
+        for k in b:
+            np.testing.assert_array_equal(a[k], b[k], err_msg=f"layer {li} {k}")
 
 
 def test_schedules_with_copy_events_equal_serial(lib):
@@ -46,7 +63,7 @@ def test_schedules_with_copy_events_equal_serial(lib):
     w_ready = [torch.cuda.Event() for _ in layers]
     layer_done = [torch.cuda.Event() for _ in layers]
     order = list(reversed(range(len(runner.groups))))
-    for sched in ("serial", "prepare", "groups"):
+    for sched in ("serial", "prepare", "groups", "layers"):
         for x in dX:
             x.zero_()
         torch.cuda.synchronize()
@@ -62,7 +79,8 @@ def test_schedules_with_copy_events_equal_serial(lib):
         kw = dict(Xs=dX, Wcats=dW, x_chunks=x_chunks, w_ready=w_ready, layer_done=layer_done, order=order)
         with lib.deferred_status():
             outs = (runner.step(**kw) if sched == "serial"
-                    else runner.step_concurrent(quantize_in_group=(sched == "groups"), **kw))
+                    else runner.step_concurrent(quantize_in_group=(sched != "prepare"),
+                                                fork_layers=(sched == "layers"), **kw))
             for ev in layer_done:
                 ev.synchronize()
             got = _snap(outs)
