@@ -30,6 +30,11 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
+# The concurrent step runs ~25 streams (groups, layers, the factorisation's own streams).
+# With the runtime's default of 8 hardware work queues, streams share queues and unrelated
+# work waits behind each other; 32 (the maximum) gives each its own. Read when the CUDA
+# context is created, so set before any CUDA call of this process.
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
 
 METRIC = "GPTQ layer quantize time (ms, incl. H+Cholesky) and % of roofline per kernel"
 L2_BYTES = 129 * 1024 * 1024
@@ -903,8 +908,8 @@ def run_ours(args, ws, rank, local):
     long_region = sum(times) >= 1000.0
     stages, kernels, roof = {}, {}, None
     if not args.no_profile:
-        lib.gptq_profile_enable(True)
-        lib.gptq_profile_read()
+        # stage times from serial steps with events only between the calls (the library's
+        # per-launch profiling below would break programmatic dependent launch inside them)
         evs = []
         for _ in range(args.steps):
             if flush:
@@ -912,10 +917,19 @@ def run_ours(args, ws, rank, local):
             runner.step(events=evs)
             lib.status_sync()
         torch.cuda.synchronize()
-        lib.gptq_profile_enable(False)
-        prof = lib.gptq_profile_read()
         for name, idx in (("hessian", (0, 1)), ("prepare", (1, 2)), ("quantize", (2, 3))):
             stages[name] = sum(e[idx[0]].elapsed_time(e[idx[1]]) for e in evs) / args.steps
+        stages["serial_step"] = sum(e[0].elapsed_time(e[3]) for e in evs) / args.steps
+        lib.gptq_profile_enable(True)
+        lib.gptq_profile_read()
+        for _ in range(args.steps):
+            if flush:
+                flush_l2(fbuf)
+            runner.step()
+            lib.status_sync()
+        torch.cuda.synchronize()
+        lib.gptq_profile_enable(False)
+        prof = lib.gptq_profile_read()
         tot = sum(v[1] for v in prof.values())
         work = algorithmic(layers)
         for name, (cnt, t) in sorted(prof.items(), key=lambda kv: -kv[1][1]):

@@ -121,7 +121,11 @@ int gptq_hessian_destroy(gptq_hessian* h);
  * triangle that is NaN or infinite is reported as NONFINITE (before any pivot check).
  * For d > 128 the factorisation runs on two library-owned streams forked from and joined
  * back to `stream`: one set per caller stream (up to 8 per device), so calls on different
- * caller streams, with different workspaces, can run side by side on the GPU.
+ * caller streams, with different workspaces, can run side by side on the GPU. The chain
+ * stream has the device's greatest priority, the other the caller stream's priority. A
+ * caller running many such calls at once should raise CUDA_DEVICE_MAX_CONNECTIONS (up to
+ * 32) before its CUDA context is created: with the default 8 hardware queues, unrelated
+ * streams share queues and their work serialises.
  * Errors: INVALID_ARG, WORKSPACE, NONFINITE, NOT_SPD, CUDA. */
 size_t gptq_prepare_workspace_bytes(int64_t d, int act_order);
 int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, float damp, int act_order,

@@ -713,12 +713,17 @@ PrepConcurrency& conc_for(int dev, cudaStream_t s) {
     return sets[(reinterpret_cast<uintptr_t>(s) >> 4) % kSetsPerDevice];
 }
 
-cudaError_t conc_init(PrepConcurrency& c) {
+// The chain stream takes the device's greatest priority (its kernels are the critical path
+// of the call); the side stream takes the caller stream's priority, so a caller that runs
+// one factorisation ahead of other work (a high-priority stream) gets its bulk updates
+// ahead of that work too, and a default-priority caller gets the default.
+cudaError_t conc_init(PrepConcurrency& c, cudaStream_t caller) {
     if (c.ready) return cudaSuccess;
-    int least = 0, greatest = 0;
+    int least = 0, greatest = 0, pc = 0;
     cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e == cudaSuccess) e = cudaStreamGetPriority(caller, &pc);
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.crit, cudaStreamNonBlocking, greatest);
-    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.side, cudaStreamNonBlocking, least);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.side, cudaStreamNonBlocking, pc);
     cudaEvent_t* evs[] = {&c.fork,          &c.trsm,        &c.rest,        &c.rest_far,  &c.side_done[0],
                           &c.side_done[1], &c.far_done[0], &c.far_done[1], &c.join_side, &c.join_crit};
     for (cudaEvent_t* ev : evs)
@@ -1038,7 +1043,7 @@ extern "C" int gptq_prepare(const float* H, const float* diag_xtx, int64_t d, fl
         return prepare_impl(H, diag_xtx, d, damp, act_order, U, perm, dead, ws, ws_bytes, stream, nullptr);
     PrepConcurrency& c = conc_for(dev, static_cast<cudaStream_t>(stream));
     std::lock_guard<std::mutex> lk(c.mu);
-    if (conc_init(c) != cudaSuccess) {
+    if (conc_init(c, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         (void)cudaGetLastError();
         return GPTQ_ERR_CUDA;
     }
