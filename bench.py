@@ -8,6 +8,7 @@ every weight that shares the layer input. Inputs are seeded synthetic layers.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
   python bench.py --op dequant_matmul [--config C] [--tokens T]   (the stored-form consumer)
   python bench.py --op layerwise [--mlp mlp4096|toy]             (apply_layerwise on a synthetic MLP)
+  python bench.py --op quantize [--shape 4096x14336] [--bits B]   (the column loop alone)
 
 Prints one JSON line. `value` is milliseconds per layer pass (lower is better),
 device-timed with CUDA events, L2 flushed between steps when the inputs fit in it.
@@ -54,7 +55,8 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-profile", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager steps instead of CUDA-graph replays")
-    ap.add_argument("--op", choices=["layer", "dequant_matmul", "layerwise"], default="layer")
+    ap.add_argument("--op", choices=["layer", "dequant_matmul", "layerwise", "quantize"], default="layer")
+    ap.add_argument("--shape", default="4096x14336", help="rows x cols of --op quantize's weight stack")
     ap.add_argument("--mlp", default="mlp4096")
     ap.add_argument("--tokens", type=int, default=8192)
     # smaller cases of the same shapes (profiler captures that must stay within a few GB):
@@ -1230,6 +1232,57 @@ def run_dequant_matmul(args):
     }), flush=True)
 
 
+def run_quantize(args):
+    """gptq_quantize alone on a rows x cols weight stack (--shape) with a synthetic,
+    well-conditioned U (the loop's cost does not depend on U's values), bits --bits (else
+    4), groups of 128, symmetric. One JSON line: ms per call (device time, CUDA events).
+    The call's trailing updates are cols/128 - 1 launches of the 3xTF32 GEMM: per 512
+    columns three inside the super-block (K = 128), then one over all columns past it
+    (K = 512)."""
+    import torch
+    import post_weight_quantization_04_gb300 as lib
+    from post_weight_quantization_04_gb300 import build as B
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    B.build()
+    lib.load()
+    dev = torch.device("cuda", 0)
+    rows, cols = (int(v) for v in args.shape.lower().split("x"))
+    bits = args.bits or 4
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    W = (torch.randn(rows, cols, device=dev, generator=g) * 0.02).contiguous()
+    U = torch.triu(torch.randn(cols, cols, device=dev, generator=g) * (0.3 / cols ** 0.5), 1)
+    U += torch.diag(torch.rand(cols, device=dev, generator=g) + 0.5)
+    ws = torch.empty(lib.gptq_quantize_workspace_bytes(rows, cols, bits, 128, True), dtype=torch.uint8, device=dev)
+    out = None
+
+    def step():
+        nonlocal out
+        out = lib.gptq_quantize(W, U, None, None, bits, 128, True, ws=ws, out=out)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n0 = lib.gptq_launch_count()
+    times = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    print(json.dumps({
+        "metric": "gptq_quantize (ms per call)", "value": statistics.mean(times), "unit": "ms",
+        "higher_is_better": False, "steps": args.steps, "n_gpus": 1, "data": "synthetic",
+        "dtype": "f32 (trailing updates 3xTF32)",
+        "config": {"rows": rows, "cols": cols, "bits": bits, "group": 128, "sym": True},
+        "gpu_launches": lib.gptq_launch_count() - n0,
+    }), flush=True)
+
+
 def run_layerwise(args):
     """The layer-wise pipeline on a synthetic MLP: per layer H from the previous quantised
     layers' bf16 outputs, prepare, quantize, and the forward pass on the stored form. One
@@ -1291,6 +1344,9 @@ def main():
     elif args.op == "layerwise":
         if rank == 0:
             run_layerwise(args)
+    elif args.op == "quantize":
+        if rank == 0:
+            run_quantize(args)
     elif args.impl == "reference":
         run_reference(args, ws, rank)
     else:
