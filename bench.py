@@ -359,7 +359,7 @@ class Runner:
     def step(self, events=None, Xs=None, Wcats=None, x_chunks=None, w_ready=None, layer_done=None, order=None):
         """One pass over every layer: per group one Hessian pass and one gptq_prepare, then
         one gptq_quantize per layer; `events` collects (start, H done, U done, end) CUDA
-        events per group. For inputs copied in on another stream: the Hessian of group g
+        events per group, followed by (layer, event after its quantisation) per layer. For inputs copied in on another stream: the Hessian of group g
         accumulates x_chunks[g] = [(token rows of its input, event, first row), ...] chunk by chunk,
         each once its copy has landed; the step waits for w_ready[li] (layer li's weights)
         just before it uses them, and records layer_done[li] once layer li's outputs are
@@ -398,6 +398,10 @@ class Runner:
                                   out=self.outs[li])
                 if layer_done is not None:
                     layer_done[li].record()
+                if e:   # after each layer's quantisation: (layer, event)
+                    le = torch.cuda.Event(enable_timing=True)
+                    le.record()
+                    e.append((li, le))
             if e:
                 e[3].record()
                 events.append(e)
@@ -922,6 +926,33 @@ def run_ours(args, ws, rank, local):
         for name, idx in (("hessian", (0, 1)), ("prepare", (1, 2)), ("quantize", (2, 3))):
             stages[name] = sum(e[idx[0]].elapsed_time(e[idx[1]]) for e in evs) / args.steps
         stages["serial_step"] = sum(e[0].elapsed_time(e[3]) for e in evs) / args.steps
+        # per input group: H and U once, then each layer's quantisation; per bit width the
+        # quantisations summed, "fresh" (the H and U of its inputs counted again for it)
+        # and "amortised" (H and U shared over the bit widths that read the same inputs)
+        ng = len(runner.groups)
+        per_group, by_bits = [], {}
+        for gi, g in enumerate(runner.groups):
+            es = evs[gi::ng]
+            hp = [sum(e[a].elapsed_time(e[b]) for e in es) / args.steps for a, b in ((0, 1), (1, 2))]
+            qs = {}
+            for e in es:
+                prev = e[2]
+                for li, le in e[4:]:
+                    qs[li] = qs.get(li, 0.0) + prev.elapsed_time(le) / args.steps
+                    prev = le
+            per_group.append({"input": list(layers[g[0]].X.shape), "layers": [layers[li].names for li in g],
+                              "hessian": hp[0], "prepare": hp[1],
+                              "quantize": {str(layers[li].spec.q.bits) + "b " + "+".join(layers[li].names): qs[li]
+                                           for li in g}})
+            for bits in sorted({layers[li].spec.q.bits for li in g}):
+                mine = [li for li in g if layers[li].spec.q.bits == bits]
+                b = by_bits.setdefault(bits, {"quantize": 0.0, "fresh": 0.0, "amortised": 0.0})
+                qb = sum(qs[li] for li in mine)
+                b["quantize"] += qb
+                b["fresh"] += qb + hp[0] + hp[1]
+                b["amortised"] += qb + (hp[0] + hp[1]) * len(mine) / len(g)
+        stages["per_group"] = per_group
+        stages["per_bits"] = {str(k): v for k, v in sorted(by_bits.items())}
         lib.gptq_profile_enable(True)
         lib.gptq_profile_read()
         for _ in range(args.steps):
@@ -944,6 +975,11 @@ def run_ours(args, ws, rank, local):
                 ach = work[name] / sec / (1e12 if unit == "TFLOP/s" else 1e9)
                 kernels[name].update({"bound": bound, "achieved": ach, "peak": peak, "unit": unit,
                                       "frac": ach / peak, "peak_source": src})
+            if name == "gptq_block_kernel":
+                # the loop's sequential chain: time per column of the stacked weights (each
+                # call walks its columns once, all rows in parallel)
+                ncols = sum(L.Wcat.shape[1] for L in layers)
+                kernels[name]["ns_per_column"] = t / args.steps * 1e6 / ncols
         top = max(kernels.items(), key=lambda kv: kv[1]["ms_per_step"])[0] if kernels else None
         if top:
             k = kernels[top]
