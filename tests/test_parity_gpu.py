@@ -437,3 +437,36 @@ def test_prepare_on_concurrent_streams_equals_sequential(lib):
         np.testing.assert_array_equal(npy(U), Ur)
         np.testing.assert_array_equal(npy(perm), pr)
         np.testing.assert_array_equal(npy(dead), dr)
+
+
+def test_prepare_on_more_caller_streams_than_sets(lib):
+    """Eleven gptq_prepare calls in flight on eleven caller streams (more than the 8 stream
+    sets per device, so some calls share a set and take its streams in turn; three of the
+    callers are high-priority streams, whose factorisations' side streams take that
+    priority): each gives its sequential result bit for bit."""
+    sizes = [256, 384, 512, 640, 768, 256, 384, 512, 640, 768, 2176]
+    inputs = []
+    for i, d in enumerate(sizes):
+        H32, diag32, _ = _h_for(d, 700 + i)
+        inputs.append((torch.tensor(H32, device=DEV), torch.tensor(diag32, device=DEV), i % 2 == 0,
+                       torch.empty(lib.gptq_prepare_workspace_bytes(d, True), dtype=torch.uint8, device=DEV)))
+    ref = []
+    for H, diag, act, ws in inputs:
+        U, perm, dead = lib.gptq_prepare(H, diag, 0.01, act_order=act, ws=ws)
+        torch.cuda.synchronize()
+        ref.append((npy(U), npy(perm), npy(dead)))
+    streams = [torch.cuda.Stream(priority=-1 if i % 4 == 1 else 0) for i in range(len(inputs))]
+    outs = []
+    with lib.deferred_status():
+        for st, (H, diag, act, ws) in zip(streams, inputs):
+            st.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(st):
+                outs.append(lib.gptq_prepare(H, diag, 0.01, act_order=act, ws=ws))
+        for st in streams:
+            torch.cuda.current_stream().wait_stream(st)
+        lib.status_sync()
+    torch.cuda.synchronize()
+    for (U, perm, dead), (Ur, pr, dr) in zip(outs, ref):
+        np.testing.assert_array_equal(npy(U), Ur)
+        np.testing.assert_array_equal(npy(perm), pr)
+        np.testing.assert_array_equal(npy(dead), dr)
