@@ -432,13 +432,28 @@ def algorithmic(cfg_layers):
         # prepare: per 128-wide panel, potrf (Cholesky n^3/3 + inverse n^3/6 FMA), the panel
         # solve 2 m n^2, the lower SYRK 2 m(m+1)/2 n, the inverse's scale 2 n k n and
         # trailing update 2 m k n (k = columns filled so far)
+        # The factorisation's critical chain (class [chain]) computes per panel its solve
+        # and the rank update of the next panel's columns (lower part), with this panel's
+        # L21 inside a super-panel and with all its panels' at the super-panel's end; the
+        # rest of the same work is the side stream's (class [prepare]). The two add up to
+        # the total above: every product is computed once, by one of them.
+        spw = 4 * NB if d >= 2048 else NB
         for k0 in (range(0, d, NB) if first else ()):
             nb = min(NB, d - k0)
             m = d - k0 - nb
             ncols = k0 + nb
             add("potrf_diag_kernel", 2.0 * (nb ** 3 / 3 + nb ** 3 / 6))
-            add("tc_gemm_nt_kernel[prepare]", 2.0 * m * nb * nb + 2.0 * (m * (m + 1) / 2) * nb
-                + 2.0 * nb * ncols * nb + 2.0 * m * ncols * nb)
+            total = (2.0 * m * nb * nb + 2.0 * (m * (m + 1) / 2) * nb
+                     + 2.0 * nb * ncols * nb + 2.0 * m * ncols * nb)
+            chain = 0.0
+            if m > 0:
+                nn = min(NB, m)
+                sp0 = k0 // spw * spw
+                sp_end = min(d, sp0 + spw)
+                ks = (sp_end - sp0) if k0 + nb == sp_end else nb
+                chain = 2.0 * m * nb * nb + 2.0 * ks * (m * nn - nn * (nn - 1) / 2)
+            add("tc_gemm_nt_kernel[chain]", chain)
+            add("tc_gemm_nt_kernel[prepare]", total - chain)
             add("split_kernel", 12.0 * (m * nb + nb * ncols))
         for W in (L.Wcat,):   # one gptq_quantize per layer over the stacked weights
             r, c = W.shape
@@ -459,6 +474,7 @@ def algorithmic(cfg_layers):
 ROOF = {
     "hessian_tc_kernel": ("tensor", "TFLOP/s"),
     "tc_gemm_nt_kernel[prepare]": ("tensor-tf32x3", "TFLOP/s"),
+    "tc_gemm_nt_kernel[chain]": ("tensor-tf32x3", "TFLOP/s"),
     "tc_gemm_nt_kernel[trailing]": ("tensor-tf32x3", "TFLOP/s"),
     "sgemm_kernel[prepare]": ("alu", "TFLOP/s"),
     "sgemm_kernel[trailing]": ("alu", "TFLOP/s"),

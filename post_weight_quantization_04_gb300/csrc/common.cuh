@@ -31,7 +31,7 @@ namespace gptq {
 enum KernelId {
     K_HESS_TC, K_HESS_SIMT, K_FINALIZE, K_PREP_DIAG, K_PREP_PERM, K_PREP_GATHER, K_POTRF, K_SGEMM_PREP,
     K_EYE, K_SCATTER, K_INIT_WORK, K_ROW_PARAMS, K_BLOCK, K_SGEMM_TRAIL, K_G_IDX, K_PACK, K_RTN,
-    K_SPLIT, K_TC_PREP, K_TC_TRAIL, K_DEQUANT_MM, K_STATUS, K_COUNT
+    K_SPLIT, K_TC_PREP, K_TC_TRAIL, K_DEQUANT_MM, K_STATUS, K_TC_CHAIN, K_COUNT
 };
 void prof_begin(int id, cudaStream_t s);
 void prof_end(int id, cudaStream_t s);

@@ -892,7 +892,7 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
                 // the panel's split: for panel 0 here; for the others it was written by the
                 // previous panel's SYRK of these columns (its rows below the diagonal block)
                 if (kb == 0) GPTQ_CUDA_TRY(split_rows(K_SPLIT, P, d, (int)m, n, w.ahi, w.alo, NB, cs, true));
-                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, n, n, 1.0f, w.ahi, w.alo, lhi, llo, NB, 0.0f, P, d,
+                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_CHAIN, (int)m, n, n, 1.0f, w.ahi, w.alo, lhi, llo, NB, 0.0f, P, d,
                                          false, w.status, cs, l21));
                 GPTQ_CUDA_TRY(record(two ? conc->trsm : nullptr, cs));
                 // the next panel's columns; the side stream's updates wrote them too: inside
@@ -915,7 +915,7 @@ int prepare_impl(const float* H, const float* diag_xtx, int64_t d, float damp, i
                 const int ks = sp_last ? (int)SPW : n;
                 const float* sh = sp_last ? Ehi : Lhi;
                 const float* sl = sp_last ? Elo : Llo;
-                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_PREP, (int)m, nn, ks, -1.0f, sh, sl, sh, sl, (int)SPW, 1.0f,
+                GPTQ_CUDA_TRY(tc_gemm_nt(K_TC_CHAIN, (int)m, nn, ks, -1.0f, sh, sl, sh, sl, (int)SPW, 1.0f,
                                          w.A + (k0 + n) * d + k0 + n, d, true, w.status, cs, strip));
                 cs_k = true;
             } else {

@@ -48,6 +48,7 @@ const char* kNames[K_COUNT] = {
     "gptq_block_kernel",   "sgemm_kernel[trailing]", "g_idx_kernel",
     "pack_kernel",         "rtn_kernel",          "split_kernel",      "tc_gemm_nt_kernel[prepare]",
     "tc_gemm_nt_kernel[trailing]", "dequant_matmul_kernel", "merge_status_kernel",
+    "tc_gemm_nt_kernel[chain]",
 };
 
 }  // namespace
