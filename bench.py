@@ -31,11 +31,6 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
-# The concurrent step runs ~25 streams (groups, layers, the factorisation's own streams).
-# With the runtime's default of 8 hardware work queues, streams share queues and unrelated
-# work waits behind each other; 32 (the maximum) gives each its own. Read when the CUDA
-# context is created, so set before any CUDA call of this process.
-os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
 
 METRIC = "GPTQ layer quantize time (ms, incl. H+Cholesky) and % of roofline per kernel"
 L2_BYTES = 129 * 1024 * 1024
@@ -722,9 +717,17 @@ def oracle_stated_layer(cfg: int, wl, X, W, q, pool: "RowPool", token_frac: floa
     r_s = max(pool.procs, int(round(rows * row_frac)))
     Wh = synth.to_numpy_f64(W[:r_s])
     tq = pool.quantize(Wh, U, perm, dead, q)
+    # the same loop in this one process on a few rows (the P = 1 figure: ms per row)
+    k = min(8, r_s)
+    t3 = time.perf_counter()
+    O.gptq_quantize(Wh[:k], U, perm, dead, q.bits, q.group, q.sym)
+    p1_row = (time.perf_counter() - t3) / k
     th, tp = (t1 - t0) / (n_s / n), t2 - t1
+    pool_row = tq / r_s
     tq = tq * rows / r_s
-    comp = {"hessian": th * 1e3, "prepare": tp * 1e3, "quantize": tq * 1e3}
+    comp = {"hessian": th * 1e3, "prepare": tp * 1e3, "quantize": tq * 1e3,
+            "quantize_ms_per_row": {"processes": pool.procs, "pooled": pool_row * 1e3, "one_process": p1_row * 1e3,
+                                    "one_process_rows_timed": k}}
     return (th + tp + tq) * 1e3, comp
 
 
@@ -1380,6 +1383,11 @@ def run_layerwise(args):
 
 
 def main():
+    # The concurrent step runs ~25 streams (groups, layers, the factorisation's own
+    # streams). With the runtime's default of 8 hardware work queues, streams share queues
+    # and unrelated work waits behind each other; 32 (the maximum) gives each its own. Read
+    # when the CUDA context is created, so set before any CUDA call of this process.
+    os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
     args = parse()
     ws, rank, local = dist_info()
     if ws > 1:
