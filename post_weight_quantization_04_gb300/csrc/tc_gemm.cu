@@ -46,6 +46,9 @@ constexpr int G_BM = 128, G_BK = 32, G_THREADS = 192;
 #define GPTQ_GEMM_WIDE_KB 16
 #endif
 constexpr int kWideKB = GPTQ_GEMM_WIDE_KB;
+#ifndef GPTQ_GEMM_TM_INNER
+#define GPTQ_GEMM_TM_INNER 1
+#endif
 constexpr int G_BOX = G_BM * G_BK * 4;         // 16 KB: one 128 x 32 fp32 box (a C chunk)
 // KB: the K step of the operand ring in fp32 columns. 32 (128-byte rows, 128-byte swizzle);
 // or 16 (64-byte rows, 64-byte swizzle), which halves a stage so twice as many stages fit
@@ -83,6 +86,7 @@ struct GParams {
     int M, N, K;
     float alpha, beta;
     int tiles_m, tiles_n, ntiles, lower_only;
+    int tm_inner;   // full launches: tile rows vary fastest (a wave spans all of A)
     int bn;     // tile width in columns
     int* status;
     // optional TF32 split of the result: mode 1 hi[r][c], mode 2 (transposed) hi[c][r]
@@ -151,8 +155,13 @@ __host__ __device__ __forceinline__ int lower_tiles_in_row(int r, int bn, int ti
 // below it, row by row
 __device__ __forceinline__ void tile_of(const GParams& p, int t, int& tm, int& tn) {
     if (!p.lower_only) {
-        tm = t / p.tiles_n;
-        tn = t % p.tiles_n;
+        if (p.tm_inner) {
+            tm = t % p.tiles_m;
+            tn = t / p.tiles_m;
+        } else {
+            tm = t / p.tiles_n;
+            tn = t % p.tiles_n;
+        }
         return;
     }
     int r = 0;
@@ -792,6 +801,10 @@ cudaError_t tc_gemm_nt(int id, int M, int N, int K, float alpha, const float* Ah
     p.tiles_n = tw == 64 ? tn64 : tw == 256 ? tn256 : tn128;
     p.lower_only = lower_only ? 1 : 0;
     p.ntiles = tw == 64 ? nt64 : tw == 256 ? nt256 : nt128;
+    // The tiles a wave of CTAs runs together read all of the operand they span in the
+    // other direction: by rows, all of B (N x K) per wave; with tile rows innermost, all of
+    // A (M x K). The one read again wave after wave should be the smaller.
+    p.tm_inner = (!lower_only && M < N) ? GPTQ_GEMM_TM_INNER : 0;
     p.status = status;
     p.ohi = out.hi;
     p.olo = out.lo;
