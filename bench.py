@@ -481,8 +481,8 @@ ROOF = {
 }
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the current kernels
-# from the ncu captures summarised under profiles/ (hessian_tc_kernel_d4096_x262144.md,
-# hessian_tc_kernel_d14336_x16384.md); a kernel changed since its capture has no entry here.
+# from the ncu captures of the Hessian kernel summarised under profiles/ (d = 4096 on 262144
+# tokens, d = 14336 on 16384 tokens); a kernel changed since its capture has no entry here.
 # The d = 14336 launch of the decoder block is estimated from its 16384-token capture: its
 # reads (X re-streamed by each wave of tiles) scale with the tokens (x16), its writes (the
 # accumulator flushes into S, one per tile) do not. Per launch, as `achieved` is.
