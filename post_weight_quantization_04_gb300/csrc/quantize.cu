@@ -110,7 +110,6 @@ __global__ void __launch_bounds__(256) init_work_kernel(const float* __restrict_
         if (r >= rows) break;
         const float* src = W + r * cols;
         float v[4];
-#pragma unroll
         bool bad = false;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
