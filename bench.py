@@ -407,6 +407,38 @@ def flush_l2(buf):
     buf.zero_()
 
 
+def stage_breakdown(evs, groups, layers, steps: int):
+    """Per input group and per bit width from the events of serial steps (Runner.step's
+    `events`: per group and step, (start, H done, U done, end) then (layer, event after
+    its quantisation) per layer; the groups in order within each step). Per group: H and
+    U once, then each layer's quantisation; per bit width: its quantisations summed,
+    "fresh" (the H and U of its inputs counted again for it) and "amortised" (H and U
+    shared over the layers that read the same inputs). Milliseconds per step."""
+    ng = len(groups)
+    per_group, by_bits = [], {}
+    for gi, g in enumerate(groups):
+        es = evs[gi::ng]
+        hp = [sum(e[a].elapsed_time(e[b]) for e in es) / steps for a, b in ((0, 1), (1, 2))]
+        qs = {}
+        for e in es:
+            prev = e[2]
+            for li, le in e[4:]:
+                qs[li] = qs.get(li, 0.0) + prev.elapsed_time(le) / steps
+                prev = le
+        per_group.append({"input": list(layers[g[0]].X.shape), "layers": [layers[li].names for li in g],
+                          "hessian": hp[0], "prepare": hp[1],
+                          "quantize": {str(layers[li].spec.q.bits) + "b " + "+".join(layers[li].names): qs[li]
+                                       for li in g}})
+        for bits in sorted({layers[li].spec.q.bits for li in g}):
+            mine = [li for li in g if layers[li].spec.q.bits == bits]
+            b = by_bits.setdefault(bits, {"quantize": 0.0, "fresh": 0.0, "amortised": 0.0})
+            qb = sum(qs[li] for li in mine)
+            b["quantize"] += qb
+            b["fresh"] += qb + hp[0] + hp[1]
+            b["amortised"] += qb + (hp[0] + hp[1]) * len(mine) / len(g)
+    return per_group, {str(k): v for k, v in sorted(by_bits.items())}
+
+
 def algorithmic(cfg_layers):
     """Per-kernel-class algorithmic work for one step: fp32/bf16 FLOPs, or bytes for the
     memory-bound kernels (the unit is fixed per class in ROOF)."""
@@ -945,33 +977,7 @@ def run_ours(args, ws, rank, local):
         for name, idx in (("hessian", (0, 1)), ("prepare", (1, 2)), ("quantize", (2, 3))):
             stages[name] = sum(e[idx[0]].elapsed_time(e[idx[1]]) for e in evs) / args.steps
         stages["serial_step"] = sum(e[0].elapsed_time(e[3]) for e in evs) / args.steps
-        # per input group: H and U once, then each layer's quantisation; per bit width the
-        # quantisations summed, "fresh" (the H and U of its inputs counted again for it)
-        # and "amortised" (H and U shared over the bit widths that read the same inputs)
-        ng = len(runner.groups)
-        per_group, by_bits = [], {}
-        for gi, g in enumerate(runner.groups):
-            es = evs[gi::ng]
-            hp = [sum(e[a].elapsed_time(e[b]) for e in es) / args.steps for a, b in ((0, 1), (1, 2))]
-            qs = {}
-            for e in es:
-                prev = e[2]
-                for li, le in e[4:]:
-                    qs[li] = qs.get(li, 0.0) + prev.elapsed_time(le) / args.steps
-                    prev = le
-            per_group.append({"input": list(layers[g[0]].X.shape), "layers": [layers[li].names for li in g],
-                              "hessian": hp[0], "prepare": hp[1],
-                              "quantize": {str(layers[li].spec.q.bits) + "b " + "+".join(layers[li].names): qs[li]
-                                           for li in g}})
-            for bits in sorted({layers[li].spec.q.bits for li in g}):
-                mine = [li for li in g if layers[li].spec.q.bits == bits]
-                b = by_bits.setdefault(bits, {"quantize": 0.0, "fresh": 0.0, "amortised": 0.0})
-                qb = sum(qs[li] for li in mine)
-                b["quantize"] += qb
-                b["fresh"] += qb + hp[0] + hp[1]
-                b["amortised"] += qb + (hp[0] + hp[1]) * len(mine) / len(g)
-        stages["per_group"] = per_group
-        stages["per_bits"] = {str(k): v for k, v in sorted(by_bits.items())}
+        stages["per_group"], stages["per_bits"] = stage_breakdown(evs, runner.groups, layers, args.steps)
         lib.gptq_profile_enable(True)
         lib.gptq_profile_read()
         for _ in range(args.steps):

@@ -68,3 +68,35 @@ def test_shared_input_counts_its_hessian_and_factorisation_once():
         assert three[k] == pytest.approx(one[k])
     for k in ("gptq_block_kernel", "tc_gemm_nt_kernel[trailing]", "init_work_kernel"):
         assert three[k] == pytest.approx(3 * one[k])
+
+
+class _Ev:
+    """A stand-in for a CUDA event: a time stamp in ms."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def elapsed_time(self, other):
+        return other.t - self.t
+
+
+def test_stage_breakdown_per_group_and_bits():
+    # two groups: input A read by layers 0 (2 bits) and 1 (4 bits); input B by layer 2 (4
+    # bits). One step: A's H 10 ms, U 4 ms, quantisations 3 and 5 ms; B's H 20, U 6, q 7.
+    XA = types.SimpleNamespace(shape=(100, 64))
+    XB = types.SimpleNamespace(shape=(100, 32))
+
+    def lay(X, bits, name):
+        return types.SimpleNamespace(X=X, names=[name], spec=types.SimpleNamespace(q=types.SimpleNamespace(bits=bits)))
+
+    layers = [lay(XA, 2, "a2"), lay(XA, 4, "a4"), lay(XB, 4, "b4")]
+    groups = [[0, 1], [2]]
+    ev = lambda *ts: [_Ev(t) for t in ts]
+    a = ev(0, 10, 14, 22) + [(0, _Ev(17)), (1, _Ev(22))]
+    b = ev(22, 42, 48, 55) + [(2, _Ev(55))]
+    per_group, per_bits = bench.stage_breakdown([a, b], groups, layers, steps=1)
+    assert per_group[0]["hessian"] == 10 and per_group[0]["prepare"] == 4
+    assert per_group[0]["quantize"] == {"2b a2": 3, "4b a4": 5}
+    assert per_group[1]["quantize"] == {"4b b4": 7}
+    assert per_bits["2"] == {"quantize": 3, "fresh": 3 + 14, "amortised": 3 + 14 / 2}
+    assert per_bits["4"] == {"quantize": 12, "fresh": 12 + 14 + 26, "amortised": 12 + 14 / 2 + 26}
