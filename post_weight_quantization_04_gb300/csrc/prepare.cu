@@ -682,7 +682,10 @@ namespace {
 // different sets, so their factorisations can overlap on the GPU; a set's mutex is held for
 // the whole call, so calls that share a set take its streams in turn (their work is then
 // ordered on the set's streams, which is still correct).
-constexpr int kChainSMs = 32;
+#ifndef GPTQ_CHAIN_SMS
+#define GPTQ_CHAIN_SMS 32
+#endif
+constexpr int kChainSMs = GPTQ_CHAIN_SMS;
 constexpr int kMaxPrepDevices = 64;
 constexpr int kSetsPerDevice = 8;
 struct PrepConcurrency {
