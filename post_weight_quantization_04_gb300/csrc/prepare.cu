@@ -40,7 +40,10 @@ namespace {
 constexpr int NB = 128;  // panel width of the blocked factorisation
 // Panels per super-panel: from kDeferMinD on, the side stream's large rank updates are
 // deferred to the end of each super-panel of kSP panels and applied with K = kSP * NB.
-constexpr int kSP = 4;
+#ifndef GPTQ_PREP_SP
+#define GPTQ_PREP_SP 4
+#endif
+constexpr int kSP = GPTQ_PREP_SP;
 constexpr int64_t kDeferMinD = 2048;
 constexpr int64_t prep_spw(int64_t d) { return (d >= kDeferMinD ? kSP : 1) * (int64_t)NB; }
 
