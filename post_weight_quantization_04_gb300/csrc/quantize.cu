@@ -42,7 +42,10 @@ constexpr int QB = 128;  // column block width
 // own columns are updated after each block (K = 128); at its end everything past it, with
 // K = sb * 128. Wide weights take 8 (fewer passes over their long trailing matrix), the
 // others 4 (measured: 4096 x 14336 6.81 -> 6.60 ms with 8; 28672 x 4096 4.40 -> 4.54 ms).
-inline int super_blocks(int64_t cols) { return cols >= 8192 ? 8 : 4; }
+#ifndef GPTQ_QUANT_SB_WIDE
+#define GPTQ_QUANT_SB_WIDE 8
+#endif
+inline int super_blocks(int64_t cols) { return cols >= 8192 ? GPTQ_QUANT_SB_WIDE : 4; }
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
